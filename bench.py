@@ -1,0 +1,559 @@
+#!/usr/bin/env python3
+"""Benchmark of the CSA / HCA hybrid compressed attention hot path on B300.
+
+One step = one pass of the whole path over one batch: compress the block the step's tokens
+complete, score the entries with the FP4 indexer, select the top-k, and attend (CSA), or
+compress and attend densely (HCA); a layer-pair workload runs both layers. The default workload
+is the CSA decode step at 128K context (batch 16, 64 heads x 128, indexer 4 x 64 FP4, top-k 512,
+window 128); --config picks another one of the five synthetic workloads.
+
+Prints one JSON line (rank 0). Timing: W untimed warm-up steps, then K steps, each bracketed by
+CUDA events on the launch stream, with a 256 MB write between steps to flush the 126 MB L2
+(outside the events); barrier + synchronize around the timed loop; max over ranks.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same workload instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CSA/HCA decode tok/s + HBM GB/s at 128K-1M ctx; prefill TFLOP/s"
+DEFAULT_CONFIG = "csa_decode_128k"
+KERNEL_SOURCES = {
+    "indexer_mxf4": "indexer.cu", "topk": "topk.cu", "csa_attend": "attend.cu",
+    "hca_attend": "attend.cu", "lse_merge": "attend.cu", "compress": "compress.cu",
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
+    ap.add_argument("--quick", action="store_true",
+                    help="timed steps only (no profiling pass, e2e or CPU baseline); for ncu runs")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------------------------
+# algorithmic work per step (what the method must move / compute; intermediates excluded)
+# ----------------------------------------------------------------------------------------------
+def _vis(t, m, E):
+    return max(0, min(E, (t + 1) // m))
+
+
+def layer_work(s):
+    """Per-kernel algorithmic bytes and FLOPs of one step of one layer."""
+    B, Nq, H, d, m, W = s.B, s.Nq, s.H, s.d, s.m, s.W
+    E = s.E
+    row = 2 * d * 2                     # one K row + one V row, bf16
+    j0 = s.compress_begin // m
+    n_new = E - j0
+    k = {}
+    k["compress"] = dict(bytes=B * n_new * m * (row + 4) + B * n_new * row, flops=B * n_new * m * 4 * d)
+    qo = B * Nq * H * d * 2 * 2
+    sel_keys = 0
+    win_keys = 0
+    idx_bytes = 0
+    idx_flops = 0
+    top_bytes = 0
+    for i in range(Nq):
+        t = s.q_pos0 + i
+        nv = _vis(t, m, E)
+        win_keys += t - max(0, t - W + 1) + 1 if W > 0 else 0
+        if s.kind == "csa":
+            sel_keys += min(s.k, nv)
+            idx_flops += 2 * s.H_I * s.d_I * nv
+            top_bytes += nv * 2 + s.k * 4
+        else:
+            sel_keys += nv
+    if s.kind == "csa":
+        # keys are read once per query group (decode: once per sequence)
+        nv_max = _vis(s.q_pos0 + Nq - 1, m, E)
+        groups = 1 if Nq == 1 else math.ceil(Nq / max(1, 64 // (s.H_I * (s.d_I // 32))))
+        idx_bytes = B * groups * nv_max * (s.d_I // 2 + s.d_I // 32) + \
+            B * Nq * s.H_I * (s.d_I // 2 + s.d_I // 32)
+        k["indexer_mxf4"] = dict(bytes=idx_bytes, flops=B * idx_flops)
+        k["topk"] = dict(bytes=B * top_bytes, flops=0)
+    name = "csa_attend" if s.kind == "csa" else "hca_attend"
+    att_flops = B * 4 * H * d * (sel_keys + win_keys)
+    k[name] = dict(bytes=B * (sel_keys + win_keys) * row // (1 if Nq == 1 else 1) + qo,
+                   flops=att_flops)
+    return k
+
+
+def step_work(wl):
+    kernels = {}
+    for s in wl.layers:
+        for n, v in layer_work(s).items():
+            a = kernels.setdefault(n, dict(bytes=0, flops=0))
+            a["bytes"] += v["bytes"]
+            a["flops"] += v["flops"]
+    # unique bytes of the step: per-layer inputs read once + outputs
+    return kernels
+
+
+def units_per_step(wl):
+    if wl.mode == "decode":
+        return wl.layers[0].B * wl.layers[0].Nq, "tok/s"
+    return None, "TFLOP/s"
+
+
+# ----------------------------------------------------------------------------------------------
+# clocks sampled during the timed region (NVML, read-only)
+# ----------------------------------------------------------------------------------------------
+class ClockSampler:
+    REASONS = {
+        0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+        0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+        0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+    }
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.index, self.period = index, period_s
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        self._thr = None
+        self.ok = False
+
+    def __enter__(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:
+            return self
+        self._thr = threading.Thread(target=self._run, daemon=True)
+        self._thr.start()
+        return self
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thr:
+            self._thr.join()
+        return False
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                    "samples": len(self.samples)}
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons - {"gpu_idle"}), "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------------------------
+# native arm
+# ----------------------------------------------------------------------------------------------
+def setup_layer(s, seed, layer_id, dev):
+    import torch
+    import long_context_compressed_pooling_b300 as csa
+    from synth import generate_layer
+    x = generate_layer(s, seed, layer_id, device=dev)
+    kc = torch.empty((s.B, s.E, s.d), dtype=torch.bfloat16, device=dev)
+    vc = torch.empty_like(kc)
+    if s.compress_begin > 0:  # the context before this step is already in the entry cache
+        csa.compress(x["k_raw"], x["v_raw"], x["logits"], s.m, kc, vc, 0, s.compress_begin)
+    d = dict(x, m=s.m, W=s.W, q_pos0=s.q_pos0, compress_begin=s.compress_begin, k_cmp=kc,
+             v_cmp=vc, out=torch.empty_like(x["q"]))
+    if s.kind == "csa":
+        d["k"] = s.k
+        d["topk_idx"] = torch.empty((s.B, s.Nq, s.k), dtype=torch.int32, device=dev)
+        d["topk_cnt"] = torch.empty((s.B, s.Nq), dtype=torch.int32, device=dev)
+    return d
+
+
+def step_inputs(s, d):
+    """(name, device view) of the tensors a serving loop would upload for this step: the queries,
+    their indexer queries, and the raw rows / logits / index keys of the tokens the step appends."""
+    n_new = s.N - s.compress_begin
+    items = [("q", d["q"]), ("k_new", d["k_raw"][:, s.N - n_new:]), ("v_new", d["v_raw"][:, s.N - n_new:]),
+             ("w_new", d["logits"][:, s.N - n_new:])]
+    if s.kind == "csa":
+        j0 = s.compress_begin // s.m
+        items += [("qi_codes", d["qi_codes"]), ("qi_scales", d["qi_scales"]),
+                  ("ki_new", d["ki_codes"][:, j0:]), ("kis_new", d["ki_scales"][:, j0:])]
+    return items
+
+
+def kernel_sha(name):
+    src = os.path.join(ROOT, "long_context_compressed_pooling_b300", "csrc", KERNEL_SOURCES[name])
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic(name, workload):
+    """ncu DRAM bytes per launch recorded for this kernel and workload, if the kernel source
+    is unchanged since the capture."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            tab = json.load(f)
+        e = tab[workload][name]
+        if e.get("source_sha") == kernel_sha(name):
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), float(j["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def run_native(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    import long_context_compressed_pooling_b300 as csa
+    from synth import get_config
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = get_config(args.config)
+    seed = wl.seed + 1000 * rank           # every rank decodes its own sequences (weak scaling)
+    states = {s.kind: setup_layer(s, seed, li, dev) for li, s in enumerate(wl.layers)}
+    call = csa.PreparedLayerPair(states.get("csa"), states.get("hca"))
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # warm-up (also triggers every one-time set-up inside the library)
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    assert csa.device_status(reset=True) == 0, "device status flags after warm-up"
+
+    graph = None
+    if not args.no_graph:
+        try:
+            s = torch.cuda.Stream(device=dev)
+            s.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(s):
+                call()
+            torch.cuda.current_stream(dev).wait_stream(s)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                call()
+            graph.replay()
+            torch.cuda.synchronize()
+        except Exception as e:  # keep eager launches if capture is refused
+            graph = None
+            print(f"# CUDA graph capture unavailable, launching eagerly: {e}", file=sys.stderr)
+    step = graph.replay if graph is not None else call
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+
+    def timed_loop(fn):
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            ev0[i].record()
+            fn()
+            ev1[i].record()
+        torch.cuda.synchronize()
+        barrier()
+        return [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
+
+    with ClockSampler(local) as clk:
+        ms = timed_loop(step)
+    ms_step = statistics.mean(ms)
+    t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_step = float(t.item())
+    assert csa.device_status(reset=True) == 0, "device status flags after the timed loop"
+
+    units, unit = units_per_step(wl)
+    work = step_work(wl)
+    step_bytes = sum(v["bytes"] for v in work.values())
+    step_flops = sum(v["flops"] for v in work.values())
+    if units is not None:
+        value = units * world / (ms_step * 1e-3)
+    else:
+        value = step_flops * world / (ms_step * 1e-3) / 1e12
+
+    out = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": K,
+           "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded; random inputs of the workload's shapes and distributions)",
+           "config": {"workload": wl.name, "description": wl.description,
+                      "batch_per_gpu": wl.layers[0].B, "context": wl.layers[0].N,
+                      "l2": "flushed between timed steps (256 MB write outside the events)",
+                      "launch": "cuda_graph" if graph is not None else "eager",
+                      "parallelism": f"replicas x{world} (independent sequences per GPU)"},
+           "step_alg_bytes": step_bytes, "step_alg_gbs": step_bytes / (ms_step * 1e-3) / 1e9,
+           "step_alg_flops": step_flops}
+    if not args.quick:
+        # per-kernel device time: the same K steps again, each launch bracketed by events
+        csa.profiler_enable(True)
+        csa.profiler_collect(reset=True)
+        timed_loop(call)
+        prof = csa.profiler_collect(reset=True)
+        csa.profiler_enable(False)
+        hbm, bf16_burst, bf16_sus, src = measured_peaks()
+        kern = {}
+        for name, (launches, tot) in prof.items():
+            per = tot / max(1, launches)
+            w = work.get(name, dict(bytes=0, flops=0))
+            lpp = launches / K
+            kern[name] = {"launches_per_step": lpp, "ms_per_launch": per,
+                          "share": tot / max(1e-12, sum(v[1] for v in prof.values())),
+                          "alg_bytes_per_launch": w["bytes"] / max(lpp, 1e-9) if w["bytes"] else None}
+        dom = max(kern, key=lambda n: kern[n]["share"]) if kern else None
+        if dom is not None:
+            d = kern[dom]
+            ab = d["alg_bytes_per_launch"] or 0
+            achieved = ab / (d["ms_per_launch"] * 1e-3) / 1e9
+            out["roofline"] = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm,
+                               "unit": "GB/s", "frac": achieved / hbm,
+                               "traffic": load_traffic(dom, wl.name),
+                               "peak_source": f"{src} hbm_gbs (STREAM-style copy)"}
+        out["kernels"] = kern
+        out["gpu_launches"] = int(round(sum(v["launches_per_step"] for v in kern.values()) * K))
+    out["clocks"] = clk.summary()
+
+    if not args.no_e2e and not args.quick:
+        out["e2e"] = run_e2e(wl, states, call, flush, K, dev, world, barrier)
+    if not args.no_cpu_baseline and not args.quick and rank == 0 and world == 1:
+        out["cpu_baseline"] = cpu_baseline(wl, states, budget_s=12.0)
+    return out
+
+
+def run_e2e(wl, states, call, flush, K, dev, world, barrier):
+    """Same metric through the public API with host buffers: every step uploads its inputs from
+    pinned host memory, runs the layer pair, and reads the outputs back."""
+    import torch
+    import torch.distributed as dist
+    ups, downs = [], []
+    for s in wl.layers:
+        d = states[s.kind]
+        for name, view in step_inputs(s, d):
+            host = torch.empty(view.shape, dtype=view.dtype, pin_memory=True)
+            host.copy_(view)
+            ups.append((view, host))
+        o = d["out"]
+        downs.append((o, torch.empty(o.shape, dtype=o.dtype, pin_memory=True)))
+    h2d = sum(h.numel() * h.element_size() for _, h in ups)
+    d2h = sum(h.numel() * h.element_size() for _, h in downs)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        e0[i].record()
+        for dv, h in ups:
+            dv.copy_(h, non_blocking=True)
+        call()
+        for dv, h in downs:
+            h.copy_(dv, non_blocking=True)
+        e1[i].record()
+    torch.cuda.synchronize()
+    barrier()
+    ms = statistics.mean(e0[i].elapsed_time(e1[i]) for i in range(K))
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    units, unit = units_per_step(wl)
+    work = step_work(wl)
+    if units is not None:
+        v = units * world / (ms * 1e-3)
+    else:
+        v = sum(w["flops"] for w in work.values()) * world / (ms * 1e-3) / 1e12
+    return {"value": v, "unit": unit, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "api": "csa_hca_layer_pair (eager launches)"}
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU oracle (baseline leg and reference arm)
+# ----------------------------------------------------------------------------------------------
+def raw_lo(s):
+    """First raw token a decode step reads: the start of the window or of the blocks the step
+    compresses, whichever is earlier."""
+    t = s.q_pos0
+    return max(0, min(s.compress_begin, t - s.W + 1 if s.W > 0 else t))
+
+
+def oracle_decode_sequence(s, seq):
+    """One decode step of one sequence with the fp64 oracle: pool the block the step completes,
+    score every visible entry, select the top-k and attend (CSA); or pool and attend densely
+    (HCA). `seq` holds numpy arrays of that sequence (bf16 as uint16 bits); its raw rows and
+    logits start at token seq["lo"]."""
+    import oracle as O
+    lo = seq["lo"]
+    t = s.q_pos0 - lo
+    E = s.E
+    kc, vc = seq["k_cmp"], seq["v_cmp"]
+    j0 = s.compress_begin // s.m
+    kr, vr = O.bf16_to_f64(seq["k_raw"]), O.bf16_to_f64(seq["v_raw"])
+    c0 = s.compress_begin - lo
+    kc[j0:] = O.compress(kr[c0:], seq["logits"][c0:], s.m)
+    vc[j0:] = O.compress(vr[c0:], seq["logits"][c0:], s.m)
+    q = O.bf16_to_f64(seq["q"][0])
+    nv = O.visible_entries(s.q_pos0, s.m, E)
+    if s.kind == "csa":
+        sc = O.index_scores(seq["qi_codes"][0], seq["qi_scales"][0], seq["ki_codes"][:nv],
+                            seq["ki_scales"][:nv], s.d_I)
+        idx, cnt = O.topk_select(O.f64_to_bf16_rne(sc), nv, s.k)
+        return O.csa_attend_one(q, kc, vc, idx, cnt, kr, vr, t, s.W)
+    return O.hca_attend_one(q, kc, vc, nv, kr, vr, t, s.W)
+
+
+def _host_sequence(s, d, b):
+    import numpy as np
+    import oracle as O
+    from synth.workloads import bf16_bits
+    lo = raw_lo(s)
+    seq = {"lo": lo, "q": bf16_bits(d["q"][b]), "k_raw": bf16_bits(d["k_raw"][b, lo:]),
+           "v_raw": bf16_bits(d["v_raw"][b, lo:]),
+           "logits": d["logits"][b, lo:].cpu().numpy().astype(np.float64),
+           "k_cmp": O.bf16_to_f64(bf16_bits(d["k_cmp"][b])),
+           "v_cmp": O.bf16_to_f64(bf16_bits(d["v_cmp"][b]))}
+    if s.kind == "csa":
+        for n in ("qi_codes", "qi_scales", "ki_codes", "ki_scales"):
+            seq[n] = d[n][b].cpu().numpy()
+    return seq
+
+
+def cpu_baseline(wl, states, budget_s=12.0):
+    """The oracle as it stands, one thread, on as many sequences of the workload as fit the
+    budget (at least one); throughput is scaled to the metric's unit."""
+    from threadpoolctl import threadpool_limits
+    if wl.mode != "decode":
+        return {"value": None, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                "sample": "prefill workloads: see --impl reference"}
+    B = wl.layers[0].B
+    done = 0
+    elapsed = 0.0
+    with threadpool_limits(1):
+        while elapsed < budget_s and done < 4 * B:
+            b = done % B
+            seqs = [(s, _host_sequence(s, states[s.kind], b)) for s in wl.layers]
+            t0 = time.perf_counter()
+            for s, seq in seqs:
+                oracle_decode_sequence(s, seq)
+            elapsed += time.perf_counter() - t0
+            done += 1
+    return {"value": done / elapsed, "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} sequence decode steps of {wl.name} (one token each, "
+                      f"all layers of the workload), {elapsed:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The fp64 oracle timed on the host cores: each step decodes one sequence of the workload."""
+    import numpy as np
+    import torch
+    from threadpoolctl import threadpool_limits
+    import oracle as O
+    from synth import get_config, generate_layer
+    if rank != 0:
+        return None
+    wl = get_config(args.config)
+    if wl.mode != "decode":
+        return {"impl": "reference", "unavailable": "the reference arm times decode workloads only"}
+    seqs = []
+    for li, s in enumerate(wl.layers):
+        x = generate_layer(s.scaled(B=1), wl.seed, li, device="cpu")
+        kr = O.bf16_to_f64(x["k_raw"][0].view(torch.int16).numpy().view(np.uint16))
+        vr = O.bf16_to_f64(x["v_raw"][0].view(torch.int16).numpy().view(np.uint16))
+        w = x["logits"][0].numpy().astype(np.float64)
+        lo = raw_lo(s)
+        seq = {"lo": lo, "q": x["q"][0].view(torch.int16).numpy().view(np.uint16),
+               "k_raw": x["k_raw"][0, lo:].view(torch.int16).numpy().view(np.uint16),
+               "v_raw": x["v_raw"][0, lo:].view(torch.int16).numpy().view(np.uint16),
+               "logits": w[lo:], "k_cmp": O.compress(kr, w, s.m), "v_cmp": O.compress(vr, w, s.m)}
+        if s.kind == "csa":
+            for n in ("qi_codes", "qi_scales", "ki_codes", "ki_scales"):
+                seq[n] = x[n][0].numpy()
+        seqs.append((s, seq))
+    with threadpool_limits(1):
+        for _ in range(max(1, args.warmup)):
+            for s, seq in seqs:
+                oracle_decode_sequence(s, seq)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            for s, seq in seqs:
+                oracle_decode_sequence(s, seq)
+        el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    v = 1.0 / (ms * 1e-3)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "description": wl.description,
+                                            "sample": "one sequence per step"},
+            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} steps x one {wl.name} sequence"},
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    out = run_native(args, rank, world)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,212 @@
+/*
+ * csa.h -- C ABI of the B300 (sm_103a) CSA / HCA hybrid compressed attention library.
+ *
+ * The method (DeepSeek-V4 hybrid attention as described by the Lighthouse page "deep deepseek
+ * v4 release", section 八.3, and the 9fzt.com DeepSeek-V4 summary, items 1 and 4):
+ *   CSA  every m = 4 consecutive KV tokens are pooled into one compressed entry; a Lightning
+ *        Indexer with an FP4 QK path scores the entries (scores rounded to BF16); a per-query
+ *        top-k keeps k entries; attention runs over the kept entries plus a sliding window of
+ *        n_win raw tokens.
+ *   HCA  every m' = 128 tokens are pooled into one entry; attention is dense over all visible
+ *        entries plus the same window.
+ * The two layer types alternate along depth (elebank "DeepSeek-V4 explained", 模型創新 1).
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers, row-major and contiguous, 16-byte aligned.
+ *     The caller owns every buffer; the library never allocates device memory on these paths.
+ *   - bf16 values travel as uint16_t bit patterns. `stream` is a cudaStream_t passed as void*
+ *     (NULL = the legacy default stream). Every call is asynchronous on `stream`.
+ *   - FP4 vectors are e2m1 codes packed two per byte, the low nibble holding the even element;
+ *     each run of 32 elements has one UE8M0 scale byte s meaning 2^(s-127) (OCP MX v1.0).
+ *   - Positions: the queries of a sequence sit at token positions q_pos0 .. q_pos0+Nq-1 of a
+ *     context of N tokens (q_pos0 + Nq <= N). A query at position t sees compressed entry j iff
+ *     (j+1)*m - 1 <= t, and the raw window tokens max(0, t-W+1) .. t. Entries and window tokens
+ *     form one softmax (no de-duplication); logits are q.k with no extra scale.
+ *   - Errors: arguments are validated before anything is launched and a CSA_ERR_* code is
+ *     returned without side effects. A failed launch returns CSA_ERR_CUDA. Kernels never trap:
+ *     an out-of-range top-k index or an expired bounded wait is recorded in a device status
+ *     word that csa_get_device_status() reads. Shapes the kernels do not implement return
+ *     CSA_ERR_UNSUPPORTED (there is no fallback path).
+ */
+#ifndef CSA_B300_H
+#define CSA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum csa_status {
+  CSA_OK = 0,
+  CSA_ERR_INVALID_ARG = 1,  /* null pointer, negative or zero size where one is required */
+  CSA_ERR_SHAPE = 2,        /* sizes inconsistent with each other */
+  CSA_ERR_ALIGN = 3,        /* a pointer is not 16-byte aligned */
+  CSA_ERR_WORKSPACE = 4,    /* workspace pointer null or smaller than the *_workspace_size() */
+  CSA_ERR_UNSUPPORTED = 5,  /* a shape outside the implemented set (see each call) */
+  CSA_ERR_CUDA = 6,         /* a CUDA runtime call or kernel launch failed */
+  CSA_ERR_DEVICE = 7        /* csa_get_device_status: a kernel recorded a fault (see below) */
+} csa_status;
+
+/* Device status bits (csa_get_device_status() returns CSA_ERR_DEVICE when any is set). */
+#define CSA_DEVFLAG_BAD_INDEX 0x1u  /* a top-k index outside [0, E) or a count above k/visible */
+#define CSA_DEVFLAG_TIMEOUT   0x2u  /* a bounded mbarrier wait expired; the kernel returned */
+
+/* ----------------------------------------------------------------------------------------
+ * csa_compress -- block pooling (CSA m=4, HCA m=128).
+ * Lighthouse "deep deepseek v4 release" 八.3 (m = 4 / m' = 128 tokens into one entry);
+ * the pooling operator is a softmax over the block's per-token logits:
+ *   p_i = softmax_i(logits[jm+i]),  k_cmp[j] = sum_i p_i k_raw[jm+i],  v_cmp[j] likewise.
+ *   k_raw, v_raw : [B, N, d] bf16          logits : [B, N] fp32
+ *   k_cmp, v_cmp : [B, N/m, d] bf16 (entry cache, written in place)
+ * Writes the entries j with tok_begin <= j*m and (j+1)*m <= tok_end; other entries are left
+ * untouched. tok_begin must be a multiple of m; 0 <= tok_begin <= tok_end <= N.
+ * Accumulation is fp32 (expf), entries are rounded to bf16 (round-to-nearest-even).
+ * Supported: d in {64, 128, 256}, m a power of two in [1, 256]. k_cmp may equal v_cmp only
+ * if k_raw equals v_raw.
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_compress(const uint16_t* k_raw, const uint16_t* v_raw, const float* logits,
+                        int B, int64_t N, int d, int m, int64_t tok_begin, int64_t tok_end,
+                        uint16_t* k_cmp, uint16_t* v_cmp, void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * csa_index_topk -- Lightning Indexer scores + per-query top-k.
+ * 9fzt.com DeepSeek-V4 summary item 4 (FP4 indexer QK path; index scores rounded from FP32 to
+ * BF16), Lighthouse 八.3 (top-k over compressed entries), 八.7 (the indexer keeps its own
+ * compressed keys).
+ *   s[b,i,j] = bf16_rne( sum_h max(0, q_I[b,i,h] . k_I[b,j]) ) for visible j
+ * with FP4 values times per-32 UE8M0 scales. When every scale byte lies in [123, 127] and
+ * d_I <= 64, H_I <= 4, the fp32 sum is exact, so the bf16 scores are exact.
+ *   qi_codes  [B, Nq, H_I, d_I/2] u8     qi_scales [B, Nq, H_I, d_I/32] u8
+ *   ki_codes  [B, E, d_I/2] u8           ki_scales [B, E, d_I/32] u8
+ *   topk_idx  [B, Nq, k] int32 out: the min(k, visible) entries with the largest score, ties
+ *             to the lower index, sorted ascending, padded with -1
+ *   topk_cnt  [B, Nq] int32 out: min(k, visible)
+ *   scores    optional [B, Nq, E] bf16 out (NULL: kept in the workspace). Only visible
+ *             entries are written.
+ * The scores are computed on the tensor cores (tcgen05 FP4 MMA, fp32 accumulators in tensor
+ * memory). Supported: d_I in {32, 64}, H_I in {1, 2, 4, 8}, k >= 1, scale bytes in [1, 254].
+ * Workspace: csa_index_topk_workspace_size().
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
+                          const uint8_t* ki_codes, const uint8_t* ki_scales,
+                          int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I, int d_I,
+                          int k, int32_t* topk_idx, int32_t* topk_cnt, uint16_t* scores,
+                          void* ws, size_t ws_bytes, void* stream);
+size_t csa_index_topk_workspace_size(int B, int Nq, int64_t E, int k, int scores_given);
+
+/* ----------------------------------------------------------------------------------------
+ * csa_topk -- the top-k selector alone, over caller-provided BF16 scores [B, Nq, E]
+ * (9fzt.com item 4: the selector works on BF16 index scores). Same outputs and tie rule as
+ * csa_index_topk. -0 counts as +0; NaN scores are not supported.
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
+                    int k, int32_t* topk_idx, int32_t* topk_cnt,
+                    void* ws, size_t ws_bytes, void* stream);
+size_t csa_topk_workspace_size(int B, int Nq, int64_t E, int k);
+
+/* ----------------------------------------------------------------------------------------
+ * csa_attend -- CSA attention over the selected entries plus the sliding window.
+ * Lighthouse 八.3 (sparse attention over the top-k compressed blocks, plus a sliding-window
+ * branch of n_win raw tokens).
+ *   out[b,i,h] = sum_n softmax_n(q[b,i,h] . key_n) value_n over
+ *   {k_cmp[b, topk_idx[b,i,r]] : r < topk_cnt[b,i]}  +  {k_raw[b,u] : u in window(t)}
+ *   q [B, Nq, H, d] bf16 (1/sqrt(d) already folded in), k_cmp/v_cmp [B, E, d] bf16,
+ *   k_raw/v_raw [B, N, d] bf16, out [B, Nq, H, d] bf16, lse optional [B, Nq, H] fp32
+ *   (natural log of the softmax denominator; -inf and out = 0 for an empty key set).
+ * Indices outside [0, E) are skipped and flagged (CSA_DEVFLAG_BAD_INDEX).
+ * Supported: d in {64, 128}, 1 <= H <= 128, 0 <= W, 0 <= k.
+ * Workspace: csa_attend_workspace_size() (split-K partials for small batches).
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_attend(const uint16_t* q, const uint16_t* k_cmp, const uint16_t* v_cmp, int64_t E,
+                      const int32_t* topk_idx, const int32_t* topk_cnt, int k,
+                      const uint16_t* k_raw, const uint16_t* v_raw, int64_t N, int W,
+                      int B, int Nq, int64_t q_pos0, int H, int d,
+                      uint16_t* out, float* lse, void* ws, size_t ws_bytes, void* stream);
+size_t csa_attend_workspace_size(int B, int Nq, int H, int d, int k, int W);
+
+/* ----------------------------------------------------------------------------------------
+ * hca_attend -- HCA dense attention over every visible entry plus the sliding window.
+ * Lighthouse 八.3 (m' = 128, dense attention, no top-k). Same tensors as csa_attend without
+ * the top-k lists; m is the block size that defines entry visibility.
+ * ---------------------------------------------------------------------------------------- */
+csa_status hca_attend(const uint16_t* q, const uint16_t* k_cmp, const uint16_t* v_cmp, int64_t E,
+                      int m, const uint16_t* k_raw, const uint16_t* v_raw, int64_t N, int W,
+                      int B, int Nq, int64_t q_pos0, int H, int d,
+                      uint16_t* out, float* lse, void* ws, size_t ws_bytes, void* stream);
+size_t hca_attend_workspace_size(int B, int Nq, int H, int d, int64_t E, int m, int W);
+
+/* ----------------------------------------------------------------------------------------
+ * csa_hca_layer_pair -- one CSA layer followed by one HCA layer (they alternate along depth:
+ * Lighthouse 八.3, elebank 模型創新 1). Each layer: compress the blocks of tokens
+ * [compress_begin, N) into its entry cache, then (CSA) index + top-k and attend, or (HCA)
+ * attend densely. The two layers get independent inputs; either descriptor may be NULL.
+ * Fields follow the single calls above.
+ * ---------------------------------------------------------------------------------------- */
+typedef struct csa_layer_desc {
+  const uint16_t* q;            /* [B, Nq, H, d] */
+  const uint16_t* k_raw;        /* [B, N, d] */
+  const uint16_t* v_raw;        /* [B, N, d] */
+  const float* logits;          /* [B, N] */
+  const uint8_t* qi_codes;      /* [B, Nq, H_I, d_I/2] */
+  const uint8_t* qi_scales;     /* [B, Nq, H_I, d_I/32] */
+  const uint8_t* ki_codes;      /* [B, N/m, d_I/2] */
+  const uint8_t* ki_scales;     /* [B, N/m, d_I/32] */
+  uint16_t* k_cmp;              /* [B, N/m, d] entry cache (in/out) */
+  uint16_t* v_cmp;              /* [B, N/m, d] entry cache (in/out) */
+  uint16_t* out;                /* [B, Nq, H, d] */
+  float* lse;                   /* optional [B, Nq, H] */
+  int32_t* topk_idx;            /* [B, Nq, k] */
+  int32_t* topk_cnt;            /* [B, Nq] */
+  uint16_t* scores;             /* optional [B, Nq, N/m] */
+  int B, Nq, H, d, m, W, k, H_I, d_I;
+  int64_t N, q_pos0, compress_begin;
+} csa_layer_desc;
+
+typedef struct hca_layer_desc {
+  const uint16_t* q;
+  const uint16_t* k_raw;
+  const uint16_t* v_raw;
+  const float* logits;
+  uint16_t* k_cmp;              /* [B, N/m, d] */
+  uint16_t* v_cmp;
+  uint16_t* out;
+  float* lse;                   /* optional */
+  int B, Nq, H, d, m, W;
+  int64_t N, q_pos0, compress_begin;
+} hca_layer_desc;
+
+csa_status csa_hca_layer_pair(const csa_layer_desc* csa, const hca_layer_desc* hca,
+                              void* ws, size_t ws_bytes, void* stream);
+size_t csa_hca_layer_pair_workspace_size(const csa_layer_desc* csa, const hca_layer_desc* hca);
+
+/* ----------------------------------------------------------------------------------------
+ * Status.
+ * csa_get_device_status synchronises `stream`, reads the device status word of the current
+ * device and returns CSA_OK, CSA_ERR_DEVICE (flags in *flags_out when non-NULL) or
+ * CSA_ERR_CUDA; reset != 0 clears the word afterwards.
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_get_device_status(void* stream, int reset, uint32_t* flags_out);
+
+/* ----------------------------------------------------------------------------------------
+ * Per-kernel timing (tracing aid; no counterpart on the pages). While enabled, every kernel
+ * launch of the library is bracketed by two CUDA events recorded on its launch stream.
+ * csa_profiler_collect synchronises those events and returns, per kernel name, the number of
+ * launches and their summed device time; reset != 0 clears the records. At most 32768 launches
+ * are recorded between resets; later ones are not timed.
+ * ---------------------------------------------------------------------------------------- */
+typedef struct csa_kernel_time {
+  char name[32];
+  int launches;
+  double total_ms;
+} csa_kernel_time;
+csa_status csa_profiler_enable(int on);
+csa_status csa_profiler_collect(csa_kernel_time* out, int max_entries, int* n_entries, int reset);
+const char* csa_status_string(csa_status s);
+int csa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA_B300_H */

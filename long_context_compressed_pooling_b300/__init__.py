@@ -1,0 +1,26 @@
+"""CSA / HCA hybrid compressed attention for B300 (sm_103a).
+
+Thin Python binding over the C ABI of include/csa.h (libcsa_b300.so, built in-tree by
+`python -m long_context_compressed_pooling_b300.build`). It only marshals torch tensors into
+pointers and sizes, allocates workspaces with torch, and passes torch's current CUDA stream;
+every step of the computation runs in the library's CUDA kernels. Importing the package fails
+loudly when the library is missing: there is no CPU or fallback path.
+"""
+from ._native import (  # noqa: F401
+    CSA_OK,
+    CsaError,
+    LIB_PATH,
+    PreparedLayerPair,
+    compress,
+    csa_attend,
+    device_status,
+    exported_symbols,
+    hca_attend,
+    index_topk,
+    layer_pair,
+    load_library,
+    profiler_collect,
+    profiler_enable,
+    topk,
+    workspace_sizes,
+)

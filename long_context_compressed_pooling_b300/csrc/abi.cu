@@ -1,0 +1,348 @@
+// extern "C" entry points of include/csa.h: argument validation, launch planning, TMA
+// descriptor encoding and the CSA/HCA layer-pair driver. No entry point allocates device
+// memory; scratch lives in the caller's workspace.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/csa.h"
+#include "kernels.h"
+
+using namespace csa;
+
+namespace {
+
+// Device status word (CSA_DEVFLAG_*), one per device that loads the library.
+__device__ uint32_t g_device_status;
+
+constexpr int kMaxDevices = 64;
+uint32_t* g_status_ptr[kMaxDevices] = {};
+std::mutex g_mu;
+
+uint32_t* status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+csa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---- validation of each call's arguments (no CUDA call is made before these pass) ----------
+csa_status check_compress(const uint16_t* k_raw, const uint16_t* v_raw, const float* logits,
+                          int B, int64_t N, int d, int m, int64_t tok_begin, int64_t tok_end,
+                          uint16_t* k_cmp, uint16_t* v_cmp) {
+  if (!k_raw || !v_raw || !logits || !k_cmp || !v_cmp) return CSA_ERR_INVALID_ARG;
+  if (!al16(k_raw) || !al16(v_raw) || !al16(k_cmp) || !al16(v_cmp) || (uintptr_t)logits % 4)
+    return CSA_ERR_ALIGN;
+  if (B < 1 || N < 1 || m < 1) return CSA_ERR_INVALID_ARG;
+  if (tok_begin < 0 || tok_end < tok_begin || tok_end > N || tok_begin % m != 0)
+    return CSA_ERR_SHAPE;
+  if (d != 64 && d != 128 && d != 256) return CSA_ERR_UNSUPPORTED;
+  if (m > 256 || (m & (m - 1)) != 0) return CSA_ERR_UNSUPPORTED;
+  if (k_cmp == v_cmp && k_raw != v_raw) return CSA_ERR_INVALID_ARG;
+  return CSA_OK;
+}
+
+csa_status check_index(const uint8_t* qi_codes, const uint8_t* qi_scales,
+                       const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
+                       int64_t q_pos0, int64_t E, int m, int H_I, int d_I, int k,
+                       const int32_t* topk_idx, const int32_t* topk_cnt, const uint16_t* scores) {
+  if (!qi_codes || !qi_scales || !ki_codes || !ki_scales || !topk_idx || !topk_cnt)
+    return CSA_ERR_INVALID_ARG;
+  if (!al16(qi_codes) || !al16(ki_codes) || !al16(topk_idx) || !al16(topk_cnt) ||
+      (scores && !al16(scores)))
+    return CSA_ERR_ALIGN;
+  if (B < 1 || Nq < 1 || q_pos0 < 0 || E < 0 || m < 1 || k < 1) return CSA_ERR_INVALID_ARG;
+  if (d_I != 32 && d_I != 64) return CSA_ERR_UNSUPPORTED;
+  if (H_I != 1 && H_I != 2 && H_I != 4 && H_I != 8) return CSA_ERR_UNSUPPORTED;
+  if (E > (int64_t)1 << 31 || (int64_t)B * Nq > ((int64_t)1 << 31) - 1) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
+csa_status check_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
+                      int k, const int32_t* topk_idx, const int32_t* topk_cnt) {
+  if (!scores || !topk_idx || !topk_cnt) return CSA_ERR_INVALID_ARG;
+  if (!al16(scores) || !al16(topk_idx) || !al16(topk_cnt)) return CSA_ERR_ALIGN;
+  if (B < 1 || Nq < 1 || q_pos0 < 0 || E < 0 || m < 1 || k < 1) return CSA_ERR_INVALID_ARG;
+  if ((int64_t)B * Nq > ((int64_t)1 << 31) - 1) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
+csa_status check_attend(const uint16_t* q, const uint16_t* k_cmp, const uint16_t* v_cmp,
+                        int64_t E, const uint16_t* k_raw, const uint16_t* v_raw, int64_t N, int W,
+                        int B, int Nq, int64_t q_pos0, int H, int d, const uint16_t* out,
+                        const float* lse) {
+  if (!q || !k_cmp || !v_cmp || !k_raw || !v_raw || !out) return CSA_ERR_INVALID_ARG;
+  if (!al16(q) || !al16(k_cmp) || !al16(v_cmp) || !al16(k_raw) || !al16(v_raw) || !al16(out) ||
+      (lse && !al16(lse)))
+    return CSA_ERR_ALIGN;
+  if (B < 1 || Nq < 1 || H < 1 || N < 1 || W < 0 || E < 0 || q_pos0 < 0)
+    return CSA_ERR_INVALID_ARG;
+  if (q_pos0 + Nq > N) return CSA_ERR_SHAPE;
+  if (d != 64 && d != 128) return CSA_ERR_UNSUPPORTED;
+  if (H > 1024 || (int64_t)B * Nq > 65535LL * 32768LL) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
+// ---- internal runners (arguments already validated) -----------------------------------------
+csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
+                          const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
+                          int64_t q_pos0, int64_t E, int m, int H_I, int d_I, int k,
+                          int32_t* topk_idx, int32_t* topk_cnt, uint16_t* scores, void* ws,
+                          cudaStream_t st) {
+  uint16_t* sc = scores ? scores : static_cast<uint16_t*>(ws);
+  if (E > 0) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return CSA_ERR_CUDA;
+    uint32_t* status = status_word();
+    if (!status) return CSA_ERR_CUDA;
+    alignas(64) CUtensorMap map;
+    const cuuint64_t row = (cuuint64_t)(d_I / 2);
+    cuuint64_t dims[3] = {row, (cuuint64_t)E, (cuuint64_t)B};
+    cuuint64_t strides[2] = {row, row * (cuuint64_t)E};
+    cuuint32_t box[3] = {32, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(ki_codes), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return CSA_ERR_CUDA;
+    const IndexerPlan plan = plan_indexer(B, Nq, E, H_I, d_I);
+    cudaError_t e = launch_indexer(&map, qi_codes, qi_scales, ki_scales, sc, B, Nq, q_pos0, E, m,
+                                   H_I, d_I, plan, status, st);
+    if (e != cudaSuccess) return CSA_ERR_CUDA;
+  }
+  return from_cuda(launch_topk(sc, B, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, st));
+}
+
+size_t index_ws_bytes(int B, int Nq, int64_t E, int scores_given) {
+  return scores_given ? 0 : round_up((size_t)B * Nq * (size_t)E * 2, 256);
+}
+
+int64_t hca_max_keys(int64_t E, int m, int64_t N, int W) {
+  const int64_t vis = N / m < E ? N / m : E;
+  return vis + W;
+}
+
+}  // namespace
+
+extern "C" {
+
+int csa_abi_version(void) { return 1; }
+
+const char* csa_status_string(csa_status s) {
+  switch (s) {
+    case CSA_OK: return "ok";
+    case CSA_ERR_INVALID_ARG: return "invalid argument";
+    case CSA_ERR_SHAPE: return "inconsistent shape";
+    case CSA_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case CSA_ERR_WORKSPACE: return "workspace missing or too small";
+    case CSA_ERR_UNSUPPORTED: return "unsupported shape";
+    case CSA_ERR_CUDA: return "CUDA error";
+    case CSA_ERR_DEVICE: return "device-side fault recorded";
+  }
+  return "unknown status";
+}
+
+csa_status csa_compress(const uint16_t* k_raw, const uint16_t* v_raw, const float* logits, int B,
+                        int64_t N, int d, int m, int64_t tok_begin, int64_t tok_end,
+                        uint16_t* k_cmp, uint16_t* v_cmp, void* stream) {
+  csa_status s = check_compress(k_raw, v_raw, logits, B, N, d, m, tok_begin, tok_end, k_cmp, v_cmp);
+  if (s != CSA_OK) return s;
+  const int64_t j0 = tok_begin / m, j1 = tok_end / m;
+  return from_cuda(launch_compress(k_raw, v_raw, logits, B, N, d, m, j0, j1 - j0, k_cmp, v_cmp,
+                                   static_cast<cudaStream_t>(stream)));
+}
+
+size_t csa_index_topk_workspace_size(int B, int Nq, int64_t E, int k, int scores_given) {
+  (void)k;
+  if (B < 1 || Nq < 1 || E < 0) return 0;
+  return index_ws_bytes(B, Nq, E, scores_given);
+}
+
+csa_status csa_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
+                          const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
+                          int64_t q_pos0, int64_t E, int m, int H_I, int d_I, int k,
+                          int32_t* topk_idx, int32_t* topk_cnt, uint16_t* scores, void* ws,
+                          size_t ws_bytes, void* stream) {
+  csa_status s = check_index(qi_codes, qi_scales, ki_codes, ki_scales, B, Nq, q_pos0, E, m, H_I,
+                             d_I, k, topk_idx, topk_cnt, scores);
+  if (s != CSA_OK) return s;
+  const size_t need = index_ws_bytes(B, Nq, E, scores != nullptr);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !al16(ws))) return CSA_ERR_WORKSPACE;
+  return run_index_topk(qi_codes, qi_scales, ki_codes, ki_scales, B, Nq, q_pos0, E, m, H_I, d_I,
+                        k, topk_idx, topk_cnt, scores, ws, static_cast<cudaStream_t>(stream));
+}
+
+size_t csa_topk_workspace_size(int B, int Nq, int64_t E, int k) {
+  (void)B; (void)Nq; (void)E; (void)k;
+  return 0;
+}
+
+csa_status csa_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
+                    int k, int32_t* topk_idx, int32_t* topk_cnt, void* ws, size_t ws_bytes,
+                    void* stream) {
+  (void)ws; (void)ws_bytes;
+  csa_status s = check_topk(scores, B, Nq, q_pos0, E, m, k, topk_idx, topk_cnt);
+  if (s != CSA_OK) return s;
+  return from_cuda(launch_topk(scores, B, Nq, q_pos0, E, m, k, topk_idx, topk_cnt,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+size_t csa_attend_workspace_size(int B, int Nq, int H, int d, int k, int W) {
+  if (B < 1 || Nq < 1 || H < 1 || k < 0 || W < 0) return 0;
+  return attend_workspace_bytes(B * Nq, H, d, (int64_t)k + W);
+}
+
+csa_status csa_attend(const uint16_t* q, const uint16_t* k_cmp, const uint16_t* v_cmp, int64_t E,
+                      const int32_t* topk_idx, const int32_t* topk_cnt, int k,
+                      const uint16_t* k_raw, const uint16_t* v_raw, int64_t N, int W, int B,
+                      int Nq, int64_t q_pos0, int H, int d, uint16_t* out, float* lse, void* ws,
+                      size_t ws_bytes, void* stream) {
+  csa_status s = check_attend(q, k_cmp, v_cmp, E, k_raw, v_raw, N, W, B, Nq, q_pos0, H, d, out, lse);
+  if (s != CSA_OK) return s;
+  if (!topk_idx || !topk_cnt || k < 0) return CSA_ERR_INVALID_ARG;
+  if (!al16(topk_idx) || !al16(topk_cnt)) return CSA_ERR_ALIGN;
+  const size_t need = attend_workspace_bytes(B * Nq, H, d, (int64_t)k + W);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !al16(ws))) return CSA_ERR_WORKSPACE;
+  uint32_t* status = status_word();
+  if (!status) return CSA_ERR_CUDA;
+  AttendArgs a{q, k_cmp, v_cmp, topk_idx, topk_cnt, k_raw, v_raw, out, lse,
+               E, N, q_pos0, k, 1, W, B, Nq, H, d};
+  return from_cuda(launch_attend(a, (int64_t)k + W, ws, status, static_cast<cudaStream_t>(stream)));
+}
+
+size_t hca_attend_workspace_size(int B, int Nq, int H, int d, int64_t E, int m, int W) {
+  if (B < 1 || Nq < 1 || H < 1 || E < 0 || m < 1 || W < 0) return 0;
+  return attend_workspace_bytes(B * Nq, H, d, E + W);
+}
+
+csa_status hca_attend(const uint16_t* q, const uint16_t* k_cmp, const uint16_t* v_cmp, int64_t E,
+                      int m, const uint16_t* k_raw, const uint16_t* v_raw, int64_t N, int W, int B,
+                      int Nq, int64_t q_pos0, int H, int d, uint16_t* out, float* lse, void* ws,
+                      size_t ws_bytes, void* stream) {
+  csa_status s = check_attend(q, k_cmp, v_cmp, E, k_raw, v_raw, N, W, B, Nq, q_pos0, H, d, out, lse);
+  if (s != CSA_OK) return s;
+  if (m < 1) return CSA_ERR_INVALID_ARG;
+  const size_t need = attend_workspace_bytes(B * Nq, H, d, E + W);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !al16(ws))) return CSA_ERR_WORKSPACE;
+  uint32_t* status = status_word();
+  if (!status) return CSA_ERR_CUDA;
+  AttendArgs a{q, k_cmp, v_cmp, nullptr, nullptr, k_raw, v_raw, out, lse,
+               E, N, q_pos0, 0, m, W, B, Nq, H, d};
+  return from_cuda(launch_attend(a, E + W, ws, status, static_cast<cudaStream_t>(stream)));
+}
+
+size_t csa_hca_layer_pair_workspace_size(const csa_layer_desc* c, const hca_layer_desc* h) {
+  size_t need = 0;
+  if (c) {
+    const int64_t E = c->N / (c->m > 0 ? c->m : 1);
+    const size_t a = index_ws_bytes(c->B, c->Nq, E, c->scores != nullptr);
+    const size_t b = attend_workspace_bytes(c->B * c->Nq, c->H, c->d, (int64_t)c->k + c->W);
+    need = a > need ? a : need;
+    need = b > need ? b : need;
+  }
+  if (h) {
+    const int64_t E = h->N / (h->m > 0 ? h->m : 1);
+    const size_t b = attend_workspace_bytes(h->B * h->Nq, h->H, h->d, E + h->W);
+    need = b > need ? b : need;
+  }
+  return need;
+}
+
+csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, void* ws,
+                              size_t ws_bytes, void* stream) {
+  if (!c && !h) return CSA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // validate everything before launching anything
+  if (c) {
+    if (c->m < 1) return CSA_ERR_INVALID_ARG;
+    const int64_t E = c->N / c->m;
+    csa_status s = check_compress(c->k_raw, c->v_raw, c->logits, c->B, c->N, c->d, c->m,
+                                  c->compress_begin, c->N, c->k_cmp, c->v_cmp);
+    if (s != CSA_OK) return s;
+    s = check_index(c->qi_codes, c->qi_scales, c->ki_codes, c->ki_scales, c->B, c->Nq, c->q_pos0,
+                    E, c->m, c->H_I, c->d_I, c->k, c->topk_idx, c->topk_cnt, c->scores);
+    if (s != CSA_OK) return s;
+    s = check_attend(c->q, c->k_cmp, c->v_cmp, E, c->k_raw, c->v_raw, c->N, c->W, c->B, c->Nq,
+                     c->q_pos0, c->H, c->d, c->out, c->lse);
+    if (s != CSA_OK) return s;
+  }
+  if (h) {
+    if (h->m < 1) return CSA_ERR_INVALID_ARG;
+    const int64_t E = h->N / h->m;
+    csa_status s = check_compress(h->k_raw, h->v_raw, h->logits, h->B, h->N, h->d, h->m,
+                                  h->compress_begin, h->N, h->k_cmp, h->v_cmp);
+    if (s != CSA_OK) return s;
+    s = check_attend(h->q, h->k_cmp, h->v_cmp, E, h->k_raw, h->v_raw, h->N, h->W, h->B, h->Nq,
+                     h->q_pos0, h->H, h->d, h->out, h->lse);
+    if (s != CSA_OK) return s;
+  }
+  const size_t need = csa_hca_layer_pair_workspace_size(c, h);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !al16(ws))) return CSA_ERR_WORKSPACE;
+  uint32_t* status = status_word();
+  if (!status) return CSA_ERR_CUDA;
+
+  if (c) {
+    const int64_t E = c->N / c->m;
+    const int64_t j0 = c->compress_begin / c->m;
+    if (launch_compress(c->k_raw, c->v_raw, c->logits, c->B, c->N, c->d, c->m, j0, E - j0,
+                        c->k_cmp, c->v_cmp, st) != cudaSuccess)
+      return CSA_ERR_CUDA;
+    csa_status s = run_index_topk(c->qi_codes, c->qi_scales, c->ki_codes, c->ki_scales, c->B,
+                                  c->Nq, c->q_pos0, E, c->m, c->H_I, c->d_I, c->k, c->topk_idx,
+                                  c->topk_cnt, c->scores, ws, st);
+    if (s != CSA_OK) return s;
+    AttendArgs a{c->q, c->k_cmp, c->v_cmp, c->topk_idx, c->topk_cnt, c->k_raw, c->v_raw, c->out,
+                 c->lse, E, c->N, c->q_pos0, c->k, c->m, c->W, c->B, c->Nq, c->H, c->d};
+    if (launch_attend(a, (int64_t)c->k + c->W, ws, status, st) != cudaSuccess) return CSA_ERR_CUDA;
+  }
+  if (h) {
+    const int64_t E = h->N / h->m;
+    const int64_t j0 = h->compress_begin / h->m;
+    if (launch_compress(h->k_raw, h->v_raw, h->logits, h->B, h->N, h->d, h->m, j0, E - j0,
+                        h->k_cmp, h->v_cmp, st) != cudaSuccess)
+      return CSA_ERR_CUDA;
+    AttendArgs a{h->q, h->k_cmp, h->v_cmp, nullptr, nullptr, h->k_raw, h->v_raw, h->out, h->lse,
+                 E, h->N, h->q_pos0, 0, h->m, h->W, h->B, h->Nq, h->H, h->d};
+    if (launch_attend(a, hca_max_keys(E, h->m, h->N, h->W), ws, status, st) != cudaSuccess)
+      return CSA_ERR_CUDA;
+  }
+  return CSA_OK;
+}
+
+csa_status csa_get_device_status(void* stream, int reset, uint32_t* flags_out) {
+  uint32_t* status = status_word();
+  if (!status) return CSA_ERR_CUDA;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return CSA_ERR_CUDA;
+  if (reset && cudaMemset(status, 0, sizeof(uint32_t)) != cudaSuccess) return CSA_ERR_CUDA;
+  if (flags_out) *flags_out = v;
+  return v ? CSA_ERR_DEVICE : CSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,403 @@
+// CSA sparse attention and HCA dense attention over compressed entries plus a sliding window.
+//
+// Lighthouse "deep deepseek v4 release" 八.3: CSA attends to the top-k selected compressed
+// entries plus a sliding-window branch of n_win raw tokens; HCA attends densely to every
+// compressed entry (m' = 128) plus the same window. One softmax spans the entries and the window
+// tokens of a query; logits are q.k (the 1/sqrt(d) is folded into q).
+//
+// MQA layout: all H query heads of a token share one K/V head, so the heads form the M side of
+// the contraction. A CTA owns one query token and up to 64 heads (16 per warp) and walks a
+// range of 64-key chunks of that token's key list: the chunk's K and V rows are gathered with
+// 16-byte cp.async into XOR-swizzled shared memory (double-buffered), QK^T and PV run on the
+// tensor cores, and the softmax is an online (running max / sum) softmax in registers. When a
+// token's keys are split over several CTAs (decode), each writes (m, l, unnormalised O) and a
+// merge kernel combines the splits with log-sum-exp weights.
+#include "common.cuh"
+#include "kernels.h"
+#include "prof.h"
+
+namespace csa {
+namespace {
+
+constexpr int kKC = 64;  // keys per chunk
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct AttnParams {
+  const uint16_t* q;
+  const uint16_t* k_cmp;
+  const uint16_t* v_cmp;
+  const int32_t* topk_idx;
+  const int32_t* topk_cnt;
+  const uint16_t* k_raw;
+  const uint16_t* v_raw;
+  uint16_t* out;
+  float* lse;
+  float* ws_o;   // [n_splits, tokens, H, D] unnormalised partial outputs
+  float* ws_ml;  // [n_splits, tokens, H, 2] running max and sum
+  int64_t E, N, q_pos0;
+  int k, m, W, Nq, H, n_splits, tokens;
+  int sparse;
+  uint32_t* status;
+};
+
+CSA_DEV void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+CSA_DEV void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+CSA_DEV void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32"
+      " {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Key list of one token: n_sel selected / visible entries, then the window tokens.
+struct KeyList {
+  int64_t b, tok, n_sel, w0, n_keys;
+};
+
+template <int D, int NW>
+__global__ void __launch_bounds__(NW * 32) attend_kernel(const AttnParams p) {
+  constexpr int CPR = D / 8;  // 16-byte chunks per row
+  constexpr int NT = 32 * NW;
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem);          // [2][kKC][D]
+  uint16_t* Vs = Ks + 2 * kKC * D;                           // [2][kKC][D]
+  uint8_t* kmask = reinterpret_cast<uint8_t*>(Vs + 2 * kKC * D);  // [2][kKC]
+
+  const int split = blockIdx.x;
+  const int64_t tok = blockIdx.y;
+  const int h_base = blockIdx.z * (16 * NW);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tq = lane & 3;
+
+  KeyList kl;
+  kl.tok = tok;
+  kl.b = tok / p.Nq;
+  const int64_t t = p.q_pos0 + tok % p.Nq;
+  if (p.sparse) {
+    int64_t c = p.topk_cnt[tok];
+    if (c < 0 || c > p.k) {
+      if (threadIdx.x == 0) atomicOr(p.status, kFlagBadIndex);
+      c = c < 0 ? 0 : p.k;
+    }
+    kl.n_sel = c;
+  } else {
+    kl.n_sel = max((int64_t)0, min(p.E, (t + 1) / p.m));
+  }
+  kl.w0 = max((int64_t)0, t - p.W + 1);
+  const int64_t n_win = p.W > 0 ? (t - kl.w0 + 1) : 0;
+  kl.n_keys = kl.n_sel + n_win;
+  const int64_t n_chunks = (kl.n_keys + kKC - 1) / kKC;
+  const int64_t c_begin = n_chunks * split / p.n_splits;
+  const int64_t c_end = n_chunks * (split + 1) / p.n_splits;
+
+  auto load_chunk = [&](int64_t c, int buf) {
+    uint16_t* kd = Ks + buf * kKC * D;
+    uint16_t* vd = Vs + buf * kKC * D;
+    for (int x = threadIdx.x; x < kKC * CPR; x += NT) {
+      const int r = x / CPR, cc = x % CPR;
+      const int64_t key = c * kKC + r;
+      const uint16_t* ks = p.k_raw;
+      const uint16_t* vs = p.v_raw;
+      bool valid = key < kl.n_keys;
+      if (valid) {
+        if (key < kl.n_sel) {
+          int64_t j = p.sparse ? (int64_t)p.topk_idx[kl.tok * p.k + key] : key;
+          if (j < 0 || j >= p.E) {
+            valid = false;
+            if (cc == 0) atomicOr(p.status, kFlagBadIndex);
+          } else {
+            ks = p.k_cmp + (kl.b * p.E + j) * D;
+            vs = p.v_cmp + (kl.b * p.E + j) * D;
+          }
+        } else {
+          const int64_t u = kl.w0 + (key - kl.n_sel);
+          ks = p.k_raw + (kl.b * p.N + u) * D;
+          vs = p.v_raw + (kl.b * p.N + u) * D;
+        }
+      }
+      const int phys = r * CPR + (cc ^ (r & 7));
+      cp_async_16(kd + phys * 8, valid ? ks + cc * 8 : p.k_raw, valid ? 16u : 0u);
+      cp_async_16(vd + phys * 8, valid ? vs + cc * 8 : p.v_raw, valid ? 16u : 0u);
+      if (cc == 0) kmask[buf * kKC + r] = valid ? 1 : 0;
+    }
+    cp_async_commit();
+  };
+
+  // Q fragments (rows h0 = h_base + warp*16 + g and h0 + 8), A layout of m16n8k16.
+  const int h0 = h_base + warp * 16 + g, h1 = h0 + 8;
+  uint32_t qa[D / 16][4];
+  {
+    const uint16_t* q0 = p.q + (tok * p.H + h0) * D;
+    const uint16_t* q1 = p.q + (tok * p.H + h1) * D;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int c0 = kk * 16 + 2 * tq;
+      qa[kk][0] = h0 < p.H ? *reinterpret_cast<const uint32_t*>(q0 + c0) : 0u;
+      qa[kk][1] = h1 < p.H ? *reinterpret_cast<const uint32_t*>(q1 + c0) : 0u;
+      qa[kk][2] = h0 < p.H ? *reinterpret_cast<const uint32_t*>(q0 + c0 + 8) : 0u;
+      qa[kk][3] = h1 < p.H ? *reinterpret_cast<const uint32_t*>(q1 + c0 + 8) : 0u;
+    }
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  if (c_begin < c_end) load_chunk(c_begin, 0);
+  for (int64_t c = c_begin; c < c_end; ++c) {
+    const int buf = (int)((c - c_begin) & 1);
+    if (c + 1 < c_end) {
+      load_chunk(c + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const uint32_t kbase = smem_addr(Ks + buf * kKC * D);
+    const uint32_t vbase = smem_addr(Vs + buf * kKC * D);
+    const uint8_t* msk = kmask + buf * kKC;
+
+    // ---- S = Q K^T over 64 keys ----
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+    const int mi = lane >> 3, rr = lane & 7;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const int r = 16 * pp + (mi >> 1) * 8 + rr;
+        const int cc = 2 * kk + (mi & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + (uint32_t)((r * CPR + (cc ^ (r & 7))) * 16), b0, b1, b2, b3);
+        mma_bf16_16816(s[2 * pp], qa[kk], b0, b1);
+        mma_bf16_16816(s[2 * pp + 1], qa[kk], b2, b3);
+      }
+    }
+    // ---- mask + online softmax ----
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = nt * 8 + 2 * tq;
+      if (!msk[col]) s[nt][0] = s[nt][2] = -INFINITY;
+      if (!msk[col + 1]) s[nt][1] = s[nt][3] = -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+    }
+#pragma unroll
+    for (int o2 = 1; o2 < 4; o2 <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float corr0 = exp2f((m0 - base0) * kLog2e), corr1 = exp2f((m1 - base1) * kLog2e);
+    m0 = mn0;
+    m1 = mn1;
+    float rs0 = 0.f, rs1 = 0.f;
+    uint32_t pa[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const float p0 = exp2f((s[nt][0] - base0) * kLog2e);
+      const float p1 = exp2f((s[nt][1] - base0) * kLog2e);
+      const float p2 = exp2f((s[nt][2] - base1) * kLog2e);
+      const float p3 = exp2f((s[nt][3] - base1) * kLog2e);
+      rs0 += p0 + p1;
+      rs1 += p2 + p3;
+      const int kk2 = nt >> 1, hi = nt & 1;
+      pa[kk2][hi * 2 + 0] = pack_bf16x2(p0, p1);
+      pa[kk2][hi * 2 + 1] = pack_bf16x2(p2, p3);
+    }
+    l0 = l0 * corr0 + rs0;
+    l1 = l1 * corr1 + rs1;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][0] *= corr0;
+      o[i][1] *= corr0;
+      o[i][2] *= corr1;
+      o[i][3] *= corr1;
+    }
+    // ---- O += P V ----
+#pragma unroll
+    for (int kk2 = 0; kk2 < 4; ++kk2) {
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {
+        const int r = 16 * kk2 + (mi & 1) * 8 + rr;
+        const int cc = 2 * dp + (mi >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vbase + (uint32_t)((r * CPR + (cc ^ (r & 7))) * 16), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dp], pa[kk2], b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], pa[kk2], b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- finish: quad-reduce the row sums, then store ----
+#pragma unroll
+  for (int o2 = 1; o2 < 4; o2 <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o2);
+  }
+  if (p.n_splits == 1) {
+    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+#pragma unroll
+    for (int dt = 0; dt < D / 8; ++dt) {
+      const int d0 = dt * 8 + 2 * tq;
+      if (h0 < p.H)
+        *reinterpret_cast<uint32_t*>(p.out + (tok * p.H + h0) * D + d0) =
+            pack_bf16x2(o[dt][0] * inv0, o[dt][1] * inv0);
+      if (h1 < p.H)
+        *reinterpret_cast<uint32_t*>(p.out + (tok * p.H + h1) * D + d0) =
+            pack_bf16x2(o[dt][2] * inv1, o[dt][3] * inv1);
+    }
+    if (p.lse != nullptr && tq == 0) {
+      if (h0 < p.H) p.lse[tok * p.H + h0] = l0 > 0.f ? m0 + logf(l0) : -INFINITY;
+      if (h1 < p.H) p.lse[tok * p.H + h1] = l1 > 0.f ? m1 + logf(l1) : -INFINITY;
+    }
+  } else {
+    const int64_t sb = ((int64_t)split * p.tokens + tok) * p.H;
+#pragma unroll
+    for (int dt = 0; dt < D / 8; ++dt) {
+      const int d0 = dt * 8 + 2 * tq;
+      if (h0 < p.H)
+        *reinterpret_cast<float2*>(p.ws_o + (sb + h0) * D + d0) = make_float2(o[dt][0], o[dt][1]);
+      if (h1 < p.H)
+        *reinterpret_cast<float2*>(p.ws_o + (sb + h1) * D + d0) = make_float2(o[dt][2], o[dt][3]);
+    }
+    if (tq == 0) {
+      if (h0 < p.H) *reinterpret_cast<float2*>(p.ws_ml + (sb + h0) * 2) = make_float2(m0, l0);
+      if (h1 < p.H) *reinterpret_cast<float2*>(p.ws_ml + (sb + h1) * 2) = make_float2(m1, l1);
+    }
+  }
+}
+
+// Combines split-K partials: out = sum_s w_s O_s / sum_s w_s l_s with w_s = exp(m_s - max m).
+template <int D>
+__global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ ws_o,
+                                                  const float* __restrict__ ws_ml, int n_splits,
+                                                  int64_t tokens, int H, uint16_t* out,
+                                                  float* lse) {
+  const int64_t th = blockIdx.x;  // tok * H + h
+  const int lane = threadIdx.x;
+  float M = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ws_ml[((int64_t)s * tokens * H + th) * 2]);
+  constexpr int PER = D / 32;
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < n_splits; ++s) {
+      const int64_t base = (int64_t)s * tokens * H + th;
+      const float ms = ws_ml[base * 2], ls = ws_ml[base * 2 + 1];
+      if (ms == -INFINITY) continue;
+      const float w = expf(ms - M);
+      L += w * ls;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] += w * ws_o[base * D + lane * PER + i];
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; i += 2)
+    *reinterpret_cast<uint32_t*>(out + th * D + lane * PER + i) =
+        pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
+  if (lse != nullptr && lane == 0) lse[th] = L > 0.f ? M + logf(L) : -INFINITY;
+}
+
+template <int D, int NW>
+cudaError_t launch_attend_t(const AttnParams& prm, int groups, cudaStream_t stream) {
+  const size_t smem = (size_t)2 * 2 * kKC * D * 2 + 2 * kKC;
+  auto kern = attend_kernel<D, NW>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)prm.n_splits, (unsigned)prm.tokens, (unsigned)groups);
+  {
+    ProfScope prof(stream, prm.sparse ? "csa_attend" : "hca_attend");
+    kern<<<grid, NW * 32, smem, stream>>>(prm);
+  }
+  e = cudaGetLastError();
+  if (e != cudaSuccess || prm.n_splits == 1) return e;
+  ProfScope prof(stream, "lse_merge");
+  merge_kernel<D><<<(unsigned)((int64_t)prm.tokens * prm.H), 32, 0, stream>>>(
+      prm.ws_o, prm.ws_ml, prm.n_splits, prm.tokens, prm.H, prm.out, prm.lse);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int plan_attend_splits(int tokens, int H, int64_t max_keys) {
+  const int64_t groups = (H + 63) / 64;
+  const int64_t chunks = (max_keys + kKC - 1) / kKC;
+  const int64_t units = (int64_t)tokens * groups;
+  const int64_t target = (int64_t)kNumSMs * 2;
+  if (units >= target || chunks <= 1) return 1;
+  int64_t s = (target + units - 1) / units;
+  if (s > chunks) s = chunks;
+  return (int)(s < 1 ? 1 : s);
+}
+
+size_t attend_workspace_bytes(int tokens, int H, int d, int64_t max_keys) {
+  const int s = plan_attend_splits(tokens, H, max_keys);
+  if (s <= 1) return 0;
+  return (size_t)s * tokens * H * (size_t)(d + 2) * sizeof(float);
+}
+
+cudaError_t launch_attend(const AttendArgs& a, int64_t max_keys, void* ws, uint32_t* status,
+                          cudaStream_t stream) {
+  AttnParams prm;
+  prm.q = a.q;
+  prm.k_cmp = a.k_cmp;
+  prm.v_cmp = a.v_cmp;
+  prm.topk_idx = a.topk_idx;
+  prm.topk_cnt = a.topk_cnt;
+  prm.k_raw = a.k_raw;
+  prm.v_raw = a.v_raw;
+  prm.out = a.out;
+  prm.lse = a.lse;
+  prm.E = a.E;
+  prm.N = a.N;
+  prm.q_pos0 = a.q_pos0;
+  prm.k = a.k;
+  prm.m = a.m;
+  prm.W = a.W;
+  prm.Nq = a.Nq;
+  prm.H = a.H;
+  prm.tokens = a.B * a.Nq;
+  prm.sparse = a.topk_idx != nullptr;
+  prm.status = status;
+  prm.n_splits = plan_attend_splits(prm.tokens, a.H, max_keys);
+  prm.ws_o = reinterpret_cast<float*>(ws);
+  prm.ws_ml = prm.ws_o + (size_t)prm.n_splits * prm.tokens * a.H * a.d;
+  if (prm.tokens == 0) return cudaSuccess;
+  const int groups = (a.H + 63) / 64;
+  const int nw = a.H >= 64 ? 4 : (a.H + 15) / 16;
+  if (a.d == 128) {
+    if (nw == 4) return launch_attend_t<128, 4>(prm, groups, stream);
+    if (nw == 2) return launch_attend_t<128, 2>(prm, groups, stream);
+    if (nw == 1) return launch_attend_t<128, 1>(prm, groups, stream);
+    return launch_attend_t<128, 4>(prm, groups, stream);
+  }
+  if (a.d == 64) {
+    if (nw == 4) return launch_attend_t<64, 4>(prm, groups, stream);
+    if (nw == 2) return launch_attend_t<64, 2>(prm, groups, stream);
+    if (nw == 1) return launch_attend_t<64, 1>(prm, groups, stream);
+    return launch_attend_t<64, 4>(prm, groups, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace csa

@@ -1,0 +1,137 @@
+// Block pooling of raw K/V into compressed entries (CSA m = 4, HCA m = 128).
+//
+// Lighthouse "deep deepseek v4 release" 八.3: every m consecutive KV tokens are merged into
+// one compressed entry. Pooling operator (not printed on the pages; the workload definition
+// fixes it): p_i = softmax_i(w[jm+i]) over the block's per-token logits, entry = sum_i p_i row_i,
+// the same weights for K and V.
+//
+// HBM-bound streaming kernel: every raw byte is read once with 128-bit loads, every entry
+// byte written once. One thread owns 8 channels (16 bytes) of one entry for both K and V,
+// so a warp reads 512 contiguous bytes per token row pair.
+#include "common.cuh"
+#include "kernels.h"
+#include "prof.h"
+
+namespace csa {
+namespace {
+
+CSA_DEV uint4 ldg_stream(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+CSA_DEV void acc8(float (&acc)[8], uint4 v, float w) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q] = fmaf(w, __uint_as_float(u[q] << 16), acc[2 * q]);
+    acc[2 * q + 1] = fmaf(w, __uint_as_float(u[q] & 0xFFFF0000u), acc[2 * q + 1]);
+  }
+}
+
+CSA_DEV uint4 pack8(const float (&acc)[8], float inv) {
+  uint4 o;
+  o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+  o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  return o;
+}
+
+// grid-stride over (b, entry, 16-byte chunk); CH = d / 8 chunks per row.
+template <int CH>
+__global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restrict__ k_raw,
+                                                       const uint16_t* __restrict__ v_raw,
+                                                       const float* __restrict__ logits,
+                                                       uint16_t* __restrict__ k_cmp,
+                                                       uint16_t* __restrict__ v_cmp, int B,
+                                                       int64_t N, int m, int64_t j_begin,
+                                                       int64_t n_entries) {
+  constexpr int D = CH * 8;
+  const int64_t E = N / m;
+  const int64_t total = (int64_t)B * n_entries * CH;
+  for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < total;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(w % CH);
+    const int64_t e = (w / CH) % n_entries;
+    const int64_t b = w / ((int64_t)CH * n_entries);
+    const int64_t j = j_begin + e;
+    const int64_t tok0 = b * N + j * m;
+    const float* wl = logits + tok0;
+
+    float mx = -INFINITY;
+    for (int i = 0; i < m; ++i) mx = fmaxf(mx, __ldg(wl + i));
+
+    float acc_k[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float acc_v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float sum = 0.f;
+    const uint16_t* kp = k_raw + tok0 * D + c * 8;
+    const uint16_t* vp = v_raw + tok0 * D + c * 8;
+    int i = 0;
+    for (; i + 4 <= m; i += 4) {
+      uint4 kv[4], vv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        kv[u] = ldg_stream(kp + (int64_t)(i + u) * D);
+        vv[u] = ldg_stream(vp + (int64_t)(i + u) * D);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float p = expf(__ldg(wl + i + u) - mx);
+        sum += p;
+        acc8(acc_k, kv[u], p);
+        acc8(acc_v, vv[u], p);
+      }
+    }
+    for (; i < m; ++i) {
+      const float p = expf(__ldg(wl + i) - mx);
+      sum += p;
+      acc8(acc_k, ldg_stream(kp + (int64_t)i * D), p);
+      acc8(acc_v, ldg_stream(vp + (int64_t)i * D), p);
+    }
+    const float inv = 1.0f / sum;
+    const int64_t o = (b * E + j) * D + c * 8;
+    *reinterpret_cast<uint4*>(k_cmp + o) = pack8(acc_k, inv);
+    *reinterpret_cast<uint4*>(v_cmp + o) = pack8(acc_v, inv);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const uint16_t* k_raw, const uint16_t* v_raw, const float* logits,
+                            int B, int64_t N, int d, int m, int64_t j_begin, int64_t n_entries,
+                            uint16_t* k_cmp, uint16_t* v_cmp, cudaStream_t stream) {
+  if (n_entries <= 0 || B <= 0) return cudaSuccess;
+  const int ch = d / 8;
+  const int64_t total = (int64_t)B * n_entries * ch;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = (int64_t)kNumSMs * 8;  // 8 resident 256-thread CTAs per SM
+  if (blocks > cap) blocks = cap;
+  ProfScope prof(stream, "compress");
+  switch (ch) {
+    case 8:
+      compress_kernel<8><<<(unsigned)blocks, threads, 0, stream>>>(k_raw, v_raw, logits, k_cmp,
+                                                                   v_cmp, B, N, m, j_begin,
+                                                                   n_entries);
+      break;
+    case 16:
+      compress_kernel<16><<<(unsigned)blocks, threads, 0, stream>>>(k_raw, v_raw, logits, k_cmp,
+                                                                    v_cmp, B, N, m, j_begin,
+                                                                    n_entries);
+      break;
+    case 32:
+      compress_kernel<32><<<(unsigned)blocks, threads, 0, stream>>>(k_raw, v_raw, logits, k_cmp,
+                                                                    v_cmp, B, N, m, j_begin,
+                                                                    n_entries);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace csa

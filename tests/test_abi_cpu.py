@@ -1,0 +1,102 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads, exports every function
+include/csa.h declares, rejects bad arguments before touching CUDA, sizes workspaces, and the
+ctypes descriptor structs match the C layout."""
+import ctypes
+import os
+
+import pytest
+
+from long_context_compressed_pooling_b300 import build as B
+import long_context_compressed_pooling_b300 as csa
+from long_context_compressed_pooling_b300 import _native as N
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return N.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = N.exported_symbols()
+    assert len(syms) >= 14
+    missing = [n for n, ok in syms.items() if not ok]
+    assert not missing, missing
+    assert lib.csa_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = lib.csa_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.csa_status_string(99) == b"unknown status"
+
+
+def _p(addr):
+    return ctypes.c_void_p(addr)
+
+
+ALN = 0x10000  # fake but aligned device addresses: validation fails before they are used
+
+
+def test_compress_validation(lib):
+    f = lib.csa_compress
+    ok = dict(k=_p(ALN), v=_p(ALN), w=_p(ALN), kc=_p(ALN * 2), vc=_p(ALN * 3))
+    # null pointer
+    assert f(None, ok["v"], ok["w"], 1, 64, 128, 4, 0, 64, ok["kc"], ok["vc"], None) == 1
+    # misaligned
+    assert f(_p(ALN + 2), ok["v"], ok["w"], 1, 64, 128, 4, 0, 64, ok["kc"], ok["vc"], None) == 3
+    # tok_begin not a multiple of m, tok_end beyond N
+    assert f(ok["k"], ok["v"], ok["w"], 1, 64, 128, 4, 2, 64, ok["kc"], ok["vc"], None) == 2
+    assert f(ok["k"], ok["v"], ok["w"], 1, 64, 128, 4, 0, 65, ok["kc"], ok["vc"], None) == 2
+    # unsupported head dim / block size
+    assert f(ok["k"], ok["v"], ok["w"], 1, 64, 96, 4, 0, 64, ok["kc"], ok["vc"], None) == 5
+    assert f(ok["k"], ok["v"], ok["w"], 1, 64, 128, 3, 0, 63, ok["kc"], ok["vc"], None) == 5
+    assert f(ok["k"], ok["v"], ok["w"], 1, 1024, 128, 512, 0, 1024, ok["kc"], ok["vc"], None) == 5
+    # shared output cache with distinct K and V inputs
+    assert f(ok["k"], _p(ALN * 5), ok["w"], 1, 64, 128, 4, 0, 64, ok["kc"], ok["kc"], None) == 1
+
+
+def test_index_and_attend_validation(lib):
+    a = _p(ALN)
+    f = lib.csa_index_topk
+    # unsupported d_I and H_I
+    assert f(a, a, a, a, 1, 1, 0, 16, 4, 4, 48, 8, a, a, None, None, 0, None) == 5
+    assert f(a, a, a, a, 1, 1, 0, 16, 4, 3, 64, 8, a, a, None, None, 0, None) == 5
+    # k = 0
+    assert f(a, a, a, a, 1, 1, 0, 16, 4, 4, 64, 0, a, a, None, None, 0, None) == 1
+    # no scores buffer and no workspace
+    assert f(a, a, a, a, 1, 1, 0, 16, 4, 4, 64, 8, a, a, None, None, 0, None) == 4
+    g = lib.csa_attend
+    # queries beyond the context
+    assert g(a, a, a, 4, a, a, 2, a, a, 10, 4, 1, 2, 9, 8, 64, a, None, None, 0, None) == 2
+    # unsupported head dim
+    assert g(a, a, a, 4, a, a, 2, a, a, 10, 4, 1, 1, 9, 8, 96, a, None, None, 0, None) == 5
+    h = lib.hca_attend
+    assert h(a, a, a, 4, 0, a, a, 10, 4, 1, 1, 9, 8, 64, a, None, None, 0, None) == 1
+    assert lib.csa_hca_layer_pair(None, None, None, 0, None) == 1
+
+
+def test_workspace_sizes(lib):
+    # prefill-sized attention needs no split-K workspace; small decode batches do
+    assert lib.csa_attend_workspace_size(1, 8192, 64, 128, 2048, 128) == 0
+    ws = lib.csa_attend_workspace_size(16, 1, 64, 128, 512, 128)
+    assert ws > 0 and ws % 4 == 0
+    assert lib.hca_attend_workspace_size(32, 1, 64, 128, 8192, 128, 128) > 0
+    # scores live in the workspace unless the caller passes a buffer
+    assert lib.csa_index_topk_workspace_size(16, 1, 32768, 512, 0) >= 16 * 32768 * 2
+    assert lib.csa_index_topk_workspace_size(16, 1, 32768, 512, 1) == 0
+
+
+def test_descriptor_struct_layout():
+    # 15 pointers, 9 ints (+4 padding), 3 int64 / 8 pointers, 6 ints, 3 int64
+    assert ctypes.sizeof(N.CsaLayerDesc) == 15 * 8 + 9 * 4 + 4 + 3 * 8
+    assert N.CsaLayerDesc.N.offset == 160
+    assert ctypes.sizeof(N.HcaLayerDesc) == 8 * 8 + 6 * 4 + 3 * 8
+    assert N.HcaLayerDesc.N.offset == 88
+
+
+def test_library_is_sm103a_build():
+    # the build targets sm_103a only
+    assert "arch=compute_103a,code=sm_103a" in " ".join(B.ARCH)
+    assert os.path.exists(N.LIB_PATH)
