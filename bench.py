@@ -26,6 +26,11 @@ import sys
 import threading
 import time
 
+# the CPU oracle legs run single-threaded; set before numpy loads its BLAS
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -465,22 +470,20 @@ def _host_sequence(s, d, b):
 def cpu_baseline(wl, states, budget_s=12.0):
     """The oracle as it stands, one thread, on as many sequences of the workload as fit the
     budget (at least one); throughput is scaled to the metric's unit."""
-    from threadpoolctl import threadpool_limits
     if wl.mode != "decode":
         return {"value": None, "unit": "tok/s", "cores": 1, "kind": "oracle",
                 "sample": "prefill workloads: see --impl reference"}
     B = wl.layers[0].B
     done = 0
     elapsed = 0.0
-    with threadpool_limits(1):
-        while elapsed < budget_s and done < 4 * B:
-            b = done % B
-            seqs = [(s, _host_sequence(s, states[s.kind], b)) for s in wl.layers]
-            t0 = time.perf_counter()
-            for s, seq in seqs:
-                oracle_decode_sequence(s, seq)
-            elapsed += time.perf_counter() - t0
-            done += 1
+    while elapsed < budget_s and done < 4 * B:
+        b = done % B
+        seqs = [(s, _host_sequence(s, states[s.kind], b)) for s in wl.layers]
+        t0 = time.perf_counter()
+        for s, seq in seqs:
+            oracle_decode_sequence(s, seq)
+        elapsed += time.perf_counter() - t0
+        done += 1
     return {"value": done / elapsed, "unit": "tok/s", "cores": 1, "kind": "oracle",
             "sample": f"{done} sequence decode steps of {wl.name} (one token each, "
                       f"all layers of the workload), {elapsed:.1f} s"}
@@ -490,7 +493,6 @@ def run_reference(args, rank, world):
     """The fp64 oracle timed on the host cores: each step decodes one sequence of the workload."""
     import numpy as np
     import torch
-    from threadpoolctl import threadpool_limits
     import oracle as O
     from synth import get_config, generate_layer
     if rank != 0:
@@ -513,15 +515,14 @@ def run_reference(args, rank, world):
             for n in ("qi_codes", "qi_scales", "ki_codes", "ki_scales"):
                 seq[n] = x[n][0].numpy()
         seqs.append((s, seq))
-    with threadpool_limits(1):
-        for _ in range(max(1, args.warmup)):
-            for s, seq in seqs:
-                oracle_decode_sequence(s, seq)
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            for s, seq in seqs:
-                oracle_decode_sequence(s, seq)
-        el = time.perf_counter() - t0
+    for _ in range(max(1, args.warmup)):
+        for s, seq in seqs:
+            oracle_decode_sequence(s, seq)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        for s, seq in seqs:
+            oracle_decode_sequence(s, seq)
+    el = time.perf_counter() - t0
     ms = el * 1e3 / args.steps
     v = 1.0 / (ms * 1e-3)
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world,
