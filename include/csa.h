@@ -97,6 +97,29 @@ csa_status csa_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
 size_t csa_index_topk_workspace_size(int B, int Nq, int64_t E, int k, int scores_given);
 
 /* ----------------------------------------------------------------------------------------
+ * csa_index_topk_noalloc -- csa_index_topk for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a deployment variant of the call above.
+ * Some callers hold no allocator of their own: a plugin or kernel-library host whose device
+ * memory is owned by a framework pool, code running under a memory budget or inside a region
+ * where cudaMalloc's implicit synchronisation is not acceptable, or a C caller that only has its
+ * input and output pointers. This entry point takes the same inputs and outputs as
+ * csa_index_topk but no workspace: its BF16 score scratch is a fixed 8 MiB array inside the
+ * library (every GPU that loads the library keeps it until the process exits), so
+ * B * Nq * E must not exceed 4,194,304 scores; larger calls return CSA_ERR_WORKSPACE.
+ * It calls no cudaMalloc, cudaFree or other allocating routine.
+ * The first call on each device resolves the array's device address (cudaGetSymbolAddress with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array, which keeps the last call's scores: calls whose
+ * execution overlaps on the GPU (other streams, or concurrent host threads) race on it and must
+ * be serialised by the caller.
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_index_topk_noalloc(const uint8_t* qi_codes, const uint8_t* qi_scales,
+                                  const uint8_t* ki_codes, const uint8_t* ki_scales,
+                                  int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I,
+                                  int d_I, int k, int32_t* topk_idx, int32_t* topk_cnt,
+                                  void* stream);
+
+/* ----------------------------------------------------------------------------------------
  * csa_topk -- the top-k selector alone, over caller-provided BF16 scores [B, Nq, E]
  * (9fzt.com item 4: the selector works on BF16 index scores). Same outputs and tie rule as
  * csa_index_topk. -0 counts as +0; NaN scores are not supported.

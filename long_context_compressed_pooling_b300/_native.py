@@ -60,6 +60,7 @@ _SIGS = {
     "csa_compress": (_I, [_P, _P, _P, _I, _L, _I, _I, _L, _L, _P, _P, _P]),
     "csa_index_topk": (_I, [_P, _P, _P, _P, _I, _I, _L, _L, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "csa_index_topk_workspace_size": (_Z, [_I, _I, _L, _I, _I]),
+    "csa_index_topk_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _L, _L, _I, _I, _I, _I, _P, _P, _P]),
     "csa_topk": (_I, [_P, _I, _I, _L, _L, _I, _I, _P, _P, _P, _Z, _P]),
     "csa_topk_workspace_size": (_Z, [_I, _I, _L, _I]),
     "csa_attend": (_I, [_P, _P, _P, _L, _P, _P, _I, _P, _P, _L, _I, _I, _I, _L, _I, _I, _P, _P, _P,

@@ -149,6 +149,11 @@ int64_t hca_max_keys(int64_t E, int m, int64_t N, int W) {
 
 }  // namespace
 
+namespace csa {
+// The library's device status word on the current device (null if it cannot be resolved).
+uint32_t* device_status_word() { return status_word(); }
+}  // namespace csa
+
 extern "C" {
 
 int csa_abi_version(void) { return 1; }

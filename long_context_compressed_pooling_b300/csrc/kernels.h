@@ -10,6 +10,9 @@ namespace csa {
 
 constexpr int kNumSMs = 148;
 
+// The library's device status word on the current device (defined in abi.cu).
+uint32_t* device_status_word();
+
 // ---- block pooling --------------------------------------------------------------------------
 cudaError_t launch_compress(const uint16_t* k_raw, const uint16_t* v_raw, const float* logits,
                             int B, int64_t N, int d, int m, int64_t j_begin, int64_t n_entries,
