@@ -8,10 +8,13 @@
 // MQA layout: all H query heads of a token share one K/V head, so the heads form the M side of
 // the contraction. A CTA owns one query token and up to 64 heads (16 per warp) and walks a
 // range of 64-key chunks of that token's key list: the chunk's K and V rows are gathered with
-// 16-byte cp.async into XOR-swizzled shared memory (double-buffered), QK^T and PV run on the
-// tensor cores, and the softmax is an online (running max / sum) softmax in registers. When a
-// token's keys are split over several CTAs (decode), each writes (m, l, unnormalised O) and a
-// merge kernel combines the splits with log-sum-exp weights.
+// 16-byte cp.async into XOR-swizzled shared memory through a 3-stage pipeline, QK^T and PV run
+// on the tensor cores, and the softmax is an online (running max / sum) softmax in registers.
+// When a token's keys are split over several CTAs (decode), the splits of one token form a
+// thread-block cluster: each CTA parks its (max, sum, unnormalised O) in its own shared memory
+// and, after a hardware cluster barrier, merges a slice of the heads by reading every split's
+// partials through distributed shared memory. Very small batches that need more than 16 splits
+// per token merge through the workspace with a separate kernel instead.
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
@@ -19,7 +22,9 @@
 namespace csa {
 namespace {
 
-constexpr int kKC = 64;  // keys per chunk
+constexpr int kKC = 64;      // keys per chunk
+constexpr int kStages = 3;   // cp.async pipeline depth
+constexpr int kMaxClusterSplits = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct AttnParams {
@@ -32,11 +37,12 @@ struct AttnParams {
   const uint16_t* v_raw;
   uint16_t* out;
   float* lse;
-  float* ws_o;   // [n_splits, tokens, H, D] unnormalised partial outputs
+  float* ws_o;   // [n_splits, tokens, H, D] unnormalised partial outputs (workspace merge)
   float* ws_ml;  // [n_splits, tokens, H, 2] running max and sum
   int64_t E, N, q_pos0;
   int k, m, W, Nq, H, n_splits, tokens;
   int sparse;
+  int cluster_merge;  // splits of a token form a cluster and merge through DSMEM
   uint32_t* status;
 };
 
@@ -58,79 +64,84 @@ CSA_DEV void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Key list of one token: n_sel selected / visible entries, then the window tokens.
-struct KeyList {
-  int64_t b, tok, n_sel, w0, n_keys;
-};
+template <int D>
+constexpr size_t attend_smem_bytes() {
+  return (size_t)kStages * 2 * kKC * D * 2 + kStages * kKC;
+}
 
 template <int D, int NW>
 __global__ void __launch_bounds__(NW * 32) attend_kernel(const AttnParams p) {
   constexpr int CPR = D / 8;  // 16-byte chunks per row
   constexpr int NT = 32 * NW;
+  constexpr int ROWS = 16 * NW;     // heads of this CTA
+  constexpr int PSTRIDE = D + 4;    // padded row stride of the parked partial outputs
   extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem);          // [2][kKC][D]
-  uint16_t* Vs = Ks + 2 * kKC * D;                           // [2][kKC][D]
-  uint8_t* kmask = reinterpret_cast<uint8_t*>(Vs + 2 * kKC * D);  // [2][kKC]
+  uint16_t* Ks = reinterpret_cast<uint16_t*>(smem);                   // [kStages][kKC][D]
+  uint16_t* Vs = Ks + kStages * kKC * D;                              // [kStages][kKC][D]
+  uint8_t* kmask = reinterpret_cast<uint8_t*>(Vs + kStages * kKC * D);  // [kStages][kKC]
 
-  const int split = blockIdx.x;
+  const int split = p.cluster_merge ? (int)cluster_ctarank() : blockIdx.x;
   const int64_t tok = blockIdx.y;
-  const int h_base = blockIdx.z * (16 * NW);
+  const int h_base = blockIdx.z * ROWS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
 
-  KeyList kl;
-  kl.tok = tok;
-  kl.b = tok / p.Nq;
+  const int64_t b = tok / p.Nq;
   const int64_t t = p.q_pos0 + tok % p.Nq;
+  int64_t n_sel;
   if (p.sparse) {
-    int64_t c = p.topk_cnt[tok];
-    if (c < 0 || c > p.k) {
+    n_sel = p.topk_cnt[tok];
+    if (n_sel < 0 || n_sel > p.k) {
       if (threadIdx.x == 0) atomicOr(p.status, kFlagBadIndex);
-      c = c < 0 ? 0 : p.k;
+      n_sel = n_sel < 0 ? 0 : p.k;
     }
-    kl.n_sel = c;
   } else {
-    kl.n_sel = max((int64_t)0, min(p.E, (t + 1) / p.m));
+    n_sel = max((int64_t)0, min(p.E, (t + 1) / p.m));
   }
-  kl.w0 = max((int64_t)0, t - p.W + 1);
-  const int64_t n_win = p.W > 0 ? (t - kl.w0 + 1) : 0;
-  kl.n_keys = kl.n_sel + n_win;
-  const int64_t n_chunks = (kl.n_keys + kKC - 1) / kKC;
+  const int64_t w0 = max((int64_t)0, t - p.W + 1);
+  const int64_t n_keys = n_sel + (p.W > 0 ? (t - w0 + 1) : 0);
+  const int64_t n_chunks = (n_keys + kKC - 1) / kKC;
   const int64_t c_begin = n_chunks * split / p.n_splits;
   const int64_t c_end = n_chunks * (split + 1) / p.n_splits;
 
-  auto load_chunk = [&](int64_t c, int buf) {
-    uint16_t* kd = Ks + buf * kKC * D;
-    uint16_t* vd = Vs + buf * kKC * D;
+  auto load_chunk = [&](int64_t c, int st) {
+    uint16_t* kd = Ks + st * kKC * D;
+    uint16_t* vd = Vs + st * kKC * D;
     for (int x = threadIdx.x; x < kKC * CPR; x += NT) {
       const int r = x / CPR, cc = x % CPR;
       const int64_t key = c * kKC + r;
       const uint16_t* ks = p.k_raw;
       const uint16_t* vs = p.v_raw;
-      bool valid = key < kl.n_keys;
+      bool valid = key < n_keys;
       if (valid) {
-        if (key < kl.n_sel) {
-          int64_t j = p.sparse ? (int64_t)p.topk_idx[kl.tok * p.k + key] : key;
+        if (key < n_sel) {
+          const int64_t j = p.sparse ? (int64_t)p.topk_idx[tok * p.k + key] : key;
           if (j < 0 || j >= p.E) {
             valid = false;
             if (cc == 0) atomicOr(p.status, kFlagBadIndex);
           } else {
-            ks = p.k_cmp + (kl.b * p.E + j) * D;
-            vs = p.v_cmp + (kl.b * p.E + j) * D;
+            ks = p.k_cmp + (b * p.E + j) * D;
+            vs = p.v_cmp + (b * p.E + j) * D;
           }
         } else {
-          const int64_t u = kl.w0 + (key - kl.n_sel);
-          ks = p.k_raw + (kl.b * p.N + u) * D;
-          vs = p.v_raw + (kl.b * p.N + u) * D;
+          const int64_t u = w0 + (key - n_sel);
+          ks = p.k_raw + (b * p.N + u) * D;
+          vs = p.v_raw + (b * p.N + u) * D;
         }
       }
       const int phys = r * CPR + (cc ^ (r & 7));
       cp_async_16(kd + phys * 8, valid ? ks + cc * 8 : p.k_raw, valid ? 16u : 0u);
       cp_async_16(vd + phys * 8, valid ? vs + cc * 8 : p.v_raw, valid ? 16u : 0u);
-      if (cc == 0) kmask[buf * kKC + r] = valid ? 1 : 0;
+      if (cc == 0) kmask[st * kKC + r] = valid ? 1 : 0;
     }
-    cp_async_commit();
   };
+
+  // Put the first chunks in flight before anything else.
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (c_begin + s < c_end) load_chunk(c_begin + s, s);
+    cp_async_commit();
+  }
 
   // Q fragments (rows h0 = h_base + warp*16 + g and h0 + 8), A layout of m16n8k16.
   const int h0 = h_base + warp * 16 + g, h1 = h0 + 8;
@@ -152,26 +163,23 @@ __global__ void __launch_bounds__(NW * 32) attend_kernel(const AttnParams p) {
 #pragma unroll
   for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const int mi = lane >> 3, rr = lane & 7;
 
-  if (c_begin < c_end) load_chunk(c_begin, 0);
   for (int64_t c = c_begin; c < c_end; ++c) {
-    const int buf = (int)((c - c_begin) & 1);
-    if (c + 1 < c_end) {
-      load_chunk(c + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    const int it = (int)(c - c_begin);
+    if (c + kStages - 1 < c_end) load_chunk(c + kStages - 1, (it + kStages - 1) % kStages);
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
     __syncthreads();
-    const uint32_t kbase = smem_addr(Ks + buf * kKC * D);
-    const uint32_t vbase = smem_addr(Vs + buf * kKC * D);
-    const uint8_t* msk = kmask + buf * kKC;
+    const int st = it % kStages;
+    const uint32_t kbase = smem_addr(Ks + st * kKC * D);
+    const uint32_t vbase = smem_addr(Vs + st * kKC * D);
+    const uint8_t* msk = kmask + st * kKC;
 
     // ---- S = Q K^T over 64 keys ----
     float s[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
-    const int mi = lane >> 3, rr = lane & 7;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
@@ -243,8 +251,9 @@ __global__ void __launch_bounds__(NW * 32) attend_kernel(const AttnParams p) {
     }
     __syncthreads();
   }
+  cp_async_wait<0>();
 
-  // ---- finish: quad-reduce the row sums, then store ----
+  // ---- finish: quad-reduce the row sums, then store / park / merge ----
 #pragma unroll
   for (int o2 = 1; o2 < 4; o2 <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, o2);
@@ -266,7 +275,9 @@ __global__ void __launch_bounds__(NW * 32) attend_kernel(const AttnParams p) {
       if (h0 < p.H) p.lse[tok * p.H + h0] = l0 > 0.f ? m0 + logf(l0) : -INFINITY;
       if (h1 < p.H) p.lse[tok * p.H + h1] = l1 > 0.f ? m1 + logf(l1) : -INFINITY;
     }
-  } else {
+    return;
+  }
+  if (!p.cluster_merge) {
     const int64_t sb = ((int64_t)split * p.tokens + tok) * p.H;
 #pragma unroll
     for (int dt = 0; dt < D / 8; ++dt) {
@@ -280,10 +291,61 @@ __global__ void __launch_bounds__(NW * 32) attend_kernel(const AttnParams p) {
       if (h0 < p.H) *reinterpret_cast<float2*>(p.ws_ml + (sb + h0) * 2) = make_float2(m0, l0);
       if (h1 < p.H) *reinterpret_cast<float2*>(p.ws_ml + (sb + h1) * 2) = make_float2(m1, l1);
     }
+    return;
   }
+  // Cluster merge: park this split's partials in shared memory (the pipeline buffers are free).
+  float* po = reinterpret_cast<float*>(smem);  // [ROWS][PSTRIDE]
+  float* pml = po + ROWS * PSTRIDE;            // [ROWS][2]
+  const int r0 = warp * 16 + g, r1 = r0 + 8;
+#pragma unroll
+  for (int dt = 0; dt < D / 8; ++dt) {
+    const int d0 = dt * 8 + 2 * tq;
+    *reinterpret_cast<float2*>(po + r0 * PSTRIDE + d0) = make_float2(o[dt][0], o[dt][1]);
+    *reinterpret_cast<float2*>(po + r1 * PSTRIDE + d0) = make_float2(o[dt][2], o[dt][3]);
+  }
+  if (tq == 0) {
+    *reinterpret_cast<float2*>(pml + r0 * 2) = make_float2(m0, l0);
+    *reinterpret_cast<float2*>(pml + r1 * 2) = make_float2(m1, l1);
+  }
+  __syncthreads();
+  cluster_sync();
+  // This CTA merges rows [rb, re) of the head group, D/4 float4 columns per row.
+  const int S = p.n_splits;
+  const int rows_per = (ROWS + S - 1) / S;
+  const int rb = split * rows_per, re = min(ROWS, rb + rows_per);
+  constexpr int C4 = D / 4;
+  for (int x = threadIdx.x; x < (re - rb) * C4; x += NT) {
+    const int row = rb + x / C4, c4 = x % C4;
+    const int h = h_base + row;
+    if (h >= p.H) continue;
+    float M = -INFINITY;
+    for (int sp = 0; sp < S; ++sp) M = fmaxf(M, dsmem_ld_f32x2(pml + row * 2, sp).x);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float L = 0.f;
+    if (M != -INFINITY) {
+      for (int sp = 0; sp < S; ++sp) {
+        const float2 ml = dsmem_ld_f32x2(pml + row * 2, sp);
+        if (ml.x == -INFINITY) continue;
+        const float w = expf(ml.x - M);
+        L += w * ml.y;
+        const float4 v = dsmem_ld_f32x4(po + row * PSTRIDE + c4 * 4, sp);
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(p.out + (tok * p.H + h) * D + c4 * 4) = pk;
+    if (p.lse != nullptr && c4 == 0) p.lse[tok * p.H + h] = L > 0.f ? M + logf(L) : -INFINITY;
+  }
+  cluster_sync();  // no CTA leaves while another may still read its shared memory
 }
 
-// Combines split-K partials: out = sum_s w_s O_s / sum_s w_s l_s with w_s = exp(m_s - max m).
+// Combines workspace split-K partials: out = sum_s w_s O_s / sum_s w_s l_s, w_s = exp(m_s - max m).
 template <int D>
 __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ ws_o,
                                                   const float* __restrict__ ws_ml, int n_splits,
@@ -317,41 +379,81 @@ __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ ws_
   if (lse != nullptr && lane == 0) lse[th] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
+struct SplitPlan {
+  int n_splits;
+  int cluster;  // 1: merge inside a cluster of n_splits CTAs
+};
+
+SplitPlan plan_splits(int tokens, int H, int64_t max_keys) {
+  const int64_t groups = (H + 63) / 64;
+  const int64_t chunks = (max_keys + kKC - 1) / kKC;
+  const int64_t units = (int64_t)tokens * groups;
+  const int64_t target = (int64_t)kNumSMs * 2;
+  if (units >= target || chunks <= 1) return {1, 0};
+  int64_t s = (target + units - 1) / units;
+  if (s > chunks) s = chunks;
+  if (s <= 1) return {1, 0};
+  if (s <= kMaxClusterSplits) return {(int)s, 1};
+  return {(int)s, 0};
+}
+
 template <int D, int NW>
-cudaError_t launch_attend_t(const AttnParams& prm, int groups, cudaStream_t stream) {
-  const size_t smem = (size_t)2 * 2 * kKC * D * 2 + 2 * kKC;
+cudaError_t launch_attend_t(AttnParams prm, int groups, cudaStream_t stream) {
+  const size_t smem = attend_smem_bytes<D>();
   auto kern = attend_kernel<D, NW>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)prm.n_splits, (unsigned)prm.tokens, (unsigned)groups);
+  if (prm.cluster_merge && prm.n_splits > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)prm.n_splits, (unsigned)prm.tokens, (unsigned)groups);
+  cfg.blockDim = dim3(NW * 32, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = prm.cluster_merge ? (unsigned)prm.n_splits : 1u;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (prm.cluster_merge && prm.n_splits > 8) {
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters == 0) {
+      (void)cudaGetLastError();
+      return cudaErrorNotSupported;  // caller falls back to the workspace merge
+    }
+  }
   {
     ProfScope prof(stream, prm.sparse ? "csa_attend" : "hca_attend");
-    kern<<<grid, NW * 32, smem, stream>>>(prm);
+    e = cudaLaunchKernelEx(&cfg, kern, prm);
   }
-  e = cudaGetLastError();
-  if (e != cudaSuccess || prm.n_splits == 1) return e;
+  if (e != cudaSuccess || prm.n_splits == 1 || prm.cluster_merge) return e;
   ProfScope prof(stream, "lse_merge");
   merge_kernel<D><<<(unsigned)((int64_t)prm.tokens * prm.H), 32, 0, stream>>>(
       prm.ws_o, prm.ws_ml, prm.n_splits, prm.tokens, prm.H, prm.out, prm.lse);
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_d(AttnParams prm, int groups, int nw, cudaStream_t stream) {
+  if (nw == 1) return launch_attend_t<D, 1>(prm, groups, stream);
+  if (nw == 2) return launch_attend_t<D, 2>(prm, groups, stream);
+  return launch_attend_t<D, 4>(prm, groups, stream);
+}
+
 }  // namespace
 
 int plan_attend_splits(int tokens, int H, int64_t max_keys) {
-  const int64_t groups = (H + 63) / 64;
-  const int64_t chunks = (max_keys + kKC - 1) / kKC;
-  const int64_t units = (int64_t)tokens * groups;
-  const int64_t target = (int64_t)kNumSMs * 2;
-  if (units >= target || chunks <= 1) return 1;
-  int64_t s = (target + units - 1) / units;
-  if (s > chunks) s = chunks;
-  return (int)(s < 1 ? 1 : s);
+  return plan_splits(tokens, H, max_keys).n_splits;
 }
 
 size_t attend_workspace_bytes(int tokens, int H, int d, int64_t max_keys) {
-  const int s = plan_attend_splits(tokens, H, max_keys);
+  // The workspace covers the non-cluster merge, which is also the fallback of the cluster one.
+  const int s = plan_splits(tokens, H, max_keys).n_splits;
   if (s <= 1) return 0;
   return (size_t)s * tokens * H * (size_t)(d + 2) * sizeof(float);
 }
@@ -379,25 +481,23 @@ cudaError_t launch_attend(const AttendArgs& a, int64_t max_keys, void* ws, uint3
   prm.tokens = a.B * a.Nq;
   prm.sparse = a.topk_idx != nullptr;
   prm.status = status;
-  prm.n_splits = plan_attend_splits(prm.tokens, a.H, max_keys);
+  const SplitPlan sp = plan_splits(prm.tokens, a.H, max_keys);
+  prm.n_splits = sp.n_splits;
+  prm.cluster_merge = sp.cluster;
   prm.ws_o = reinterpret_cast<float*>(ws);
   prm.ws_ml = prm.ws_o + (size_t)prm.n_splits * prm.tokens * a.H * a.d;
   if (prm.tokens == 0) return cudaSuccess;
   const int groups = (a.H + 63) / 64;
-  const int nw = a.H >= 64 ? 4 : (a.H + 15) / 16;
-  if (a.d == 128) {
-    if (nw == 4) return launch_attend_t<128, 4>(prm, groups, stream);
-    if (nw == 2) return launch_attend_t<128, 2>(prm, groups, stream);
-    if (nw == 1) return launch_attend_t<128, 1>(prm, groups, stream);
-    return launch_attend_t<128, 4>(prm, groups, stream);
+  const int nw = a.H >= 64 ? 4 : (a.H + 15) / 16 >= 3 ? 4 : (a.H + 15) / 16;
+  if (a.d != 128 && a.d != 64) return cudaErrorInvalidValue;
+  cudaError_t e = a.d == 128 ? launch_d<128>(prm, groups, nw, stream)
+                             : launch_d<64>(prm, groups, nw, stream);
+  if (e == cudaErrorNotSupported && prm.cluster_merge) {
+    prm.cluster_merge = 0;
+    e = a.d == 128 ? launch_d<128>(prm, groups, nw, stream)
+                   : launch_d<64>(prm, groups, nw, stream);
   }
-  if (a.d == 64) {
-    if (nw == 4) return launch_attend_t<64, 4>(prm, groups, stream);
-    if (nw == 2) return launch_attend_t<64, 2>(prm, groups, stream);
-    if (nw == 1) return launch_attend_t<64, 1>(prm, groups, stream);
-    return launch_attend_t<64, 4>(prm, groups, stream);
-  }
-  return cudaErrorInvalidValue;
+  return e;
 }
 
 }  // namespace csa

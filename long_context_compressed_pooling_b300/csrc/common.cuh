@@ -217,4 +217,49 @@ CSA_DEV void tmem_st8_fill(uint32_t taddr, uint32_t v) {
       : "memory");
 }
 
+// ---------------------------------------------------------------------------------------------
+// thread-block clusters and distributed shared memory
+// ---------------------------------------------------------------------------------------------
+CSA_DEV uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+CSA_DEV uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Hardware cluster barrier (all threads of every CTA of the cluster); release/acquire ordering
+// makes shared-memory writes before it visible to distributed-shared-memory reads after it.
+CSA_DEV void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+// Reads a 32-bit word at the same shared-memory offset in CTA `cta` of this cluster.
+CSA_DEV uint32_t dsmem_ld_u32(const void* local_ptr, uint32_t cta) {
+  uint32_t ra, v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local_ptr)), "r"(cta));
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+CSA_DEV float4 dsmem_ld_f32x4(const void* local_ptr, uint32_t cta) {
+  uint32_t ra;
+  float4 v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local_ptr)), "r"(cta));
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(ra)
+               : "memory");
+  return v;
+}
+CSA_DEV float2 dsmem_ld_f32x2(const void* local_ptr, uint32_t cta) {
+  uint32_t ra;
+  float2 v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local_ptr)), "r"(cta));
+  asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(ra) : "memory");
+  return v;
+}
+
 }  // namespace csa

@@ -99,6 +99,100 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restric
   }
 }
 
+// Large blocks (m >= 32): one CTA per entry. The block's softmax weights are computed once into
+// shared memory; thread (slice, chunk) accumulates the tokens slice, slice+TS, ... of 16-byte
+// channel chunk `chunk` for K and V, so all of a thread's loads are independent and in flight
+// together; the TS partial sums are then reduced through shared memory.
+template <int CH>
+__global__ void __launch_bounds__(256) compress_large_kernel(const uint16_t* __restrict__ k_raw,
+                                                             const uint16_t* __restrict__ v_raw,
+                                                             const float* __restrict__ logits,
+                                                             uint16_t* __restrict__ k_cmp,
+                                                             uint16_t* __restrict__ v_cmp, int B,
+                                                             int64_t N, int m, int64_t j_begin,
+                                                             int64_t n_entries) {
+  constexpr int D = CH * 8;
+  constexpr int TS = 256 / CH;  // token slices
+  __shared__ float wexp[256];
+  __shared__ float red[2];
+  __shared__ float part[2][TS][CH * 8 + 1];
+  const int tid = threadIdx.x;
+  const int c = tid % CH, ts = tid / CH;
+  const int64_t E = N / m;
+  for (int64_t w = blockIdx.x; w < (int64_t)B * n_entries; w += gridDim.x) {
+    const int64_t b = w / n_entries, j = j_begin + w % n_entries;
+    const int64_t tok0 = b * N + j * m;
+    // softmax weights of the block (m <= 256)
+    const float x = tid < m ? __ldg(logits + tok0 + tid) : -INFINITY;
+    float mx = x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((tid & 31) == 0) wexp[tid >> 5] = mx;  // per-warp maxima (scratch)
+    __syncthreads();
+    if (tid == 0) {
+      float M = wexp[0];
+      for (int q = 1; q < 8; ++q) M = fmaxf(M, wexp[q]);
+      red[0] = M;
+    }
+    __syncthreads();
+    const float e = tid < m ? expf(x - red[0]) : 0.f;
+    float sm = e;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    __syncthreads();
+    if ((tid & 31) == 0) wexp[tid >> 5] = sm;
+    __syncthreads();
+    if (tid == 0) {
+      float S = 0.f;
+      for (int q = 0; q < 8; ++q) S += wexp[q];
+      red[1] = S;
+    }
+    __syncthreads();
+    wexp[tid] = e;
+    __syncthreads();
+
+    float acc_k[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float acc_v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const uint16_t* kp = k_raw + tok0 * D + c * 8;
+    const uint16_t* vp = v_raw + tok0 * D + c * 8;
+    int i = ts;
+    for (; i + 3 * TS < m; i += 4 * TS) {
+      uint4 kv[4], vv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        kv[u] = ldg_stream(kp + (int64_t)(i + u * TS) * D);
+        vv[u] = ldg_stream(vp + (int64_t)(i + u * TS) * D);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc8(acc_k, kv[u], wexp[i + u * TS]);
+        acc8(acc_v, vv[u], wexp[i + u * TS]);
+      }
+    }
+    for (; i < m; i += TS) {
+      acc8(acc_k, ldg_stream(kp + (int64_t)i * D), wexp[i]);
+      acc8(acc_v, ldg_stream(vp + (int64_t)i * D), wexp[i]);
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      part[0][ts][c * 8 + q] = acc_k[q];
+      part[1][ts][c * 8 + q] = acc_v[q];
+    }
+    __syncthreads();
+    // 2 * D outputs; thread tid reduces output channel tid of K (tid < D) or V (tid >= D)
+    const float inv = 1.0f / red[1];
+    for (int o = tid; o < 2 * D; o += 256) {
+      const int kv = o / D, ch = o % D;
+      float s = 0.f;
+#pragma unroll
+      for (int q = 0; q < TS; ++q) s += part[kv][q][ch];
+      uint16_t* dst = (kv == 0 ? k_cmp : v_cmp) + (b * E + j) * D + ch;
+      *dst = f32_to_bf16_bits(s * inv);
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_compress(const uint16_t* k_raw, const uint16_t* v_raw, const float* logits,
@@ -106,6 +200,29 @@ cudaError_t launch_compress(const uint16_t* k_raw, const uint16_t* v_raw, const 
                             uint16_t* k_cmp, uint16_t* v_cmp, cudaStream_t stream) {
   if (n_entries <= 0 || B <= 0) return cudaSuccess;
   const int ch = d / 8;
+  if (m >= 32 && ch <= 32) {
+    int64_t blocks = (int64_t)B * n_entries;
+    const int64_t cap = (int64_t)kNumSMs * 8;
+    if (blocks > cap) blocks = cap;
+    ProfScope prof(stream, "compress");
+    switch (ch) {
+      case 8:
+        compress_large_kernel<8><<<(unsigned)blocks, 256, 0, stream>>>(
+            k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
+        break;
+      case 16:
+        compress_large_kernel<16><<<(unsigned)blocks, 256, 0, stream>>>(
+            k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
+        break;
+      case 32:
+        compress_large_kernel<32><<<(unsigned)blocks, 256, 0, stream>>>(
+            k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
+        break;
+      default:
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+  }
   const int64_t total = (int64_t)B * n_entries * ch;
   const int threads = 256;
   int64_t blocks = (total + threads - 1) / threads;

@@ -3,10 +3,18 @@
 // entries). Order: score descending, ties to the lower entry index; output sorted ascending,
 // padded with -1; count = min(k, visible).
 //
-// One CTA per query row. BF16 scores map to order-preserving 16-bit keys, so selection is an
-// exact two-digit radix select (high byte, then low byte) followed by an ordered compaction:
-// everything above the threshold key T, plus the lowest-index entries equal to T until k are
-// taken. The row is cached in shared memory when it fits; otherwise it is re-read from L2.
+// BF16 scores map to order-preserving 16-bit keys, so selection is an exact two-digit radix
+// select (high byte, then low byte) followed by an ordered compaction: every key above the
+// threshold T, plus the lowest-index keys equal to T until k are taken.
+//
+// One thread-block cluster per query row. The row is split into C contiguous chunks, one per
+// CTA, staged in shared memory. Each CTA builds its chunk's 256-bin histograms with
+// warp-aggregated shared atomics; the cluster sums them through distributed shared memory
+// after a hardware cluster barrier, and every CTA derives the same threshold. For the
+// compaction each CTA counts its keys above / equal to T, reads the counts of the lower-ranked
+// CTAs of its cluster, and writes its selected indices at their final, ascending positions.
+// Decode rows (few rows, up to 262144 entries) use clusters of up to 16 CTAs; prefill (thousands
+// of rows) uses one CTA per row. No grid-wide synchronisation and no spin waits are involved.
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
@@ -15,19 +23,27 @@ namespace csa {
 namespace {
 
 constexpr int kTopkThreads = 512;
-constexpr int kSmemKeys = 48 * 1024;  // keys cached in shared memory (96 KB)
+constexpr int kMaxChunkKeys = 16384;  // keys one CTA stages in shared memory (32 KB)
 
 CSA_DEV uint32_t order_key(uint32_t bits) {
   if (bits == 0x8000u) bits = 0u;  // -0 counts as +0
   return (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
 }
 
-// Finds the bin b with count(bins > b) < need <= count(bins >= b) over 256 bins; returns the bin
-// and count(bins > b). Called by all threads; uses warp 0.
+// Adds one to hist[bin] for every lane with valid set; lanes sharing a bin add once together.
+// Must be called by all 32 lanes of the warp.
+CSA_DEV void hist_add_warp(uint32_t* hist, uint32_t bin, bool valid) {
+  const uint32_t key = valid ? bin : 0xFFFFFFFFu;
+  const unsigned peers = __match_any_sync(0xffffffffu, key);
+  if (valid && (threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1))
+    atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+}
+
+// Finds the bin b with count(bins > b) < need <= count(bins >= b) over 256 bins; writes the bin
+// and count(bins > b). Executed by warp 0.
 CSA_DEV void select_bin(const uint32_t* hist, uint32_t need, int* out_bin, uint32_t* out_above) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
-    // lane owns bins [248 - 8*lane .. 255 - 8*lane] (descending blocks of 8)
     uint32_t local[8];
     uint32_t tot = 0;
 #pragma unroll
@@ -35,11 +51,10 @@ CSA_DEV void select_bin(const uint32_t* hist, uint32_t need, int* out_bin, uint3
       local[q] = hist[255 - (lane * 8 + q)];
       tot += local[q];
     }
-    // inclusive scan over lanes (descending bin order)
     uint32_t inc = tot;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += v;
     }
     const uint32_t exc = inc - tot;
@@ -57,125 +72,212 @@ CSA_DEV void select_bin(const uint32_t* hist, uint32_t need, int* out_bin, uint3
   }
 }
 
-// Block-wide exclusive scan of two counters (one per thread).
-CSA_DEV void block_exclusive_scan2(uint32_t a, uint32_t b, uint32_t* ex_a, uint32_t* ex_b,
-                                   uint32_t* warp_a, uint32_t* warp_b) {
+// Block-wide exclusive scan of two counters (one pair per thread); also returns the totals.
+CSA_DEV void block_scan2(uint32_t a, uint32_t b, uint32_t* ex_a, uint32_t* ex_b, uint32_t* tot_a,
+                         uint32_t* tot_b, uint32_t* wa, uint32_t* wb) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   uint32_t ia = a, ib = b;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    uint32_t va = __shfl_up_sync(0xffffffffu, ia, o);
-    uint32_t vb = __shfl_up_sync(0xffffffffu, ib, o);
+    const uint32_t va = __shfl_up_sync(0xffffffffu, ia, o);
+    const uint32_t vb = __shfl_up_sync(0xffffffffu, ib, o);
     if (lane >= o) {
       ia += va;
       ib += vb;
     }
   }
   if (lane == 31) {
-    warp_a[w] = ia;
-    warp_b[w] = ib;
+    wa[w] = ia;
+    wb[w] = ib;
   }
   __syncthreads();
   if (w == 0) {
     const int nw = blockDim.x >> 5;
-    uint32_t xa = lane < nw ? warp_a[lane] : 0u, xb = lane < nw ? warp_b[lane] : 0u;
+    const uint32_t xa = lane < nw ? wa[lane] : 0u, xb = lane < nw ? wb[lane] : 0u;
     uint32_t sa = xa, sb = xb;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      uint32_t va = __shfl_up_sync(0xffffffffu, sa, o);
-      uint32_t vb = __shfl_up_sync(0xffffffffu, sb, o);
+      const uint32_t va = __shfl_up_sync(0xffffffffu, sa, o);
+      const uint32_t vb = __shfl_up_sync(0xffffffffu, sb, o);
       if (lane >= o) {
         sa += va;
         sb += vb;
       }
     }
     if (lane < nw) {
-      warp_a[lane] = sa - xa;
-      warp_b[lane] = sb - xb;
+      wa[lane] = sa - xa;
+      wb[lane] = sb - xb;
+    }
+    if (lane == nw - 1) {
+      wa[32] = sa;
+      wb[32] = sb;
     }
   }
   __syncthreads();
-  *ex_a = warp_a[w] + ia - a;
-  *ex_b = warp_b[w] + ib - b;
+  *ex_a = wa[w] + ia - a;
+  *ex_b = wb[w] + ib - b;
+  *tot_a = wa[32];
+  *tot_b = wb[32];
+  __syncthreads();  // wa / wb are reused by the next call
 }
+
+struct TopkShared {
+  uint32_t hist1[256];
+  uint32_t hist2[256];
+  uint32_t gsum[256];
+  uint32_t wa[33], wb[33];
+  uint32_t cta_gt, cta_eq;  // this CTA's keys above / equal to the threshold (read by the cluster)
+  int bin;
+  uint32_t above;
+};
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __restrict__ scores,
                                                             int Nq, int64_t q_pos0, int64_t E,
-                                                            int m, int k, int64_t cap,
+                                                            int m, int k, int cap,
                                                             int32_t* __restrict__ topk_idx,
                                                             int32_t* __restrict__ topk_cnt) {
-  extern __shared__ uint16_t skeys[];  // `cap` keys
-  __shared__ uint32_t hist[256];
-  __shared__ uint32_t warp_a[32], warp_b[32];
-  __shared__ int sh_bin;
-  __shared__ uint32_t sh_above;
-
-  const int64_t row = blockIdx.x;  // b * Nq + i
+  extern __shared__ uint16_t skeys[];  // `cap` keys: this CTA's chunk when it fits
+  __shared__ TopkShared sh;
+  const uint32_t C = cluster_nctarank();
+  const uint32_t rank = cluster_ctarank();
+  const int64_t row = blockIdx.y;  // b * Nq + i
   const int64_t t = q_pos0 + (row % Nq);
   const int64_t n = max((int64_t)0, min(E, (t + 1) / m));
   const uint16_t* src = scores + row * E;
   int32_t* out = topk_idx + row * (int64_t)k;
   const int tid = threadIdx.x, nt = blockDim.x;
 
-  if (n <= k) {
-    for (int64_t r = tid; r < k; r += nt) out[r] = (r < n) ? (int32_t)r : -1;
-    if (tid == 0) topk_cnt[row] = (int32_t)n;
+  if (n <= k) {  // uniform over the cluster: every CTA of it works on this row
+    for (int64_t r = (int64_t)rank * nt + tid; r < k; r += (int64_t)C * nt)
+      out[r] = (r < n) ? (int32_t)r : -1;
+    if (rank == 0 && tid == 0) topk_cnt[row] = (int32_t)n;
     return;
   }
-  const bool cached = n <= cap;
-  if (cached) {
-    for (int64_t r = tid; r < n; r += nt) skeys[r] = (uint16_t)order_key(src[r]);
-  }
-  auto key_at = [&](int64_t r) -> uint32_t {
-    return cached ? (uint32_t)skeys[r] : order_key(src[r]);
+
+  const int64_t L = (n + C - 1) / C;
+  const int64_t lo = min(n, (int64_t)rank * L), hi = min(n, lo + L);
+  const int len = (int)(hi - lo);
+  const bool cached = len <= cap;
+  if (cached)
+    for (int r = tid; r < len; r += nt) skeys[r] = (uint16_t)order_key(src[lo + r]);
+  auto key_at = [&](int r) -> uint32_t {
+    return cached ? (uint32_t)skeys[r] : order_key(src[lo + r]);
   };
-
-  // ---- digit 1: high byte ----
-  for (int q = tid; q < 256; q += nt) hist[q] = 0u;
-  __syncthreads();
-  for (int64_t r = tid; r < n; r += nt) atomicAdd(&hist[key_at(r) >> 8], 1u);
-  __syncthreads();
-  select_bin(hist, (uint32_t)k, &sh_bin, &sh_above);
-  __syncthreads();
-  const uint32_t hi = (uint32_t)sh_bin;
-  const uint32_t above_hi = sh_above;
-  __syncthreads();
-  // ---- digit 2: low byte within the high bin ----
-  for (int q = tid; q < 256; q += nt) hist[q] = 0u;
-  __syncthreads();
-  for (int64_t r = tid; r < n; r += nt) {
-    const uint32_t kk = key_at(r);
-    if ((kk >> 8) == hi) atomicAdd(&hist[kk & 0xFFu], 1u);
+  for (int q = tid; q < 256; q += nt) {
+    sh.hist1[q] = 0u;
+    sh.hist2[q] = 0u;
   }
   __syncthreads();
-  select_bin(hist, (uint32_t)k - above_hi, &sh_bin, &sh_above);
-  __syncthreads();
-  const uint32_t T = (hi << 8) | (uint32_t)sh_bin;
-  const uint32_t n_gt = above_hi + sh_above;
-  const uint32_t need_eq = (uint32_t)k - n_gt;
 
-  // ---- ordered compaction over contiguous per-thread segments ----
-  const int64_t seg = (n + nt - 1) / nt;
-  const int64_t r0 = min(n, seg * tid), r1 = min(n, r0 + seg);
-  uint32_t c_gt = 0, c_eq = 0;
-  for (int64_t r = r0; r < r1; ++r) {
-    const uint32_t kk = key_at(r);
-    c_gt += kk > T;
-    c_eq += kk == T;
+  // ---- digit 1: high byte --------------------------------------------------------------------
+  for (int base = 0; base < len; base += nt) {
+    const int r = base + tid;
+    const bool v = r < len;
+    hist_add_warp(sh.hist1, v ? key_at(r) >> 8 : 0u, v);
   }
-  uint32_t gt_before, eq_before;
-  block_exclusive_scan2(c_gt, c_eq, &gt_before, &eq_before, warp_a, warp_b);
-  for (int64_t r = r0; r < r1; ++r) {
-    const uint32_t kk = key_at(r);
-    if (kk > T) {
-      out[gt_before + min(eq_before, need_eq)] = (int32_t)r;
-      ++gt_before;
-    } else if (kk == T) {
-      if (eq_before < need_eq) out[gt_before + eq_before] = (int32_t)r;
-      ++eq_before;
+  __syncthreads();
+  cluster_sync();
+  for (int q = tid; q < 256; q += nt) {
+    uint32_t s = 0;
+    for (uint32_t c = 0; c < C; ++c) s += dsmem_ld_u32(&sh.hist1[q], c);
+    sh.gsum[q] = s;
+  }
+  __syncthreads();
+  select_bin(sh.gsum, (uint32_t)k, &sh.bin, &sh.above);
+  __syncthreads();
+  const uint32_t hi_byte = (uint32_t)sh.bin;
+  const uint32_t above_hi = sh.above;
+
+  // ---- digit 2: low byte inside the high bin -------------------------------------------------
+  for (int base = 0; base < len; base += nt) {
+    const int r = base + tid;
+    uint32_t kk = 0;
+    bool v = r < len;
+    if (v) {
+      kk = key_at(r);
+      v = (kk >> 8) == hi_byte;
+    }
+    hist_add_warp(sh.hist2, kk & 0xFFu, v);
+  }
+  __syncthreads();
+  cluster_sync();
+  for (int q = tid; q < 256; q += nt) {
+    uint32_t s = 0;
+    for (uint32_t c = 0; c < C; ++c) s += dsmem_ld_u32(&sh.hist2[q], c);
+    sh.gsum[q] = s;
+  }
+  __syncthreads();
+  select_bin(sh.gsum, (uint32_t)k - above_hi, &sh.bin, &sh.above);
+  __syncthreads();
+  const uint32_t T = (hi_byte << 8) | (uint32_t)sh.bin;
+  const uint32_t need_eq = (uint32_t)k - (above_hi + sh.above);
+
+  // ---- ordered compaction: rounds of nt groups of 8 consecutive keys -------------------------
+  const int groups = (len + 7) / 8;
+  const int rounds = (groups + nt - 1) / nt;
+  uint32_t my_gt = 0, my_eq = 0;
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int g = rd * nt + tid;
+    for (int j = 0; j < 8; ++j) {
+      const int r = g * 8 + j;
+      if (g < groups && r < len) {
+        const uint32_t kk = key_at(r);
+        my_gt += kk > T;
+        my_eq += kk == T;
+      }
     }
   }
-  if (tid == 0) topk_cnt[row] = k;
+  uint32_t ex_a, ex_b, cta_gt, cta_eq;
+  block_scan2(my_gt, my_eq, &ex_a, &ex_b, &cta_gt, &cta_eq, sh.wa, sh.wb);
+  if (tid == 0) {
+    sh.cta_gt = cta_gt;
+    sh.cta_eq = cta_eq;
+  }
+  __syncthreads();
+  cluster_sync();
+  uint32_t gt_before = 0, eq_before = 0;  // keys of the lower-ranked CTAs of this row
+  for (uint32_t c = 0; c < rank; ++c) {
+    gt_before += dsmem_ld_u32(&sh.cta_gt, c);
+    eq_before += dsmem_ld_u32(&sh.cta_eq, c);
+  }
+  for (int rd = 0; rd < rounds; ++rd) {
+    const int g = rd * nt + tid;
+    uint32_t c_gt = 0, c_eq = 0;
+    uint32_t keys8[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = g * 8 + j;
+      keys8[j] = (g < groups && r < len) ? key_at(r) : 0u;  // 0 is below every real key
+      c_gt += keys8[j] > T;
+      c_eq += keys8[j] == T;
+    }
+    uint32_t xg, xe, tg, te;
+    block_scan2(c_gt, c_eq, &xg, &xe, &tg, &te, sh.wa, sh.wb);
+    uint32_t gb = gt_before + xg, eb = eq_before + xe;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t kk = keys8[j];
+      const int64_t idx = lo + (int64_t)g * 8 + j;
+      if (kk > T) {
+        out[gb + min(eb, need_eq)] = (int32_t)idx;
+        ++gb;
+      } else if (kk == T) {
+        if (eb < need_eq) out[gb + eb] = (int32_t)idx;
+        ++eb;
+      }
+    }
+    gt_before += tg;
+    eq_before += te;
+  }
+  if (rank == 0 && tid == 0) topk_cnt[row] = k;
+  cluster_sync();  // no CTA leaves while another may still read its shared memory
+}
+
+int pick_cluster(int64_t rows, int64_t n_max) {
+  int C = 1;
+  while (C < 16 && rows * C < kNumSMs && n_max / (2 * C) >= 2048) C <<= 1;
+  while (C < 16 && (n_max + C - 1) / C > kMaxChunkKeys) C <<= 1;
+  return C;
 }
 
 }  // namespace
@@ -184,17 +286,40 @@ cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, i
                         int k, int32_t* topk_idx, int32_t* topk_cnt, cudaStream_t stream) {
   const int64_t rows = (int64_t)B * Nq;
   if (rows <= 0) return cudaSuccess;
-  int64_t max_vis = min(E, (q_pos0 + Nq) / m);
-  if (max_vis < 0) max_vis = 0;
-  const int64_t cap = max_vis > k ? min(max_vis, (int64_t)kSmemKeys) : 0;
-  const size_t smem = (size_t)cap * 2;
+  int64_t n_max = min(E, (q_pos0 + Nq) / m);
+  if (n_max < 0) n_max = 0;
+  int C = pick_cluster(rows, n_max);
   cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemKeys * 2);
+                                       kMaxChunkKeys * 2);
   if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  int cap = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kTopkThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Clusters of 16 are a non-portable size: fall back to 8 if this GPU cannot hold one.
+  for (;; C >>= 1) {
+    const int64_t chunk = (n_max + C - 1) / C;
+    cap = (n_max > k && chunk <= kMaxChunkKeys) ? (int)chunk : 0;
+    cfg.dynamicSmemBytes = (size_t)cap * 2;
+    cfg.gridDim = dim3((unsigned)C, (unsigned)rows, 1);
+    attr[0].val.clusterDim.x = (unsigned)C;
+    int nclusters = 0;
+    if (C <= 8 || (cudaOccupancyMaxActiveClusters(&nclusters, topk_kernel, &cfg) == cudaSuccess &&
+                   nclusters > 0))
+      break;
+    (void)cudaGetLastError();
+  }
   ProfScope prof(stream, "topk");
-  topk_kernel<<<(unsigned)rows, kTopkThreads, smem, stream>>>(scores, Nq, q_pos0, E, m, k, cap,
-                                                              topk_idx, topk_cnt);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, topk_kernel, scores, Nq, q_pos0, E, m, k, cap, topk_idx,
+                            topk_cnt);
 }
 
 }  // namespace csa

@@ -106,7 +106,9 @@ def _tie_scores(rng, shape):
 
 @pytest.mark.parametrize("E,Nq,q_pos0,m,k", [(300, 4, 1196, 4, 50), (64, 3, 100, 1, 64),
                                              (5000, 2, 19999, 4, 700), (60000, 1, 239999, 4, 300),
-                                             (1000, 1, 3999, 4, 999)])
+                                             (1000, 1, 3999, 4, 999),
+                                             (6000, 150, 23850, 4, 100),   # one CTA, 2 rounds
+                                             (300000, 1, 1199999, 4, 2048)])  # unstaged chunks
 def test_topk_ties_and_negative_scores(E, Nq, q_pos0, m, k):
     rng = np.random.default_rng(E + k)
     sc_np = _tie_scores(rng, (2, Nq, E))
@@ -130,6 +132,7 @@ ATT_CASES = [
     (1, 40, 0, 40, 8, 64, 4, 64, 6),         # config-1 shape from position 0 (early rows empty)
     (2, 3, 700, 703, 16, 64, 4, 5, 100),     # k above visible, short window
     (1, 2, 4000, 4096, 128, 128, 4, 128, 40),  # two head groups
+    (16, 1, 4095, 4096, 64, 128, 4, 128, 512),  # decode batch 16: 10-CTA cluster merge
 ]
 
 
@@ -175,6 +178,7 @@ HCA_CASES = [
     (3, 1, 8191, 8192, 64, 128, 128, 128),   # decode, split-K over 64 entries + window
     (1, 50, 0, 300, 8, 64, 128, 64),         # config-1 shape: no entry visible for t < 127
     (1, 4, 996, 1000, 64, 64, 4, 0),         # no window at all
+    (2, 1, 131071, 131072, 64, 128, 128, 128),  # 18 splits per token: workspace merge
 ]
 
 
