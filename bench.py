@@ -53,6 +53,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
+    ap.add_argument("--context", type=int, default=None,
+                    help="override the workload's context length (smaller ncu captures)")
     ap.add_argument("--quick", action="store_true",
                     help="timed steps only (no profiling pass, e2e or CPU baseline); for ncu runs")
     return ap.parse_args(argv)
@@ -116,6 +118,32 @@ def step_work(wl):
     return kernels
 
 
+def rank_seed(wl, rank):
+    """Every rank decodes its own sequences: the workload's seed offset by the rank."""
+    return wl.seed + 1000 * rank
+
+
+def max_over_ranks(x, world, device):
+    """The slowest rank's value (the job's step time)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def resize_context(wl, N):
+    """The same workload at context length N (queries keep their offset from the end)."""
+    import dataclasses
+    layers = []
+    for s in wl.layers:
+        back = s.N - s.q_pos0
+        layers.append(s.scaled(N=N, q_pos0=N - back, compress_begin=max(0, N - (s.N - s.compress_begin))))
+    return dataclasses.replace(wl, name=f"{wl.name}@ctx{N}", layers=tuple(layers))
+
+
 def units_per_step(wl):
     if wl.mode == "decode":
         return wl.layers[0].B * wl.layers[0].Nq, "tok/s"
@@ -147,11 +175,40 @@ class ClockSampler:
             self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
             self.ok = True
+            self._thr = threading.Thread(target=self._run, daemon=True)
         except Exception:
-            return self
-        self._thr = threading.Thread(target=self._run, daemon=True)
+            self._thr = threading.Thread(target=self._run_smi, daemon=True)
         self._thr.start()
         return self
+
+    def _run_smi(self):
+        """Same samples through nvidia-smi (read-only query loop) when NVML bindings are absent."""
+        import subprocess
+        cmd = ["nvidia-smi", "-i", str(self.index), "--query-gpu=clocks.sm,clocks.max.sm,"
+               "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "20"]
+        try:
+            proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.ok = True
+        try:
+            while not self._stop.is_set():
+                line = proc.stdout.readline()
+                if not line:
+                    break
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                    r = int(f[2], 16)
+                    for bit, name in self.REASONS.items():
+                        if r & bit:
+                            self.reasons.add(name)
+                except (ValueError, IndexError):
+                    pass
+        finally:
+            proc.terminate()
+            proc.wait()
 
     def _run(self):
         nv = self._nv
@@ -255,7 +312,9 @@ def run_native(args, rank, world):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     wl = get_config(args.config)
-    seed = wl.seed + 1000 * rank           # every rank decodes its own sequences (weak scaling)
+    if args.context:
+        wl = resize_context(wl, args.context)
+    seed = rank_seed(wl, rank)             # every rank decodes its own sequences (weak scaling)
     states = {s.kind: setup_layer(s, seed, li, dev) for li, s in enumerate(wl.layers)}
     call = csa.PreparedLayerPair(states.get("csa"), states.get("hca"))
     torch.cuda.synchronize()
@@ -307,11 +366,7 @@ def run_native(args, rank, world):
 
     with ClockSampler(local) as clk:
         ms = timed_loop(step)
-    ms_step = statistics.mean(ms)
-    t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_step = float(t.item())
+    ms_step = max_over_ranks(statistics.mean(ms), world, dev)
     assert csa.device_status(reset=True) == 0, "device status flags after the timed loop"
 
     units, unit = units_per_step(wl)
@@ -401,11 +456,7 @@ def run_e2e(wl, states, call, flush, K, dev, world, barrier):
         e1[i].record()
     torch.cuda.synchronize()
     barrier()
-    ms = statistics.mean(e0[i].elapsed_time(e1[i]) for i in range(K))
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(e0[i].elapsed_time(e1[i]) for i in range(K)), world, dev)
     units, unit = units_per_step(wl)
     work = step_work(wl)
     if units is not None:

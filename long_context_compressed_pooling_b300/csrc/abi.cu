@@ -73,8 +73,8 @@ csa_status check_index(const uint8_t* qi_codes, const uint8_t* qi_scales,
                        const int32_t* topk_idx, const int32_t* topk_cnt, const uint16_t* scores) {
   if (!qi_codes || !qi_scales || !ki_codes || !ki_scales || !topk_idx || !topk_cnt)
     return CSA_ERR_INVALID_ARG;
-  if (!al16(qi_codes) || !al16(ki_codes) || !al16(topk_idx) || !al16(topk_cnt) ||
-      (scores && !al16(scores)))
+  if (!al16(qi_codes) || !al16(ki_codes) || !al16(ki_scales) || !al16(topk_idx) ||
+      !al16(topk_cnt) || (scores && !al16(scores)))
     return CSA_ERR_ALIGN;
   if (B < 1 || Nq < 1 || q_pos0 < 0 || E < 0 || m < 1 || k < 1) return CSA_ERR_INVALID_ARG;
   if (d_I != 32 && d_I != 64) return CSA_ERR_UNSUPPORTED;
@@ -131,7 +131,7 @@ csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return CSA_ERR_CUDA;
     const IndexerPlan plan = plan_indexer(B, Nq, E, H_I, d_I);
-    cudaError_t e = launch_indexer(&map, qi_codes, qi_scales, ki_scales, sc, B, Nq, q_pos0, E, m,
+    cudaError_t e = launch_indexer(&map, ki_codes, qi_codes, qi_scales, ki_scales, sc, B, Nq, q_pos0, E, m,
                                    H_I, d_I, plan, status, st);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   }

@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(NW * 32) attend_kernel(const AttnParams p) {
   uint16_t* Vs = Ks + kStages * kKC * D;                              // [kStages][kKC][D]
   uint8_t* kmask = reinterpret_cast<uint8_t*>(Vs + kStages * kKC * D);  // [kStages][kKC]
 
+  pdl_trigger();
+  pdl_wait();
   const int split = p.cluster_merge ? (int)cluster_ctarank() : blockIdx.x;
   const int64_t tok = blockIdx.y;
   const int h_base = blockIdx.z * ROWS;
@@ -318,21 +320,30 @@ __global__ void __launch_bounds__(NW * 32) attend_kernel(const AttnParams p) {
     const int row = rb + x / C4, c4 = x % C4;
     const int h = h_base + row;
     if (h >= p.H) continue;
+    float2 ml[kMaxClusterSplits];
+#pragma unroll
+    for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+      ml[sp] = sp < S ? dsmem_ld_f32x2(pml + row * 2, sp) : make_float2(-INFINITY, 0.f);
     float M = -INFINITY;
-    for (int sp = 0; sp < S; ++sp) M = fmaxf(M, dsmem_ld_f32x2(pml + row * 2, sp).x);
+#pragma unroll
+    for (int sp = 0; sp < kMaxClusterSplits; ++sp) M = fmaxf(M, ml[sp].x);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float L = 0.f;
     if (M != -INFINITY) {
-      for (int sp = 0; sp < S; ++sp) {
-        const float2 ml = dsmem_ld_f32x2(pml + row * 2, sp);
-        if (ml.x == -INFINITY) continue;
-        const float w = expf(ml.x - M);
-        L += w * ml.y;
-        const float4 v = dsmem_ld_f32x4(po + row * PSTRIDE + c4 * 4, sp);
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
+      float4 v[kMaxClusterSplits];
+#pragma unroll
+      for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+        v[sp] = sp < S ? dsmem_ld_f32x4(po + row * PSTRIDE + c4 * 4, sp)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+        if (ml[sp].x == -INFINITY) continue;
+        const float w = expf(ml[sp].x - M);
+        L += w * ml[sp].y;
+        acc.x += w * v[sp].x;
+        acc.y += w * v[sp].y;
+        acc.z += w * v[sp].z;
+        acc.w += w * v[sp].w;
       }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -351,6 +362,8 @@ __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ ws_
                                                   const float* __restrict__ ws_ml, int n_splits,
                                                   int64_t tokens, int H, uint16_t* out,
                                                   float* lse) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t th = blockIdx.x;  // tok * H + h
   const int lane = threadIdx.x;
   float M = -INFINITY;
@@ -413,13 +426,15 @@ cudaError_t launch_attend_t(AttnParams prm, int groups, cudaStream_t stream) {
   cfg.blockDim = dim3(NW * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = prm.cluster_merge ? (unsigned)prm.n_splits : 1u;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   if (prm.cluster_merge && prm.n_splits > 8) {
     int nclusters = 0;
     if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters == 0) {
@@ -433,9 +448,9 @@ cudaError_t launch_attend_t(AttnParams prm, int groups, cudaStream_t stream) {
   }
   if (e != cudaSuccess || prm.n_splits == 1 || prm.cluster_merge) return e;
   ProfScope prof(stream, "lse_merge");
-  merge_kernel<D><<<(unsigned)((int64_t)prm.tokens * prm.H), 32, 0, stream>>>(
-      prm.ws_o, prm.ws_ml, prm.n_splits, prm.tokens, prm.H, prm.out, prm.lse);
-  return cudaGetLastError();
+  return launch_ex(merge_kernel<D>, dim3((unsigned)((int64_t)prm.tokens * prm.H)), dim3(32), 0,
+                   stream, 1, (const float*)prm.ws_o, (const float*)prm.ws_ml, prm.n_splits,
+                   (int64_t)prm.tokens, prm.H, prm.out, prm.lse);
 }
 
 template <int D>

@@ -56,14 +56,19 @@ CSA_DEV void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// The suspend-time hint lets the hardware park the waiting thread until the phase completes
+// (up to ~1 ms per try) instead of returning at once: spinning waiters would otherwise take the
+// issue slots of the producer and MMA threads they are waiting for.
+constexpr uint32_t kSuspendHintNs = 1000000;
+
 CSA_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -74,13 +79,31 @@ CSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (clock64() - t0 > kWaitBudgetCycles) {
       atomicOr(status, kFlagTimeout);
       return false;
     }
   }
+}
+
+// Warp-wide bounded wait: every lane waits (each lane's wait is bounded) and the warp takes lane
+// 0's verdict, so the result is uniform across the warp.
+CSA_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  const int ok = mbar_wait(bar, parity, status) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// One lane of a converged warp (elect.sync). Single-thread operations (TMA / bulk copy issue,
+// tcgen05.mma, tcgen05.commit) are issued this way from a warp that runs its loop converged: a
+// lone lane looping in a diverged branch issues tcgen05.mma about 1.8x slower.
+CSA_DEV bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t.reg .b32 rr;\n\telect.sync rr|P, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(e));
+  return e != 0;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -92,6 +115,15 @@ CSA_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, 
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_addr(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// Non-tensor bulk copy global -> shared (both addresses 16-byte aligned, size a multiple of 16).
+CSA_DEV void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
 
@@ -216,6 +248,14 @@ CSA_DEV void tmem_st8_fill(uint32_t taddr, uint32_t v) {
       "r"(v)
       : "memory");
 }
+
+// ---------------------------------------------------------------------------------------------
+// programmatic dependent launch: a kernel lets its successor launch early (trigger), and waits
+// for its predecessor's completion and memory (wait) before touching data the predecessor wrote
+// or may still read
+// ---------------------------------------------------------------------------------------------
+CSA_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+CSA_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------------------------------------
 // thread-block clusters and distributed shared memory

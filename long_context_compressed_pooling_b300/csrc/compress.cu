@@ -51,6 +51,8 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restric
                                                        int64_t N, int m, int64_t j_begin,
                                                        int64_t n_entries) {
   constexpr int D = CH * 8;
+  pdl_trigger();
+  pdl_wait();
   const int64_t E = N / m;
   const int64_t total = (int64_t)B * n_entries * CH;
   for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < total;
@@ -119,6 +121,8 @@ __global__ void __launch_bounds__(256) compress_large_kernel(const uint16_t* __r
   const int tid = threadIdx.x;
   const int c = tid % CH, ts = tid / CH;
   const int64_t E = N / m;
+  pdl_trigger();
+  pdl_wait();
   for (int64_t w = blockIdx.x; w < (int64_t)B * n_entries; w += gridDim.x) {
     const int64_t b = w / n_entries, j = j_begin + w % n_entries;
     const int64_t tok0 = b * N + j * m;
@@ -205,23 +209,24 @@ cudaError_t launch_compress(const uint16_t* k_raw, const uint16_t* v_raw, const 
     const int64_t cap = (int64_t)kNumSMs * 8;
     if (blocks > cap) blocks = cap;
     ProfScope prof(stream, "compress");
+    cudaError_t e = cudaSuccess;
     switch (ch) {
       case 8:
-        compress_large_kernel<8><<<(unsigned)blocks, 256, 0, stream>>>(
-            k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
+        e = launch_ex(compress_large_kernel<8>, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                      k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
         break;
       case 16:
-        compress_large_kernel<16><<<(unsigned)blocks, 256, 0, stream>>>(
-            k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
+        e = launch_ex(compress_large_kernel<16>, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                      k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
         break;
       case 32:
-        compress_large_kernel<32><<<(unsigned)blocks, 256, 0, stream>>>(
-            k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
+        e = launch_ex(compress_large_kernel<32>, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                      k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
         break;
       default:
         return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+    return e;
   }
   const int64_t total = (int64_t)B * n_entries * ch;
   const int threads = 256;
@@ -229,26 +234,24 @@ cudaError_t launch_compress(const uint16_t* k_raw, const uint16_t* v_raw, const 
   const int64_t cap = (int64_t)kNumSMs * 8;  // 8 resident 256-thread CTAs per SM
   if (blocks > cap) blocks = cap;
   ProfScope prof(stream, "compress");
+  cudaError_t e = cudaSuccess;
   switch (ch) {
     case 8:
-      compress_kernel<8><<<(unsigned)blocks, threads, 0, stream>>>(k_raw, v_raw, logits, k_cmp,
-                                                                   v_cmp, B, N, m, j_begin,
-                                                                   n_entries);
+      e = launch_ex(compress_kernel<8>, dim3((unsigned)blocks), dim3(threads), 0, stream, 1,
+                    k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
       break;
     case 16:
-      compress_kernel<16><<<(unsigned)blocks, threads, 0, stream>>>(k_raw, v_raw, logits, k_cmp,
-                                                                    v_cmp, B, N, m, j_begin,
-                                                                    n_entries);
+      e = launch_ex(compress_kernel<16>, dim3((unsigned)blocks), dim3(threads), 0, stream, 1,
+                    k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
       break;
     case 32:
-      compress_kernel<32><<<(unsigned)blocks, threads, 0, stream>>>(k_raw, v_raw, logits, k_cmp,
-                                                                    v_cmp, B, N, m, j_begin,
-                                                                    n_entries);
+      e = launch_ex(compress_kernel<32>, dim3((unsigned)blocks), dim3(threads), 0, stream, 1,
+                    k_raw, v_raw, logits, k_cmp, v_cmp, B, N, m, j_begin, n_entries);
       break;
     default:
       return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace csa

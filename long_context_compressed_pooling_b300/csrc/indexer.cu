@@ -7,19 +7,30 @@
 // with q_I, k_I block-scaled FP4 vectors (e2m1 codes, one UE8M0 scale per 32 elements).
 //
 // Layout of the contraction. A = the entries' FP4 index keys (M = 128 entries per tile,
-// K = 64 e2m1 values = 32 bytes per row, TMA-loaded with the 32-byte swizzle). B = the queries,
-// one B row per (query, head, 32-element block): the row holds that block's codes and zeros
-// elsewhere, so D[j, (q,h,blk)] is the UNSCALED partial dot product of one scale block. The
+// K = 64 e2m1 values = 32 bytes per row). B = the queries, one B row per (query, head, 32-element
+// block): the row holds that block's codes and zeros elsewhere, so D[j, (q,h,blk)] is the
+// UNSCALED partial dot product of one scale block. With d_I = 64 a tile is 4 KB contiguous in
+// HBM and arrives with ONE bulk copy (a tensor-map box with 32-byte rows would cost 128 small
+// TMA requests per tile); it lands unswizzled while the MMA reads it through the 32-byte swizzle,
+// which swaps the two 16-byte halves of rows whose bit 2 is set. Those rows therefore meet the
+// query blocks in swapped positions, so B carries each head twice (blocks in place, blocks
+// swapped) and every epilogue thread reads the pair that matches its row. d_I = 32 rows (16 B)
+// keep the TMA path, whose box is zero-filled to 32 bytes. The
 // MMA runs kind::mxf4 with every scale factor set to 1.0; the real UE8M0 scales are applied in
 // the epilogue as exact power-of-two multiplies. Partial sums of e2m1 products are multiples of
 // 1/4 below 2^11, so the tensor core's fp32 accumulation is exact, and the epilogue's scaled
 // sums stay exact for the scale range the workloads use (2^-4..2^0): the BF16 rounding is then
 // the only rounding, as the method specifies.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads into a 4-stage ring, warp 1 allocates
-// tensor memory and issues one MMA per 128-entry tile into a double-buffered accumulator,
-// warps 2-5 drain the accumulator (tcgen05.ld), apply scales / ReLU / head sum / BF16 rounding
-// and store the scores. Every mbarrier wait is bounded (kFlagTimeout on expiry).
+// Pipeline. Work is processed in groups of G tiles: the TMA warp loads a group into one slot
+// of a 12-tile ring, the MMA thread issues the group's G MMAs into the next accumulator group of
+// a ring in tensor memory (3 groups of 4 x 16 columns for decode, 3 of 2 x 64 for prefill) and
+// commits once, and eight epilogue warps (two per tensor-memory lane quarter) drain the group
+// together. The commit -> epilogue round trip is paid once per group,
+// not per tile. The first groups' loads are issued before the CTA's set-up so their DRAM latency
+// overlaps it. Decode (one query per sequence) runs persistent CTAs over all (sequence, tile)
+// pairs; prefill gives each CTA one (sequence, query group). Every mbarrier wait is bounded
+// (kFlagTimeout on expiry).
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
@@ -28,12 +39,21 @@ namespace csa {
 namespace {
 
 constexpr int kTileM = 128;
-constexpr int kStages = 4;
 constexpr int kRowBytes = 32;
 constexpr int kATileBytes = kTileM * kRowBytes;
-constexpr int kThreads = 192;
+constexpr int kSlotTiles = 8;   // tiles per copy slot (one code copy + one scale copy)
+constexpr int kSlots = 3;       // slots in the ring
+constexpr int kRingTiles = kSlotTiles * kSlots;
+constexpr int kScaleTileBytes = kTileM * 2;  // one tile's UE8M0 scales (NB = 2)
+constexpr int kEW = 2;                      // epilogue warps per tensor-memory lane quarter
+constexpr int kThreads = 64 + 128 * kEW;    // copy warp, MMA warp, 8 epilogue warps
+constexpr int kWorkThreads = kThreads - 32; // every warp but the copy warp
 constexpr int kMaxCols = 64;
+constexpr int kMaxG = 4;
+constexpr int kMaxAcc = 8;  // accumulator groups in tensor memory (a ring)
 constexpr int kSfCols = 16;  // tensor-memory columns filled with scale 1.0 for each of A and B
+constexpr int kMaxSeqPerCta = 8;  // decode: query operands of up to 8 sequences stay resident
+constexpr int kBRows = 128;       // B-operand rows held in shared memory (decode 8 x 16, prefill 64)
 
 struct IdxParams {
   const uint8_t* qi_codes;   // [B, Nq, H_I, NB*16]
@@ -41,192 +61,318 @@ struct IdxParams {
   const uint8_t* ki_scales;  // [B, E, NB]
   uint16_t* scores;          // [B, Nq, E]
   int64_t q_pos0, E;
-  int Nq, m, QN, ncols, n_splits, tmem_cols;
+  int Nq, m, QN, ncols, G, nacc, n_splits, tmem_cols;
+  int B, tiles_per_seq;      // decode: CTAs walk contiguous ranges of (sequence, tile)
+  int64_t total_tiles;
+  const uint8_t* ki_codes;   // [B, E, 32] (bulk-copy path)
   uint32_t* status;
 };
 
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + kStages * kATileBytes +
-                              kMaxCols * kRowBytes + kMaxCols * sizeof(float) + 256;
+constexpr size_t kSmemBytes = 1024 /*align slack*/ + kRingTiles * kATileBytes +
+                              kRingTiles * kScaleTileBytes + kBRows * kRowBytes +
+                              kBRows * sizeof(float) + kMaxCols * sizeof(int64_t) +
+                              (2 * kSlots + 2 * kMaxAcc + 3) * 8 + 64;
 
-// H_I heads, NB = d_I / 32 scale blocks per vector; CPQ = H_I * NB MMA columns per query.
-template <int H_I, int NB>
+// Named barrier over every warp but the copy warp (the copy warp never waits on set-up).
+CSA_DEV void work_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kWorkThreads) : "memory"); }
+
+// H_I heads, NB = d_I / 32 scale blocks per vector, SW = 2 for the bulk-copy path (each head's
+// blocks in place and swapped), else 1; CPQ = H_I * NB * SW MMA columns per query.
+template <int H_I, int NB, int SW>
 __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                                                            const IdxParams p) {
-  constexpr int CPQ = H_I * NB;
+  constexpr int CPQ = H_I * NB * SW;
   static_assert(16 % CPQ == 0, "columns per query must divide 16");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* atiles = base;                                   // kStages x 4096, 1024-aligned
-  uint8_t* btile = atiles + kStages * kATileBytes;          // ncols x 32, 1024-aligned
-  float* qscale = reinterpret_cast<float*>(btile + kMaxCols * kRowBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(qscale + kMaxCols);
-  uint64_t* full = bars;                 // [kStages]
-  uint64_t* empty = bars + kStages;      // [kStages]
-  uint64_t* tfull = bars + 2 * kStages;  // [2]
-  uint64_t* tempty = tfull + 2;          // [2]
-  uint64_t* drain = tempty + 2;          // [1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint8_t* atiles = base;                                    // kRingTiles x 4096, 1024-aligned
+  uint8_t* btile = atiles + kRingTiles * kATileBytes;        // kBRows x 32, 1024-aligned
+  uint8_t* stiles = btile + kBRows * kRowBytes;              // bulk path: kRingTiles x 256 B
+  float* qscale = reinterpret_cast<float*>(stiles + kRingTiles * kScaleTileBytes);
+  int64_t* qvis = reinterpret_cast<int64_t*>(qscale + kBRows);  // visible entries per query
+  uint64_t* bars = reinterpret_cast<uint64_t*>(qvis + kMaxCols);
+  uint64_t* full = bars;                 // [kSlots]
+  uint64_t* empty = bars + kSlots;       // [kSlots]
+  uint64_t* tfull = bars + 2 * kSlots;   // [kMaxAcc]
+  uint64_t* tempty = tfull + kMaxAcc;    // [kMaxAcc]
+  uint64_t* drain = tempty + kMaxAcc;    // [1]
+  uint64_t* done = drain + 1;            // [1] every epilogue warp finished with TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   int* aborted = reinterpret_cast<int*>(tmem_slot + 1);
 
-  const int split = blockIdx.x, group = blockIdx.y, b = blockIdx.z;
-  const int i0 = group * p.QN;
-  const int nq = min(p.QN, p.Nq - i0);
-  const int64_t t_last = p.q_pos0 + i0 + nq - 1;
-  const int64_t nv_max = min(p.E, (t_last + 1) / p.m);
-  const int64_t tiles = (nv_max + kTileM - 1) / kTileM;
-  const int64_t tb = tiles * split / p.n_splits;
-  const int64_t te = tiles * (split + 1) / p.n_splits;
+  pdl_trigger();
+  // Work: prefill (Nq > 1) -> one (sequence, query group) per grid (y, z) and a range of entry
+  // tiles per x. Decode (Nq == 1) -> CTA x walks the flattened (sequence, tile) range
+  // [tb, te) of all sequences; the query operands of the sequences it touches stay resident.
+  const bool decode = p.Nq == 1;
+  const int split = blockIdx.x, group = blockIdx.y;
+  const int i0 = decode ? 0 : group * p.QN;
+  const int nq = decode ? 1 : min(p.QN, p.Nq - i0);
+  int64_t tb, te;
+  int b_first;
+  if (decode) {
+    tb = p.total_tiles * split / p.n_splits;
+    te = p.total_tiles * (split + 1) / p.n_splits;
+    b_first = (int)(tb / p.tiles_per_seq);
+  } else {
+    const int64_t t_last = p.q_pos0 + i0 + nq - 1;
+    const int64_t nv_max = min(p.E, (t_last + 1) / p.m);
+    const int64_t tiles = (nv_max + kTileM - 1) / kTileM;
+    tb = tiles * split / p.n_splits;
+    te = tiles * (split + 1) / p.n_splits;
+    b_first = blockIdx.z;
+  }
   if (tb >= te) return;  // uniform over the CTA
   const int ntiles = (int)(te - tb);
+  const int n_seq = decode ? (int)((te - 1) / p.tiles_per_seq) - b_first + 1 : 1;
+  if (n_seq > kMaxSeqPerCta) {  // the launch plan never produces this; refuse rather than overflow
+    if (threadIdx.x == 0) atomicOr(p.status, kFlagBadIndex);
+    return;
+  }
+  const int G = p.G;                      // tiles per MMA / epilogue group (divides kSlotTiles)
+  const int ngroups = (ntiles + G - 1) / G;
+  const int nunits = (ntiles + kSlotTiles - 1) / kSlotTiles;  // copy slots to fill
+  // Tile `it` of this CTA -> (sequence, first entry) with 32-bit arithmetic only (64-bit
+  // integer division is emulated in software and must stay out of the loops).
+  const int tps = p.tiles_per_seq;
+  const int t_first = decode ? (int)(tb - (int64_t)b_first * tps) : (int)tb;
+  auto tile_seq = [&](int it) -> int {
+    return decode ? b_first + (int)((unsigned)(t_first + it) / (unsigned)tps) : b_first;
+  };
+  auto tile_row0 = [&](int it) -> int {
+    const unsigned t = (unsigned)(t_first + it);
+    return (int)(decode ? t % (unsigned)tps : t) * kTileM;
+  };
+  auto ring_tile = [&](int it) -> int {  // position of tile `it` in the shared-memory ring
+    return ((it / kSlotTiles) % kSlots) * kSlotTiles + it % kSlotTiles;
+  };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- B operand: queries (generic-proxy writes, fenced to the async proxy below) ----------
-  for (int idx = threadIdx.x; idx < p.ncols * 2; idx += kThreads) {
-    const int r = idx >> 1, c = idx & 1;
-    const int ql = r / CPQ, h = (r / NB) % H_I, blk = r % NB;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (ql < nq && c == blk) {
-      const uint8_t* src =
-          p.qi_codes + (((int64_t)b * p.Nq + i0 + ql) * H_I + h) * (NB * 16) + blk * 16;
-      v = *reinterpret_cast<const uint4*>(src);
-    }
-    const int phys = r * kRowBytes + ((c ^ ((r >> 2) & 1)) << 4);  // 32-byte swizzle
-    *reinterpret_cast<uint4*>(btile + phys) = v;
-  }
-  for (int r = threadIdx.x; r < p.ncols; r += kThreads) {
-    const int ql = r / CPQ, h = (r / NB) % H_I, blk = r % NB;
-    float s = 0.f;
-    if (ql < nq)
-      s = exp2_int((int)p.qi_scales[(((int64_t)b * p.Nq + i0 + ql) * H_I + h) * NB + blk] - 127);
-    qscale[r] = s;
-  }
-  fence_proxy_async_smem();
-
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < p.nacc; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], 4 * kEW);
     }
     mbar_init(drain, 1);
+    mbar_init(done, 4 * kEW);
     *aborted = 0;
     fence_mbar_init();
     prefetch_tensormap(&kmap);
   }
+  __syncwarp();
+  __syncthreads();
+
+  if (warp == 0) {
+    // ---------------- copy warp: fills the ring slot by slot, never joins the set-up ----------
+    // The index keys are inputs of this call (not a predecessor's output), so copying starts
+    // before the predecessor-dependent part. Every bulk copy costs ~0.3 us to issue whatever its
+    // size, so a slot (8 tiles) is one code copy and one scale copy whenever the tiles form one
+    // contiguous span of HBM (always, unless a ragged sequence tail intervenes).
+    auto tile_bytes = [&](int it) -> uint32_t {  // rows that exist in this tile x 32 B
+      return (uint32_t)min((int64_t)kTileM, p.E - (int64_t)tile_row0(it)) * kRowBytes;
+    };
+    auto tile_addr = [&](int it) -> int64_t {  // entry index of the tile's first row
+      return (int64_t)tile_seq(it) * p.E + tile_row0(it);
+    };
+    auto issue_unit = [&](int u) {
+      const int slot = u % kSlots;
+      const int t0 = u * kSlotTiles, t1 = min(ntiles, t0 + kSlotTiles);
+      if (SW == 2) {
+        uint32_t bytes = 0;
+        for (int it = t0; it < t1; ++it) bytes += tile_bytes(it) + tile_bytes(it) / 16;
+        mbar_arrive_expect_tx(&full[slot], bytes);
+        int a = t0;
+        while (a < t1) {
+          const int64_t e0 = tile_addr(a);
+          uint32_t rows = tile_bytes(a) / kRowBytes;
+          int b = a + 1;
+          while (b < t1 && rows == (uint32_t)(b - a) * kTileM && tile_addr(b) == e0 + rows) {
+            rows += tile_bytes(b) / kRowBytes;
+            ++b;
+          }
+          const int rt = ring_tile(a);
+          bulk_load(atiles + rt * kATileBytes, p.ki_codes + e0 * kRowBytes, rows * kRowBytes,
+                    &full[slot]);
+          bulk_load(stiles + rt * kScaleTileBytes, p.ki_scales + e0 * 2, rows * 2, &full[slot]);
+          a = b;
+        }
+      } else {
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)((t1 - t0) * kATileBytes));
+        for (int it = t0; it < t1; ++it)
+          tma_load_3d(atiles + ring_tile(it) * kATileBytes, &kmap, &full[slot], 0, tile_row0(it),
+                      tile_seq(it));
+      }
+    };
+    int issued = 0;
+    for (int u = 0; u < nunits; ++u) {
+      const int slot = u % kSlots, use = u / kSlots;
+      if (use > 0 && !mbar_wait_warp(&empty[slot], (uint32_t)(use - 1) & 1u, p.status)) {
+        if (lane == 0) *aborted = 1;
+        break;
+      }
+      if (elect_one()) issue_unit(u);
+      __syncwarp();
+      issued = u + 1;
+    }
+    // stay until this CTA's own copies have landed (the MMA warp normally sees them first)
+    for (int u = max(0, issued - kSlots); u < issued; ++u)
+      mbar_wait_warp(&full[u % kSlots], (uint32_t)(u / kSlots) & 1u, p.status);
+    return;
+  }
+
+  // ---- set-up of the work warps: B operand, query scales, visibility, TMEM, scale factors ----
+  // Sequence sl of this CTA owns B rows [sl * ncols, (sl + 1) * ncols).
+  const int wt = threadIdx.x - 32;
+  for (int idx = wt; idx < n_seq * p.ncols * 2; idx += kWorkThreads) {
+    const int rr = idx >> 1, c = idx & 1;
+    const int sl = rr / p.ncols, r = rr % p.ncols;
+    const int ql = r / CPQ, h = (r / (NB * SW)) % H_I, sw = (r / NB) % SW, blk = r % NB;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (ql < nq && c == (blk ^ sw)) {
+      const uint8_t* src = p.qi_codes +
+          (((int64_t)(b_first + sl) * p.Nq + i0 + ql) * H_I + h) * (NB * 16) + blk * 16;
+      v = *reinterpret_cast<const uint4*>(src);
+    }
+    const int phys = rr * kRowBytes + ((c ^ ((rr >> 2) & 1)) << 4);  // 32-byte swizzle
+    *reinterpret_cast<uint4*>(btile + phys) = v;
+  }
+  for (int rr = wt; rr < n_seq * p.ncols; rr += kWorkThreads) {
+    const int sl = rr / p.ncols, r = rr % p.ncols;
+    const int ql = r / CPQ, h = (r / (NB * SW)) % H_I, blk = r % NB;
+    float s = 0.f;
+    if (ql < nq)
+      s = exp2_int((int)p.qi_scales[(((int64_t)(b_first + sl) * p.Nq + i0 + ql) * H_I + h) * NB +
+                                    blk] - 127);
+    qscale[rr] = s;
+  }
+  for (int ql = wt; ql < nq; ql += kWorkThreads)
+    qvis[ql] = min(p.E, (p.q_pos0 + i0 + ql + 1) / p.m);
+  fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(tmem_slot, (uint32_t)p.tmem_cols);
     tmem_relinquish();
   }
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  work_sync();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t sfa_col = 2u * p.ncols, sfb_col = 2u * p.ncols + kSfCols;
-
-  if (warp >= 2) {
+  const uint32_t acc_cols = (uint32_t)(G * p.ncols);  // one accumulator group
+  const uint32_t sfa_col = (uint32_t)p.nacc * acc_cols, sfb_col = sfa_col + kSfCols;
+  if (warp >= 2 && warp < 6) {
     // scale factors = 1.0 everywhere in the two scale regions (all lanes of this quarter)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 #pragma unroll
     for (int c = 0; c < 2 * kSfCols; c += 8) tmem_st8_fill(tmem + lane_base + sfa_col + c, 0x7F7F7F7Fu);
     tmem_st_wait();
   }
+  __syncwarp();
   tc_fence_before();
-  __syncthreads();
+  work_sync();
   tc_fence_after();
+  pdl_wait();  // the predecessor may still read the score buffer this kernel writes
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      int issued = 0;
-      for (int it = 0; it < ntiles; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-        if (!mbar_wait(&empty[s], ph ^ 1u, p.status)) {
-          *aborted = 1;
-          break;
-        }
-        mbar_arrive_expect_tx(&full[s], kATileBytes);
-        tma_load_3d(atiles + s * kATileBytes, &kmap, &full[s], 0, (int)((tb + it) * kTileM), b);
-        ++issued;
-      }
-      if (*aborted) {  // let this CTA's own copies land before the CTA exits
-        for (int it = max(0, issued - kStages); it < issued; ++it)
-          mbar_wait(&full[it % kStages], (uint32_t)(it / kStages) & 1u, p.status);
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      const uint32_t idesc = idesc_mxf4(kTileM, p.ncols);
-      const uint64_t bdesc = smem_desc(smem_addr(btile), 16, 256, kSwizzle32B);
-      for (int it = 0; it < ntiles; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (uint32_t)(it / kStages) & 1u;
-        const int a = it & 1;
-        const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-        if (!mbar_wait(&tempty[a], aph ^ 1u, p.status) || !mbar_wait(&full[s], ph, p.status)) {
-          *aborted = 1;
-          break;
-        }
-        tc_fence_after();
-        const uint64_t adesc = smem_desc(smem_addr(atiles + s * kATileBytes), 16, 256, kSwizzle32B);
-        umma_mxf4(tmem + (uint32_t)(a * p.ncols), adesc, bdesc, idesc, tmem + sfa_col,
-                  tmem + sfb_col, 0u);
-        umma_commit(&empty[s]);
-        umma_commit(&tfull[a]);
-      }
-      umma_commit(drain);  // arrives once every MMA above has finished
-      mbar_wait(drain, 0, p.status);
-    }
-  } else {
-    // ---------------- epilogue: 4 warps, one tensor-memory lane quarter each ----------------
-    const int quarter = warp & 3;
-    const int row = quarter * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    for (int it = 0; it < ntiles; ++it) {
-      const int a = it & 1;
-      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(&tfull[a], aph, p.status) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
+  if (warp == 1) {
+    // ---------------- MMA issuer (whole warp, one elected lane issues) ----------------
+    const uint32_t idesc = idesc_mxf4(kTileM, p.ncols);
+    for (int g = 0; g < ngroups; ++g) {
+      const int u = g * G / kSlotTiles;
+      const int slot = u % kSlots;
+      const int a = g % p.nacc;
+      const uint32_t aph = (uint32_t)(g / p.nacc) & 1u;
+      if (!mbar_wait_warp(&tempty[a], aph ^ 1u, p.status) ||
+          !mbar_wait_warp(&full[slot], (uint32_t)(u / kSlots) & 1u, p.status)) {
         if (lane == 0) *aborted = 1;
         break;
       }
       tc_fence_after();
-      const int64_t j = (tb + it) * kTileM + row;
-      float sk[NB];
-#pragma unroll
-      for (int blk = 0; blk < NB; ++blk)
-        sk[blk] = (j < p.E) ? exp2_int((int)p.ki_scales[((int64_t)b * p.E + j) * NB + blk] - 127)
-                            : 0.f;
-      for (int c0 = 0; c0 < p.ncols; c0 += 16) {
+      const int nt = min(G, ntiles - g * G);
+      const bool unit_done = (g + 1) * G >= min(ntiles, (u + 1) * kSlotTiles);
+      if (elect_one()) {
+        for (int i = 0; i < nt; ++i) {
+          const int it = g * G + i;
+          const uint64_t adesc =
+              smem_desc(smem_addr(atiles + ring_tile(it) * kATileBytes), 16, 256, kSwizzle32B);
+          const uint64_t bdesc = smem_desc(
+              smem_addr(btile + (tile_seq(it) - b_first) * p.ncols * kRowBytes), 16, 256,
+              kSwizzle32B);
+          umma_mxf4(tmem + (uint32_t)(a * acc_cols + i * p.ncols), adesc, bdesc, idesc,
+                    tmem + sfa_col, tmem + sfb_col, 0u);
+        }
+        if (unit_done) umma_commit(&empty[slot]);  // the slot's last group frees the slot
+        umma_commit(&tfull[a]);
+      }
+      __syncwarp();
+    }
+    if (elect_one()) umma_commit(drain);  // arrives once every MMA above has finished
+    __syncwarp();
+    mbar_wait_warp(drain, 0, p.status);
+  } else {
+    // ---------------- epilogue: 8 warps, two per tensor-memory lane quarter ----------------
+    const int quarter = warp & 3;
+    const int sub = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    const bool swapped = SW == 2 && ((row >> 2) & 1);  // unswizzled row read through the swizzle
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int cchunks = p.ncols / 16;
+    for (int g = 0; g < ngroups; ++g) {
+      const int a = g % p.nacc;
+      const uint32_t aph = (uint32_t)(g / p.nacc) & 1u;
+      if (!mbar_wait_warp(&tfull[a], aph, p.status)) {
+        if (lane == 0) *aborted = 1;
+        break;
+      }
+      tc_fence_after();
+      const int nt = min(G, ntiles - g * G);
+      for (int u = sub; u < nt * cchunks; u += kEW) {
+        const int i = u / cchunks, c0 = (u % cchunks) * 16;
+        const int it = g * G + i;
+        const int b = tile_seq(it);
+        const int64_t j = (int64_t)tile_row0(it) + row;
+        const float* qs = qscale + (b - b_first) * p.ncols;
+        uint32_t sbits = 0;
+        if (j < p.E) {
+          if (SW == 2)
+            sbits = *reinterpret_cast<const uint16_t*>(stiles + ring_tile(it) * kScaleTileBytes +
+                                                       row * 2);
+          else
+            sbits = NB == 2
+                ? (uint32_t)*reinterpret_cast<const uint16_t*>(p.ki_scales + ((int64_t)b * p.E + j) * 2)
+                : (uint32_t)p.ki_scales[(int64_t)b * p.E + j];
+        }
+        float sk[NB];
+        sk[0] = exp2_int((int)(sbits & 0xFF) - 127);
+        if (NB == 2) sk[NB - 1] = exp2_int((int)((sbits >> 8) & 0xFF) - 127);
         uint32_t r[16];
-        tmem_ld16(tmem + lane_base + (uint32_t)(a * p.ncols + c0), r);
+        tmem_ld16(tmem + lane_base + (uint32_t)(a * acc_cols + i * p.ncols + c0), r);
         tmem_ld_wait();
+        if (j < p.E) {
 #pragma unroll
-        for (int cc = 0; cc < 16; cc += CPQ) {
-          const int ql = (c0 + cc) / CPQ;
-          if (ql < nq) {
-            float sc = 0.f;
+          for (int cc = 0; cc < 16; cc += CPQ) {
+            const int ql = (c0 + cc) / CPQ;
+            if (ql < nq) {
+              float s = 0.f;
 #pragma unroll
-            for (int h = 0; h < H_I; ++h) {
-              float dot = 0.f;
+              for (int h = 0; h < H_I; ++h) {
+                float dot = 0.f;
 #pragma unroll
-              for (int blk = 0; blk < NB; ++blk)
-                dot += (__uint_as_float(r[cc + h * NB + blk]) * qscale[c0 + cc + h * NB + blk]) *
-                       sk[blk];
-              sc += fmaxf(dot, 0.f);
+                for (int blk = 0; blk < NB; ++blk) {
+                  const int c_in = cc + h * NB * SW + blk;             // blocks in place
+                  const int c_sw = cc + h * NB * SW + (SW - 1) * NB + blk;  // blocks swapped
+                  const float d = swapped ? __uint_as_float(r[c_sw]) : __uint_as_float(r[c_in]);
+                  dot += (d * qs[c0 + c_in]) * sk[blk];
+                }
+                s += fmaxf(dot, 0.f);
+              }
+              s += 0.0f;  // -0 -> +0
+              if (j < qvis[ql])
+                p.scores[((int64_t)b * p.Nq + i0 + ql) * p.E + j] = f32_to_bf16_bits(s);
             }
-            sc += 0.0f;  // -0 -> +0
-            const int64_t t = p.q_pos0 + i0 + ql;
-            const int64_t nv = min(p.E, (t + 1) / p.m);
-            if (j < nv) p.scores[((int64_t)b * p.Nq + i0 + ql) * p.E + j] = f32_to_bf16_bits(sc);
           }
         }
       }
@@ -234,27 +380,32 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[a]);
     }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(done);
   }
 
-  tc_fence_before();
-  __syncthreads();
+  // Teardown: tensor memory is freed by the allocating warp only after every epilogue warp has
+  // signalled `done` (and the MMA warp has drained its MMAs above); the other warps just exit.
+  __syncwarp();
   if (warp == 1) {
+    mbar_wait_warp(done, 0, p.status);  // bounded; a timeout is already recorded
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
   }
 }
 
-template <int H_I, int NB>
+template <int H_I, int NB, int SW>
 cudaError_t launch_t(const CUtensorMap* kmap, const IdxParams& prm, const IndexerPlan& plan, int B,
                      cudaStream_t stream) {
-  auto kern = indexer_kernel<H_I, NB>;
+  auto kern = indexer_kernel<H_I, NB, SW>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)plan.n_splits, (unsigned)plan.n_groups, (unsigned)B);
+  dim3 grid((unsigned)plan.n_splits, (unsigned)plan.n_groups,
+            (unsigned)(prm.Nq == 1 ? 1 : B));
   ProfScope prof(stream, "indexer_mxf4");
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(*kmap, prm);
-  return cudaGetLastError();
+  return launch_ex(kern, grid, dim3(kThreads), kSmemBytes, stream, 1, *kmap, prm);
 }
 
 int next_pow2_at_least32(int x) {
@@ -265,29 +416,48 @@ int next_pow2_at_least32(int x) {
 
 }  // namespace
 
+// Bulk-copy path: 32-byte key rows, each head doubled into 16 columns, 16-byte aligned scale runs.
+bool indexer_bulk_path(int H_I, int d_I, int64_t E) { return d_I == 64 && H_I <= 4 && E % 8 == 0; }
+
 IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I) {
   IndexerPlan pl{};
-  const int cpq = H_I * (d_I / 32);
-  if (Nq == 1) {
+  const int cpq = H_I * (d_I / 32) * (indexer_bulk_path(H_I, d_I, E) ? 2 : 1);
+  if (Nq == 1) {  // two CTAs per SM: 3 x 64 + 32 scale columns fit in 256
     pl.QN = 1;
-    pl.ncols = 16;
-  } else {
+    pl.ncols = cpq > 16 ? 32 : 16;
+    pl.G = kMaxG;
+    pl.nacc = 3;
+  } else {         // one CTA per SM: 3 x (2 x 64) + 32 columns fit in 512
     pl.ncols = kMaxCols;
     pl.QN = kMaxCols / cpq;
+    pl.G = 2;
+    pl.nacc = 3;
   }
   pl.n_groups = (Nq + pl.QN - 1) / pl.QN;
   const int64_t tiles = (E + kTileM - 1) / kTileM;
-  const int64_t units = (int64_t)B * pl.n_groups;
-  const int64_t target = (int64_t)kNumSMs * 4;
-  int64_t splits = (target + units - 1) / units;
-  if (splits > tiles) splits = tiles;
-  if (splits < 1) splits = 1;
-  pl.n_splits = (int)splits;
-  pl.tmem_cols = next_pow2_at_least32(2 * pl.ncols + 2 * kSfCols);
+  if (Nq == 1) {
+    // persistent: two CTAs per SM over all (sequence, tile) pairs; a CTA spans at most
+    // kMaxSeqPerCta sequences
+    const int64_t total = (int64_t)B * tiles;
+    int64_t g = (int64_t)kNumSMs * 2;
+    const int64_t span_min = ((int64_t)B * tiles + (int64_t)(kMaxSeqPerCta - 1) * tiles - 1) /
+                             ((int64_t)(kMaxSeqPerCta - 1) * tiles);
+    if (g < span_min) g = span_min;
+    if (g > total) g = total;
+    pl.n_splits = (int)(g < 1 ? 1 : g);
+  } else {
+    const int64_t units = (int64_t)B * pl.n_groups;
+    const int64_t target = (int64_t)kNumSMs;
+    int64_t splits = (target + units - 1) / units;
+    if (splits > tiles) splits = tiles;
+    if (splits < 1) splits = 1;
+    pl.n_splits = (int)splits;
+  }
+  pl.tmem_cols = next_pow2_at_least32(pl.nacc * pl.G * pl.ncols + 2 * kSfCols);
   return pl;
 }
 
-cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* qi_codes,
+cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, const uint8_t* qi_codes,
                            const uint8_t* qi_scales, const uint8_t* ki_scales, uint16_t* scores,
                            int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I, int d_I,
                            const IndexerPlan& plan, uint32_t* status, cudaStream_t stream) {
@@ -302,14 +472,22 @@ cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* qi_codes,
   prm.m = m;
   prm.QN = plan.QN;
   prm.ncols = plan.ncols;
+  prm.G = plan.G;
+  prm.nacc = plan.nacc;
   prm.n_splits = plan.n_splits;
   prm.tmem_cols = plan.tmem_cols;
+  prm.B = B;
+  prm.tiles_per_seq = (int)((E + kTileM - 1) / kTileM);
+  prm.total_tiles = (int64_t)B * prm.tiles_per_seq;
+  prm.ki_codes = ki_codes;
   prm.status = status;
   const int NB = d_I / 32;
-#define CSA_IDX_CASE(HH, NN) \
-  if (H_I == HH && NB == NN) return launch_t<HH, NN>(kmap, prm, plan, B, stream);
-  CSA_IDX_CASE(1, 1) CSA_IDX_CASE(2, 1) CSA_IDX_CASE(4, 1) CSA_IDX_CASE(8, 1)
-  CSA_IDX_CASE(1, 2) CSA_IDX_CASE(2, 2) CSA_IDX_CASE(4, 2) CSA_IDX_CASE(8, 2)
+  const int SW = indexer_bulk_path(H_I, d_I, E) ? 2 : 1;
+#define CSA_IDX_CASE(HH, NN, SS) \
+  if (H_I == HH && NB == NN && SW == SS) return launch_t<HH, NN, SS>(kmap, prm, plan, B, stream);
+  CSA_IDX_CASE(1, 1, 1) CSA_IDX_CASE(2, 1, 1) CSA_IDX_CASE(4, 1, 1) CSA_IDX_CASE(8, 1, 1)
+  CSA_IDX_CASE(1, 2, 2) CSA_IDX_CASE(2, 2, 2) CSA_IDX_CASE(4, 2, 2) CSA_IDX_CASE(8, 2, 1)
+  CSA_IDX_CASE(1, 2, 1) CSA_IDX_CASE(2, 2, 1) CSA_IDX_CASE(4, 2, 1)
 #undef CSA_IDX_CASE
   return cudaErrorInvalidValue;
 }

@@ -6,7 +6,37 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace csa {
+
+// Launches `kern` with programmatic stream serialisation (the kernel may start while its
+// predecessor on the stream finishes; every kernel of the library waits on griddepcontrol before
+// touching data a predecessor wrote) and, when cluster_x > 1, as clusters of cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t stream, unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 constexpr int kNumSMs = 148;
 
@@ -22,12 +52,15 @@ cudaError_t launch_compress(const uint16_t* k_raw, const uint16_t* v_raw, const 
 struct IndexerPlan {
   int QN;        // queries per CTA
   int ncols;     // MMA N
+  int G;         // tiles per MMA commit / epilogue pass
+  int nacc;      // accumulator groups in tensor memory
   int n_groups;  // ceil(Nq / QN)
   int n_splits;  // entry-tile splits per (sequence, query group)
   int tmem_cols; // tensor-memory columns allocated per CTA
 };
 IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I);
-cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* qi_codes,
+bool indexer_bulk_path(int H_I, int d_I, int64_t E);
+cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, const uint8_t* qi_codes,
                            const uint8_t* qi_scales, const uint8_t* ki_scales, uint16_t* scores,
                            int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I, int d_I,
                            const IndexerPlan& plan, uint32_t* status, cudaStream_t stream);

@@ -59,8 +59,8 @@ extern "C" csa_status csa_index_topk_noalloc(const uint8_t* qi_codes, const uint
                                              int32_t* topk_cnt, void* stream) {
   if (!qi_codes || !qi_scales || !ki_codes || !ki_scales || !topk_idx || !topk_cnt)
     return CSA_ERR_INVALID_ARG;
-  if (!aligned16(qi_codes) || !aligned16(ki_codes) || !aligned16(topk_idx) ||
-      !aligned16(topk_cnt))
+  if (!aligned16(qi_codes) || !aligned16(ki_codes) || !aligned16(ki_scales) ||
+      !aligned16(topk_idx) || !aligned16(topk_cnt))
     return CSA_ERR_ALIGN;
   if (B < 1 || Nq < 1 || q_pos0 < 0 || E < 0 || m < 1 || k < 1) return CSA_ERR_INVALID_ARG;
   if (d_I != 32 && d_I != 64) return CSA_ERR_UNSUPPORTED;
@@ -85,7 +85,7 @@ extern "C" csa_status csa_index_topk_noalloc(const uint8_t* qi_codes, const uint
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return CSA_ERR_CUDA;
     const csa::IndexerPlan plan = csa::plan_indexer(B, Nq, E, H_I, d_I);
-    if (csa::launch_indexer(&map, qi_codes, qi_scales, ki_scales, scores, B, Nq, q_pos0, E, m, H_I,
+    if (csa::launch_indexer(&map, ki_codes, qi_codes, qi_scales, ki_scales, scores, B, Nq, q_pos0, E, m, H_I,
                             d_I, plan, status, st) != cudaSuccess)
       return CSA_ERR_CUDA;
   }

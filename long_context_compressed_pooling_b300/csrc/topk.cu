@@ -22,7 +22,7 @@
 namespace csa {
 namespace {
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 256;
 constexpr int kMaxChunkKeys = 16384;  // keys one CTA stages in shared memory (32 KB)
 
 CSA_DEV uint32_t order_key(uint32_t bits) {
@@ -30,13 +30,16 @@ CSA_DEV uint32_t order_key(uint32_t bits) {
   return (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
 }
 
-// Adds one to hist[bin] for every lane with valid set; lanes sharing a bin add once together.
-// Must be called by all 32 lanes of the warp.
-CSA_DEV void hist_add_warp(uint32_t* hist, uint32_t bin, bool valid) {
-  const uint32_t key = valid ? bin : 0xFFFFFFFFu;
-  const unsigned peers = __match_any_sync(0xffffffffu, key);
-  if (valid && (threadIdx.x & 31) == (unsigned)(__ffs(peers) - 1))
-    atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+constexpr int kWarps = kTopkThreads / 32;
+
+// Sums the per-warp histograms whist[kWarps][256] into hist[256] (all threads call it).
+CSA_DEV void reduce_warp_hists(const uint32_t* whist, uint32_t* hist) {
+  for (int q = threadIdx.x; q < 256; q += blockDim.x) {
+    uint32_t s = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += whist[w * 256 + q];
+    hist[q] = s;
+  }
 }
 
 // Finds the bin b with count(bins > b) < need <= count(bins >= b) over 256 bins; writes the bin
@@ -121,7 +124,20 @@ CSA_DEV void block_scan2(uint32_t a, uint32_t b, uint32_t* ex_a, uint32_t* ex_b,
   __syncthreads();  // wa / wb are reused by the next call
 }
 
+// Sum of the 32-bit word at `p` over CTAs 0..n-1 of the cluster (n <= 16): all remote loads are
+// issued before any of them is consumed.
+CSA_DEV uint32_t cluster_sum(const uint32_t* p, uint32_t n) {
+  uint32_t v[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) v[c] = (uint32_t)c < n ? dsmem_ld_u32(p, (uint32_t)c) : 0u;
+  uint32_t s = 0;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) s += v[c];
+  return s;
+}
+
 struct TopkShared {
+  uint32_t whist[kWarps * 256];  // per-warp histograms (plain shared atomics, no cross-warp contention)
   uint32_t hist1[256];
   uint32_t hist2[256];
   uint32_t gsum[256];
@@ -138,6 +154,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __re
                                                             int32_t* __restrict__ topk_cnt) {
   extern __shared__ uint16_t skeys[];  // `cap` keys: this CTA's chunk when it fits
   __shared__ TopkShared sh;
+  pdl_trigger();
+  pdl_wait();
   const uint32_t C = cluster_nctarank();
   const uint32_t rank = cluster_ctarank();
   const int64_t row = blockIdx.y;  // b * Nq + i
@@ -158,30 +176,31 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __re
   const int64_t lo = min(n, (int64_t)rank * L), hi = min(n, lo + L);
   const int len = (int)(hi - lo);
   const bool cached = len <= cap;
-  if (cached)
-    for (int r = tid; r < len; r += nt) skeys[r] = (uint16_t)order_key(src[lo + r]);
+  if (cached) {
+    for (int r0 = tid; r0 < len; r0 += 4 * nt) {  // four independent loads in flight per thread
+      uint32_t v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = r0 + u * nt < len ? (uint32_t)src[lo + r0 + u * nt] : 0u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (r0 + u * nt < len) skeys[r0 + u * nt] = (uint16_t)order_key(v[u]);
+    }
+  }
   auto key_at = [&](int r) -> uint32_t {
     return cached ? (uint32_t)skeys[r] : order_key(src[lo + r]);
   };
-  for (int q = tid; q < 256; q += nt) {
-    sh.hist1[q] = 0u;
-    sh.hist2[q] = 0u;
-  }
+  uint32_t* wh = sh.whist + (tid >> 5) * 256;
+  for (int q = tid; q < kWarps * 256; q += nt) sh.whist[q] = 0u;
   __syncthreads();
 
   // ---- digit 1: high byte --------------------------------------------------------------------
-  for (int base = 0; base < len; base += nt) {
-    const int r = base + tid;
-    const bool v = r < len;
-    hist_add_warp(sh.hist1, v ? key_at(r) >> 8 : 0u, v);
-  }
+  for (int r = tid; r < len; r += nt) atomicAdd(&wh[key_at(r) >> 8], 1u);
+  __syncthreads();
+  reduce_warp_hists(sh.whist, sh.hist1);
+  for (int q = tid; q < kWarps * 256; q += nt) sh.whist[q] = 0u;
   __syncthreads();
   cluster_sync();
-  for (int q = tid; q < 256; q += nt) {
-    uint32_t s = 0;
-    for (uint32_t c = 0; c < C; ++c) s += dsmem_ld_u32(&sh.hist1[q], c);
-    sh.gsum[q] = s;
-  }
+  for (int q = tid; q < 256; q += nt) sh.gsum[q] = cluster_sum(&sh.hist1[q], C);
   __syncthreads();
   select_bin(sh.gsum, (uint32_t)k, &sh.bin, &sh.above);
   __syncthreads();
@@ -189,23 +208,15 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __re
   const uint32_t above_hi = sh.above;
 
   // ---- digit 2: low byte inside the high bin -------------------------------------------------
-  for (int base = 0; base < len; base += nt) {
-    const int r = base + tid;
-    uint32_t kk = 0;
-    bool v = r < len;
-    if (v) {
-      kk = key_at(r);
-      v = (kk >> 8) == hi_byte;
-    }
-    hist_add_warp(sh.hist2, kk & 0xFFu, v);
+  for (int r = tid; r < len; r += nt) {
+    const uint32_t kk = key_at(r);
+    if ((kk >> 8) == hi_byte) atomicAdd(&wh[kk & 0xFFu], 1u);
   }
   __syncthreads();
+  reduce_warp_hists(sh.whist, sh.hist2);
+  __syncthreads();
   cluster_sync();
-  for (int q = tid; q < 256; q += nt) {
-    uint32_t s = 0;
-    for (uint32_t c = 0; c < C; ++c) s += dsmem_ld_u32(&sh.hist2[q], c);
-    sh.gsum[q] = s;
-  }
+  for (int q = tid; q < 256; q += nt) sh.gsum[q] = cluster_sum(&sh.hist2[q], C);
   __syncthreads();
   select_bin(sh.gsum, (uint32_t)k - above_hi, &sh.bin, &sh.above);
   __syncthreads();
@@ -235,11 +246,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __re
   }
   __syncthreads();
   cluster_sync();
-  uint32_t gt_before = 0, eq_before = 0;  // keys of the lower-ranked CTAs of this row
-  for (uint32_t c = 0; c < rank; ++c) {
-    gt_before += dsmem_ld_u32(&sh.cta_gt, c);
-    eq_before += dsmem_ld_u32(&sh.cta_eq, c);
-  }
+  // keys of the lower-ranked CTAs of this row
+  uint32_t gt_before = cluster_sum(&sh.cta_gt, rank), eq_before = cluster_sum(&sh.cta_eq, rank);
   for (int rd = 0; rd < rounds; ++rd) {
     const int g = rd * nt + tid;
     uint32_t c_gt = 0, c_eq = 0;
@@ -298,12 +306,14 @@ cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, i
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kTopkThreads, 1, 1);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   // Clusters of 16 are a non-portable size: fall back to 8 if this GPU cannot hold one.
   for (;; C >>= 1) {
     const int64_t chunk = (n_max + C - 1) / C;
