@@ -22,15 +22,15 @@
 // sums stay exact for the scale range the workloads use (2^-4..2^0): the BF16 rounding is then
 // the only rounding, as the method specifies.
 //
-// Pipeline. Work is processed in groups of G tiles: the TMA warp loads a group into one slot
-// of a 12-tile ring, the MMA thread issues the group's G MMAs into the next accumulator group of
-// a ring in tensor memory (3 groups of 4 x 16 columns for decode, 3 of 2 x 64 for prefill) and
-// commits once, and eight epilogue warps (two per tensor-memory lane quarter) drain the group
-// together. The commit -> epilogue round trip is paid once per group,
-// not per tile. The first groups' loads are issued before the CTA's set-up so their DRAM latency
-// overlaps it. Decode (one query per sequence) runs persistent CTAs over all (sequence, tile)
-// pairs; prefill gives each CTA one (sequence, query group). Every mbarrier wait is bounded
-// (kFlagTimeout on expiry).
+// Pipeline. A copy warp fills a 3-slot ring (8 tiles per slot: one bulk copy of codes and one
+// of scales per slot, since each copy instruction costs ~0.3 us to issue whatever its size); it
+// starts at once and never joins the set-up barriers of the other warps. The MMA warp issues
+// groups of G tiles (one elected lane of a converged warp) into the next accumulator group of a
+// ring in tensor memory (3 x 4 x 16 columns for decode, 3 x 2 x 64 for prefill) and commits
+// once per group; eight epilogue warps (two per tensor-memory lane quarter) drain a group
+// together, so the commit -> epilogue round trip is paid once per group. Decode (one query per
+// sequence) runs persistent CTAs over all (sequence, tile) pairs; prefill gives each CTA one
+// (sequence, query group). Every mbarrier wait is bounded (kFlagTimeout on expiry).
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
