@@ -13,8 +13,15 @@
 // after a hardware cluster barrier, and every CTA derives the same threshold. For the
 // compaction each CTA counts its keys above / equal to T, reads the counts of the lower-ranked
 // CTAs of its cluster, and writes its selected indices at their final, ascending positions.
-// Decode rows (few rows, up to 262144 entries) use clusters of up to 16 CTAs; prefill (thousands
-// of rows) uses one CTA per row. No grid-wide synchronisation and no spin waits are involved.
+// Rows of up to 32768 entries (decode at 128K context, every prefill row) take one CTA of 1024
+// threads holding the row in registers (32 contiguous keys per thread) and no cluster phase at
+// all; longer rows (decode at 1M context) use clusters of up to 16 CTAs. No grid-wide
+// synchronisation and no spin waits are involved.
+//
+// Fast threshold: scores sit on the BF16 grid, so most of a row's top k lie within 255 grid
+// steps of the row maximum. One histogram of (max - key) over those 255 steps finds T in a
+// single pass; only when fewer than k keys fall in that band does the exact two-digit radix
+// select run.
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
@@ -22,22 +29,23 @@
 namespace csa {
 namespace {
 
-constexpr int kTopkThreads = 256;
-constexpr int kMaxChunkKeys = 16384;  // keys one CTA stages in shared memory (32 KB)
+constexpr int kClusterThreads = 256;   // threads per CTA of a multi-CTA (cluster) row
+constexpr int kRowThreads = 1024;      // threads of a one-CTA row
+constexpr int kMaxChunkKeys = 16384;   // keys one cluster CTA stages in shared memory (32 KB)
+constexpr int kMaxRowKeys = 32768;     // keys a one-CTA row stages in shared memory (64 KB)
 
 CSA_DEV uint32_t order_key(uint32_t bits) {
   if (bits == 0x8000u) bits = 0u;  // -0 counts as +0
   return (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
 }
 
-constexpr int kWarps = kTopkThreads / 32;
-
-// Sums the per-warp histograms whist[kWarps][256] into hist[256] (all threads call it).
+// Sums the per-warp histograms whist[NW][256] into hist[256] (all threads call it).
+template <int NW>
 CSA_DEV void reduce_warp_hists(const uint32_t* whist, uint32_t* hist) {
   for (int q = threadIdx.x; q < 256; q += blockDim.x) {
     uint32_t s = 0;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) s += whist[w * 256 + q];
+    for (int w = 0; w < NW; ++w) s += whist[w * 256 + q];
     hist[q] = s;
   }
 }
@@ -73,6 +81,52 @@ CSA_DEV void select_bin(const uint32_t* hist, uint32_t need, int* out_bin, uint3
       }
     }
   }
+}
+
+// Finds the first bin b (ascending) with prefix(b-1) < need <= prefix(b) over bins [0, 255);
+// writes b and prefix(b-1), or bin -1 when the 255 bins hold fewer than `need`. Warp 0 only.
+CSA_DEV void select_prefix(const uint32_t* hist, uint32_t need, int* out_bin, uint32_t* out_before) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    uint32_t local[8];
+    uint32_t tot = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int bin = lane * 8 + q;
+      local[q] = bin < 255 ? hist[bin] : 0u;
+      tot += local[q];
+    }
+    uint32_t inc = tot;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += v;
+    }
+    const uint32_t exc = inc - tot;
+    if (lane == 31 && inc < need) *out_bin = -1;
+    if (exc < need && need <= inc) {
+      uint32_t run = exc;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (run < need && need <= run + local[q]) {
+          *out_bin = lane * 8 + q;
+          *out_before = run;
+        }
+        run += local[q];
+      }
+    }
+  }
+}
+
+// Largest 32-bit word at `p` over CTAs 0..n-1 of the cluster (n <= 16).
+CSA_DEV uint32_t cluster_max(const uint32_t* p, uint32_t n) {
+  uint32_t v[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) v[c] = (uint32_t)c < n ? dsmem_ld_u32(p, (uint32_t)c) : 0u;
+  uint32_t m = 0;
+#pragma unroll
+  for (int c = 0; c < 16; ++c) m = max(m, v[c]);
+  return m;
 }
 
 // Block-wide exclusive scan of two counters (one pair per thread); also returns the totals.
@@ -136,8 +190,11 @@ CSA_DEV uint32_t cluster_sum(const uint32_t* p, uint32_t n) {
   return s;
 }
 
+template <int NW>
 struct TopkShared {
-  uint32_t whist[kWarps * 256];  // per-warp histograms (plain shared atomics, no cross-warp contention)
+  uint32_t whist[NW * 256];  // per-warp histograms (plain shared atomics, no cross-warp contention)
+  uint32_t wmax[32];
+  uint32_t cta_max;          // this CTA's largest key (read by the cluster)
   uint32_t hist1[256];
   uint32_t hist2[256];
   uint32_t gsum[256];
@@ -147,13 +204,15 @@ struct TopkShared {
   uint32_t above;
 };
 
-__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __restrict__ scores,
-                                                            int Nq, int64_t q_pos0, int64_t E,
-                                                            int m, int k, int cap,
-                                                            int32_t* __restrict__ topk_idx,
-                                                            int32_t* __restrict__ topk_cnt) {
+// NT threads per CTA; the cluster (1 to 16 CTAs) works on one row.
+template <int NT>
+__global__ void __launch_bounds__(NT) topk_kernel(const uint16_t* __restrict__ scores, int Nq,
+                                                  int64_t q_pos0, int64_t E, int m, int k, int cap,
+                                                  int32_t* __restrict__ topk_idx,
+                                                  int32_t* __restrict__ topk_cnt) {
+  constexpr int NW = NT / 32;
   extern __shared__ uint16_t skeys[];  // `cap` keys: this CTA's chunk when it fits
-  __shared__ TopkShared sh;
+  __shared__ TopkShared<NW> sh;
   pdl_trigger();
   pdl_wait();
   const uint32_t C = cluster_nctarank();
@@ -163,7 +222,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __re
   const int64_t n = max((int64_t)0, min(E, (t + 1) / m));
   const uint16_t* src = scores + row * E;
   int32_t* out = topk_idx + row * (int64_t)k;
-  const int tid = threadIdx.x, nt = blockDim.x;
+  const int tid = threadIdx.x, nt = NT;
 
   if (n <= k) {  // uniform over the cluster: every CTA of it works on this row
     for (int64_t r = (int64_t)rank * nt + tid; r < k; r += (int64_t)C * nt)
@@ -190,38 +249,90 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __re
     return cached ? (uint32_t)skeys[r] : order_key(src[lo + r]);
   };
   uint32_t* wh = sh.whist + (tid >> 5) * 256;
-  for (int q = tid; q < kWarps * 256; q += nt) sh.whist[q] = 0u;
+  for (int q = tid; q < NW * 256; q += nt) sh.whist[q] = 0u;
   __syncthreads();
 
-  // ---- digit 1: high byte --------------------------------------------------------------------
-  for (int r = tid; r < len; r += nt) atomicAdd(&wh[key_at(r) >> 8], 1u);
+  // ---- the row's largest key -------------------------------------------------------------------
+  uint32_t mx = 0;
+  for (int r = tid; r < len; r += nt) mx = max(mx, key_at(r));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((tid & 31) == 0) sh.wmax[tid >> 5] = mx;
   __syncthreads();
-  reduce_warp_hists(sh.whist, sh.hist1);
-  for (int q = tid; q < kWarps * 256; q += nt) sh.whist[q] = 0u;
-  __syncthreads();
-  cluster_sync();
-  for (int q = tid; q < 256; q += nt) sh.gsum[q] = cluster_sum(&sh.hist1[q], C);
-  __syncthreads();
-  select_bin(sh.gsum, (uint32_t)k, &sh.bin, &sh.above);
-  __syncthreads();
-  const uint32_t hi_byte = (uint32_t)sh.bin;
-  const uint32_t above_hi = sh.above;
-
-  // ---- digit 2: low byte inside the high bin -------------------------------------------------
-  for (int r = tid; r < len; r += nt) {
-    const uint32_t kk = key_at(r);
-    if ((kk >> 8) == hi_byte) atomicAdd(&wh[kk & 0xFFu], 1u);
+  if (tid == 0) {
+    uint32_t m2 = 0;
+    for (int w = 0; w < NW; ++w) m2 = max(m2, sh.wmax[w]);
+    sh.cta_max = m2;
   }
   __syncthreads();
-  reduce_warp_hists(sh.whist, sh.hist2);
+  if (C > 1) cluster_sync();
+  const uint32_t row_max = C > 1 ? cluster_max(&sh.cta_max, C) : sh.cta_max;
+
+  // ---- near-max histogram: one bin per BF16 step below the maximum ---------------------------
+  // The k-th largest key of a row with k << n sits a few octaves of BF16 steps below the
+  // maximum, so only the keys within 255 steps are counted: few atomics and no hot bin (a
+  // histogram of the high byte would pile almost every score into the same few bins).
+  for (int r = tid; r < len; r += nt) {
+    const uint32_t dd = row_max - key_at(r);
+    if (dd < 255u) atomicAdd(&wh[dd], 1u);
+  }
   __syncthreads();
-  cluster_sync();
-  for (int q = tid; q < 256; q += nt) sh.gsum[q] = cluster_sum(&sh.hist2[q], C);
+  reduce_warp_hists<NW>(sh.whist, sh.hist1);
   __syncthreads();
-  select_bin(sh.gsum, (uint32_t)k - above_hi, &sh.bin, &sh.above);
+  for (int q = tid; q < NW * 256; q += nt) sh.whist[q] = 0u;
+  if (C > 1) {
+    cluster_sync();
+    for (int q = tid; q < 256; q += nt) sh.gsum[q] = cluster_sum(&sh.hist1[q], C);
+  } else {
+    for (int q = tid; q < 256; q += nt) sh.gsum[q] = sh.hist1[q];
+  }
   __syncthreads();
-  const uint32_t T = (hi_byte << 8) | (uint32_t)sh.bin;
-  const uint32_t need_eq = (uint32_t)k - (above_hi + sh.above);
+  select_prefix(sh.gsum, (uint32_t)k, &sh.bin, &sh.above);
+  __syncthreads();
+  uint32_t T, need_eq;
+  if (sh.bin >= 0) {
+    T = row_max - (uint32_t)sh.bin;
+    need_eq = (uint32_t)k - sh.above;
+  } else {
+    // Fallback (the k-th key lies further below the maximum): exact two-digit radix select.
+    __syncthreads();
+    // ---- digit 1: high byte ----
+    for (int r = tid; r < len; r += nt) atomicAdd(&wh[key_at(r) >> 8], 1u);
+    __syncthreads();
+    reduce_warp_hists<NW>(sh.whist, sh.hist2);
+    __syncthreads();  // every bin is summed before the per-warp histograms are cleared
+    for (int q = tid; q < NW * 256; q += nt) sh.whist[q] = 0u;
+    if (C > 1) {
+      cluster_sync();
+      for (int q = tid; q < 256; q += nt) sh.gsum[q] = cluster_sum(&sh.hist2[q], C);
+    } else {
+      for (int q = tid; q < 256; q += nt) sh.gsum[q] = sh.hist2[q];
+    }
+    __syncthreads();
+    select_bin(sh.gsum, (uint32_t)k, &sh.bin, &sh.above);
+    __syncthreads();
+    const uint32_t hi_byte = (uint32_t)sh.bin;
+    const uint32_t above_hi = sh.above;
+    // ---- digit 2: low byte inside the high bin ----
+    for (int r = tid; r < len; r += nt) {
+      const uint32_t kk = key_at(r);
+      if ((kk >> 8) == hi_byte) atomicAdd(&wh[kk & 0xFFu], 1u);
+    }
+    __syncthreads();
+    reduce_warp_hists<NW>(sh.whist, sh.hist1);
+    __syncthreads();
+    if (C > 1) {
+      cluster_sync();
+      for (int q = tid; q < 256; q += nt) sh.gsum[q] = cluster_sum(&sh.hist1[q], C);
+    } else {
+      for (int q = tid; q < 256; q += nt) sh.gsum[q] = sh.hist1[q];
+    }
+    __syncthreads();
+    select_bin(sh.gsum, (uint32_t)k - above_hi, &sh.bin, &sh.above);
+    __syncthreads();
+    T = (hi_byte << 8) | (uint32_t)sh.bin;
+    need_eq = (uint32_t)k - (above_hi + sh.above);
+  }
 
   // ---- ordered compaction: rounds of nt groups of 8 consecutive keys -------------------------
   const int groups = (len + 7) / 8;
@@ -245,9 +356,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __re
     sh.cta_eq = cta_eq;
   }
   __syncthreads();
-  cluster_sync();
   // keys of the lower-ranked CTAs of this row
-  uint32_t gt_before = cluster_sum(&sh.cta_gt, rank), eq_before = cluster_sum(&sh.cta_eq, rank);
+  uint32_t gt_before = 0, eq_before = 0;
+  if (C > 1) {
+    cluster_sync();
+    gt_before = cluster_sum(&sh.cta_gt, rank);
+    eq_before = cluster_sum(&sh.cta_eq, rank);
+  }
   for (int rd = 0; rd < rounds; ++rd) {
     const int g = rd * nt + tid;
     uint32_t c_gt = 0, c_eq = 0;
@@ -266,11 +381,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __re
     for (int j = 0; j < 8; ++j) {
       const uint32_t kk = keys8[j];
       const int64_t idx = lo + (int64_t)g * 8 + j;
+      // positions are < k by construction; the guard keeps any inconsistency inside the row
       if (kk > T) {
-        out[gb + min(eb, need_eq)] = (int32_t)idx;
+        const uint32_t pos = gb + min(eb, need_eq);
+        if (pos < (uint32_t)k) out[pos] = (int32_t)idx;
         ++gb;
       } else if (kk == T) {
-        if (eb < need_eq) out[gb + eb] = (int32_t)idx;
+        if (eb < need_eq && gb + eb < (uint32_t)k) out[gb + eb] = (int32_t)idx;
         ++eb;
       }
     }
@@ -278,33 +395,161 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const uint16_t* __re
     eq_before += te;
   }
   if (rank == 0 && tid == 0) topk_cnt[row] = k;
-  cluster_sync();  // no CTA leaves while another may still read its shared memory
+  if (C > 1) cluster_sync();  // no CTA leaves while another may still read its shared memory
+}
+
+
+// Rows of up to 32768 entries: one CTA of 1024 threads; thread t owns the contiguous keys
+// [t*KPT, t*KPT + KPT) in registers (KPT = 32), loaded with four 16-byte loads when the row is
+// 16-byte aligned. Max, near-max histogram, counts and the ordered write all run on registers;
+// one block scan orders the output because every thread's segment is contiguous.
+constexpr int kKPT = 32;
+__global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const uint16_t* __restrict__ scores,
+                                                               int Nq, int64_t q_pos0, int64_t E,
+                                                               int m, int k,
+                                                               int32_t* __restrict__ topk_idx,
+                                                               int32_t* __restrict__ topk_cnt) {
+  constexpr int NW = kRowThreads / 32;
+  __shared__ uint32_t whist[NW * 256];
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t wmax[NW];
+  __shared__ uint32_t wa[33], wb[33];
+  __shared__ int sh_bin;
+  __shared__ uint32_t sh_above;
+  pdl_trigger();
+  pdl_wait();
+  const int64_t row = blockIdx.x;
+  const int64_t t = q_pos0 + (row % Nq);
+  const int n = (int)max((int64_t)0, min(E, (t + 1) / m));
+  const uint16_t* src = scores + row * E;
+  int32_t* out = topk_idx + row * (int64_t)k;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  if (n <= k) {
+    for (int r = tid; r < k; r += kRowThreads) out[r] = (r < n) ? r : -1;
+    if (tid == 0) topk_cnt[row] = n;
+    return;
+  }
+  // ---- keys of this thread's segment -----------------------------------------------------------
+  const int seg0 = tid * kKPT;
+  uint32_t key[kKPT];
+  const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) && seg0 + kKPT <= n;
+  if (vec) {
+    uint4 v[kKPT / 8];
+#pragma unroll
+    for (int q = 0; q < kKPT / 8; ++q) v[q] = __ldg(reinterpret_cast<const uint4*>(src + seg0) + q);
+#pragma unroll
+    for (int q = 0; q < kKPT / 8; ++q) {
+      const uint32_t u[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        key[q * 8 + 2 * h] = order_key(u[h] & 0xFFFFu);
+        key[q * 8 + 2 * h + 1] = order_key(u[h] >> 16);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kKPT; ++j) key[j] = seg0 + j < n ? order_key(src[seg0 + j]) : 0u;
+  }
+  // slots past the row end hold 0 and are excluded by index, never by value
+  // ---- row maximum ----
+  uint32_t mx = 0;
+#pragma unroll
+  for (int j = 0; j < kKPT; ++j) mx = max(mx, key[j]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) wmax[w] = mx;
+  for (int q = tid; q < NW * 256; q += kRowThreads) whist[q] = 0u;
+  __syncthreads();
+  uint32_t row_max = 0;
+#pragma unroll
+  for (int q = 0; q < NW; ++q) row_max = max(row_max, wmax[q]);
+  // ---- near-max histogram (one bin per BF16 step below the maximum) ----
+  uint32_t* wh = whist + w * 256;
+#pragma unroll
+  for (int j = 0; j < kKPT; ++j) {
+    const uint32_t dd = row_max - key[j];
+    if (dd < 255u && seg0 + j < n) atomicAdd(&wh[dd], 1u);
+  }
+  __syncthreads();
+  reduce_warp_hists<NW>(whist, hist);
+  __syncthreads();
+  select_prefix(hist, (uint32_t)k, &sh_bin, &sh_above);
+  __syncthreads();
+  uint32_t T, need_eq;
+  if (sh_bin >= 0) {
+    T = row_max - (uint32_t)sh_bin;
+    need_eq = (uint32_t)k - sh_above;
+  } else {
+    // fallback: exact two-digit radix select on the registers
+    for (int q = tid; q < NW * 256; q += kRowThreads) whist[q] = 0u;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kKPT; ++j)
+      if (seg0 + j < n) atomicAdd(&wh[key[j] >> 8], 1u);
+    __syncthreads();
+    reduce_warp_hists<NW>(whist, hist);
+    __syncthreads();
+    for (int q = tid; q < NW * 256; q += kRowThreads) whist[q] = 0u;
+    select_bin(hist, (uint32_t)k, &sh_bin, &sh_above);
+    __syncthreads();
+    const uint32_t hi_byte = (uint32_t)sh_bin, above_hi = sh_above;
+#pragma unroll
+    for (int j = 0; j < kKPT; ++j)
+      if (seg0 + j < n && (key[j] >> 8) == hi_byte) atomicAdd(&wh[key[j] & 0xFFu], 1u);
+    __syncthreads();
+    reduce_warp_hists<NW>(whist, hist);
+    __syncthreads();
+    select_bin(hist, (uint32_t)k - above_hi, &sh_bin, &sh_above);
+    __syncthreads();
+    T = (hi_byte << 8) | (uint32_t)sh_bin;
+    need_eq = (uint32_t)k - (above_hi + sh_above);
+  }
+  // ---- ordered write: one scan over the threads' contiguous segments ----
+  uint32_t c_gt = 0, c_eq = 0;
+#pragma unroll
+  for (int j = 0; j < kKPT; ++j) {
+    c_gt += (seg0 + j < n) && key[j] > T;
+    c_eq += (seg0 + j < n) && key[j] == T;
+  }
+  uint32_t gb, eb, tg, te;
+  block_scan2(c_gt, c_eq, &gb, &eb, &tg, &te, wa, wb);
+#pragma unroll
+  for (int j = 0; j < kKPT; ++j) {
+    const uint32_t kk = key[j];
+    if (seg0 + j >= n) {
+    } else if (kk > T) {
+      const uint32_t pos = gb + min(eb, need_eq);
+      if (pos < (uint32_t)k) out[pos] = seg0 + j;
+      ++gb;
+    } else if (kk == T) {
+      if (eb < need_eq && gb + eb < (uint32_t)k) out[gb + eb] = seg0 + j;
+      ++eb;
+    }
+  }
+  if (tid == 0) topk_cnt[row] = k;
 }
 
 int pick_cluster(int64_t rows, int64_t n_max) {
+  if (n_max <= kMaxRowKeys) return 1;
   int C = 1;
   while (C < 16 && rows * C < kNumSMs && n_max / (2 * C) >= 2048) C <<= 1;
   while (C < 16 && (n_max + C - 1) / C > kMaxChunkKeys) C <<= 1;
   return C;
 }
 
-}  // namespace
-
-cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
-                        int k, int32_t* topk_idx, int32_t* topk_cnt, cudaStream_t stream) {
-  const int64_t rows = (int64_t)B * Nq;
-  if (rows <= 0) return cudaSuccess;
-  int64_t n_max = min(E, (q_pos0 + Nq) / m);
-  if (n_max < 0) n_max = 0;
-  int C = pick_cluster(rows, n_max);
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kMaxChunkKeys * 2);
+template <int NT>
+cudaError_t launch_topk_t(const uint16_t* scores, int Nq, int64_t q_pos0, int64_t E, int m, int k,
+                          int32_t* topk_idx, int32_t* topk_cnt, int64_t rows, int64_t n_max,
+                          int C, int chunk_cap, cudaStream_t stream) {
+  auto kern = topk_kernel<NT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       chunk_cap * 2);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   int cap = 0;
   cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kTopkThreads, 1, 1);
+  cfg.blockDim = dim3(NT, 1, 1);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -317,19 +562,36 @@ cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, i
   // Clusters of 16 are a non-portable size: fall back to 8 if this GPU cannot hold one.
   for (;; C >>= 1) {
     const int64_t chunk = (n_max + C - 1) / C;
-    cap = (n_max > k && chunk <= kMaxChunkKeys) ? (int)chunk : 0;
+    cap = (n_max > k && chunk <= chunk_cap) ? (int)chunk : 0;
     cfg.dynamicSmemBytes = (size_t)cap * 2;
     cfg.gridDim = dim3((unsigned)C, (unsigned)rows, 1);
     attr[0].val.clusterDim.x = (unsigned)C;
     int nclusters = 0;
-    if (C <= 8 || (cudaOccupancyMaxActiveClusters(&nclusters, topk_kernel, &cfg) == cudaSuccess &&
+    if (C <= 8 || (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) == cudaSuccess &&
                    nclusters > 0))
       break;
     (void)cudaGetLastError();
   }
   ProfScope prof(stream, "topk");
-  return cudaLaunchKernelEx(&cfg, topk_kernel, scores, Nq, q_pos0, E, m, k, cap, topk_idx,
-                            topk_cnt);
+  return cudaLaunchKernelEx(&cfg, kern, scores, Nq, q_pos0, E, m, k, cap, topk_idx, topk_cnt);
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
+                        int k, int32_t* topk_idx, int32_t* topk_cnt, cudaStream_t stream) {
+  const int64_t rows = (int64_t)B * Nq;
+  if (rows <= 0) return cudaSuccess;
+  int64_t n_max = min(E, (q_pos0 + Nq) / m);
+  if (n_max < 0) n_max = 0;
+  const int C = pick_cluster(rows, n_max);
+  if (C == 1) {
+    ProfScope prof(stream, "topk");
+    return launch_ex(topk_row_kernel, dim3((unsigned)rows), dim3(kRowThreads), 0, stream, 1,
+                     scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt);
+  }
+  return launch_topk_t<kClusterThreads>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows,
+                                        n_max, C, kMaxChunkKeys, stream);
 }
 
 }  // namespace csa
