@@ -24,7 +24,9 @@
 //
 // Pipeline. A copy warp fills a 3-slot ring (8 tiles per slot: one bulk copy of codes and one
 // of scales per slot, since each copy instruction costs ~0.3 us to issue whatever its size); it
-// starts at once and never joins the set-up barriers of the other warps. The MMA warp issues
+// starts at once and never joins the set-up barriers of the other warps. A slot is refilled only
+// after the MMAs that read its codes have completed AND every epilogue warp has finished the
+// slot's last group (the epilogue reads the slot's scale tile). The MMA warp issues
 // groups of G tiles (one elected lane of a converged warp) into the next accumulator group of a
 // ring in tensor memory (3 x 4 x 16 columns for decode, 3 x 2 x 64 for prefill) and commits
 // once per group; eight epilogue warps (two per tensor-memory lane quarter) drain a group
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 1 + 4 * kEW);  // the MMAs' commit + every epilogue warp
     }
     for (int a = 0; a < p.nacc; ++a) {
       mbar_init(&tfull[a], 1);
@@ -323,12 +325,18 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
     for (int g = 0; g < ngroups; ++g) {
       const int a = g % p.nacc;
       const uint32_t aph = (uint32_t)(g / p.nacc) & 1u;
-      if (!mbar_wait_warp(&tfull[a], aph, p.status)) {
+      const int unit = g * G / kSlotTiles;
+      const int slot = unit % kSlots;
+      // The slot's scale tile is read below: acquire the copy that filled it (its phase is
+      // complete, and it cannot be refilled before this warp releases it).
+      if (!mbar_wait_warp(&tfull[a], aph, p.status) ||
+          (SW == 2 && !mbar_wait_warp(&full[slot], (uint32_t)(unit / kSlots) & 1u, p.status))) {
         if (lane == 0) *aborted = 1;
         break;
       }
       tc_fence_after();
       const int nt = min(G, ntiles - g * G);
+      const bool unit_done = (g + 1) * G >= min(ntiles, (unit + 1) * kSlotTiles);
       for (int u = sub; u < nt * cchunks; u += kEW) {
         const int i = u / cchunks, c0 = (u % cchunks) * 16;
         const int it = g * G + i;
@@ -378,7 +386,11 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[a]);
+      if (lane == 0) {
+        mbar_arrive(&tempty[a]);
+        // the slot's last group: its scale tile is no longer read by this warp
+        if (unit_done) mbar_arrive(&empty[slot]);
+      }
     }
     tc_fence_before();
     __syncwarp();

@@ -75,6 +75,8 @@ INDEX_CASES = [
     (1, 70, 500, 600, 4, 4, 64, 24),     # prefill chunk, several query groups
     (2, 9, 1500, 2048, 4, 8, 64, 32),    # 8 indexer heads
     (1, 5, 95, 128, 1, 1, 32, 7),        # block size 1, one head
+    (1, 12, 60000, 64000, 4, 4, 64, 100),  # prefill, ~120 tiles per CTA: the copy ring wraps
+    (4, 1, 1048575, 1048576, 4, 4, 64, 512),  # decode at 1M: ~28 tiles per CTA, ring wraps
 ]
 
 
