@@ -1,4 +1,6 @@
-// CSA sparse attention and HCA dense attention over compressed entries plus a sliding window.
+// CSA sparse attention and HCA dense attention over compressed entries plus a sliding window:
+// the mma.sync kernel (head dim 64), the split planner, the workspace merge and the dispatcher
+// (head dim 128 goes to the tcgen05 kernel in attend_tc.cu).
 //
 // Lighthouse "deep deepseek v4 release" 八.3: CSA attends to the top-k selected compressed
 // entries plus a sliding-window branch of n_win raw tokens; HCA attends densely to every
@@ -397,13 +399,17 @@ struct SplitPlan {
   int cluster;  // 1: merge inside a cluster of n_splits CTAs
 };
 
-SplitPlan plan_splits(int tokens, int H, int64_t max_keys) {
+// Splits of a token's key chunks over CTAs. The mma.sync kernel (64-key chunks, two CTAs per SM)
+// aims at 2 x 148 CTAs; the tcgen05 kernel (128-key chunks, one CTA per SM) at one wave of 148.
+SplitPlan plan_splits(int tokens, int H, int64_t max_keys, int d) {
+  const bool tc = d == 128;
+  const int64_t kc = tc ? attend_tc_chunk_keys() : kKC;
   const int64_t groups = (H + 63) / 64;
-  const int64_t chunks = (max_keys + kKC - 1) / kKC;
+  const int64_t chunks = (max_keys + kc - 1) / kc;
   const int64_t units = (int64_t)tokens * groups;
-  const int64_t target = (int64_t)kNumSMs * 2;
+  const int64_t target = tc ? (int64_t)kNumSMs : (int64_t)kNumSMs * 2;
   if (units >= target || chunks <= 1) return {1, 0};
-  int64_t s = (target + units - 1) / units;
+  int64_t s = tc ? target / units : (target + units - 1) / units;
   if (s > chunks) s = chunks;
   if (s <= 1) return {1, 0};
   if (s <= kMaxClusterSplits) return {(int)s, 1};
@@ -462,19 +468,49 @@ cudaError_t launch_d(AttnParams prm, int groups, int nw, cudaStream_t stream) {
 
 }  // namespace
 
-int plan_attend_splits(int tokens, int H, int64_t max_keys) {
-  return plan_splits(tokens, H, max_keys).n_splits;
+int plan_attend_splits(int tokens, int H, int d, int64_t max_keys) {
+  return plan_splits(tokens, H, max_keys, d).n_splits;
 }
 
 size_t attend_workspace_bytes(int tokens, int H, int d, int64_t max_keys) {
   // The workspace covers the non-cluster merge, which is also the fallback of the cluster one.
-  const int s = plan_splits(tokens, H, max_keys).n_splits;
+  const int s = plan_splits(tokens, H, max_keys, d).n_splits;
   if (s <= 1) return 0;
   return (size_t)s * tokens * H * (size_t)(d + 2) * sizeof(float);
 }
 
+namespace {
+cudaError_t launch_merge(int D, const float* ws_o, const float* ws_ml, int n_splits, int tokens,
+                         int H, uint16_t* out, float* lse, cudaStream_t stream) {
+  ProfScope prof(stream, "lse_merge");
+  const dim3 grid((unsigned)((int64_t)tokens * H));
+  if (D == 128)
+    return launch_ex(merge_kernel<128>, grid, dim3(32), 0, stream, 1, ws_o, ws_ml, n_splits,
+                     (int64_t)tokens, H, out, lse);
+  return launch_ex(merge_kernel<64>, grid, dim3(32), 0, stream, 1, ws_o, ws_ml, n_splits,
+                   (int64_t)tokens, H, out, lse);
+}
+}  // namespace
+
 cudaError_t launch_attend(const AttendArgs& a, int64_t max_keys, void* ws, uint32_t* status,
                           cudaStream_t stream) {
+  const int tokens = a.B * a.Nq;
+  if (tokens == 0) return cudaSuccess;
+  if (a.d != 128 && a.d != 64) return cudaErrorInvalidValue;
+  const SplitPlan sp = plan_splits(tokens, a.H, max_keys, a.d);
+  float* ws_o = reinterpret_cast<float*>(ws);
+  float* ws_ml = ws_o + (size_t)sp.n_splits * tokens * a.H * a.d;
+  if (a.d == 128) {
+    // tcgen05 kernel
+    int cluster = sp.cluster;
+    cudaError_t e = launch_attend_tc(a, sp.n_splits, cluster, ws_o, ws_ml, status, stream);
+    if (e == cudaErrorNotSupported && cluster) {
+      cluster = 0;
+      e = launch_attend_tc(a, sp.n_splits, 0, ws_o, ws_ml, status, stream);
+    }
+    if (e != cudaSuccess || sp.n_splits == 1 || cluster) return e;
+    return launch_merge(a.d, ws_o, ws_ml, sp.n_splits, tokens, a.H, a.out, a.lse, stream);
+  }
   AttnParams prm;
   prm.q = a.q;
   prm.k_cmp = a.k_cmp;
@@ -493,24 +529,19 @@ cudaError_t launch_attend(const AttendArgs& a, int64_t max_keys, void* ws, uint3
   prm.W = a.W;
   prm.Nq = a.Nq;
   prm.H = a.H;
-  prm.tokens = a.B * a.Nq;
+  prm.tokens = tokens;
   prm.sparse = a.topk_idx != nullptr;
   prm.status = status;
-  const SplitPlan sp = plan_splits(prm.tokens, a.H, max_keys);
   prm.n_splits = sp.n_splits;
   prm.cluster_merge = sp.cluster;
-  prm.ws_o = reinterpret_cast<float*>(ws);
-  prm.ws_ml = prm.ws_o + (size_t)prm.n_splits * prm.tokens * a.H * a.d;
-  if (prm.tokens == 0) return cudaSuccess;
+  prm.ws_o = ws_o;
+  prm.ws_ml = ws_ml;
   const int groups = (a.H + 63) / 64;
   const int nw = a.H >= 64 ? 4 : (a.H + 15) / 16 >= 3 ? 4 : (a.H + 15) / 16;
-  if (a.d != 128 && a.d != 64) return cudaErrorInvalidValue;
-  cudaError_t e = a.d == 128 ? launch_d<128>(prm, groups, nw, stream)
-                             : launch_d<64>(prm, groups, nw, stream);
+  cudaError_t e = launch_d<64>(prm, groups, nw, stream);
   if (e == cudaErrorNotSupported && prm.cluster_merge) {
     prm.cluster_merge = 0;
-    e = a.d == 128 ? launch_d<128>(prm, groups, nw, stream)
-                   : launch_d<64>(prm, groups, nw, stream);
+    e = launch_d<64>(prm, groups, nw, stream);
   }
   return e;
 }

@@ -1,0 +1,657 @@
+// CSA sparse attention and HCA dense attention on the 5th-generation tensor cores (tcgen05), for
+// head dim 128.
+//
+// Lighthouse "deep deepseek v4 release" 八.3: CSA attends to the top-k selected compressed
+// entries plus a sliding-window branch of n_win raw tokens; HCA attends densely to every
+// compressed entry plus the same window. One softmax spans a query's entries and window tokens;
+// logits are q.k (the 1/sqrt(d) is folded into q).
+//
+// MQA: the H query heads of a token share one K/V head, so one CTA owns one query token and 64
+// heads, which form the M = 64 side of both contractions:
+//   S[64 heads, 128 keys]  = Q[64, 128 d] . K_chunk^T        (A = Q, B = K rows; both K-major)
+//   O[64 heads, 128 d]    += P[64, 128 keys] . V_chunk        (A = P, B = V rows read MN-major)
+// S and O live in tensor memory (S double-buffered: 2 x 128 columns; O: 128 columns). With M = 64
+// the accumulator rows 16w..16w+15 sit in lanes 32w..32w+15, so softmax warp w reads its 16 rows
+// with the 16x256b load, which hands every thread two rows in the m16n8 fragment layout.
+//
+// Warp roles (224 threads, one CTA per SM):
+//   warps 0-3  softmax: read S, mask, online softmax, write P (bf16) to shared memory, rescale O
+//              in tensor memory when the running maximum has risen by more than 2^8 (the
+//              reference maximum of a row only moves then, so P stays below 2^8 and the
+//              normalisation at the end uses the same reference), final normalisation and store;
+//   warps 4-7  loaders: gather the key rows of each 128-key chunk (selected entries or window
+//              tokens) with 16-byte cp.async into 128-byte-swizzled K and V tiles, two 256-byte
+//              rows per warp instruction, and write a validity byte per key (missing keys and
+//              out-of-range indices are zero-filled and masked); each loader thread arrives on
+//              the stage's barrier twice: at once (releasing the mask bytes) and when its
+//              copies land (cp.async.mbarrier.arrive);
+//   warp 6     tensor-memory allocation and the MMAs (one elected lane of the converged warp),
+//              issued as soon as they are ready: QK^T of chunk c+1 overlaps the softmax of
+//              chunk c, and PV of chunk c never waits for the loads of chunk c+1.
+// Three K/V stages (64 KB each) and one P buffer; every mbarrier wait is bounded.
+//
+// Decode splits a token's key chunks over several CTAs: the splits of a token form a cluster and
+// merge their (max, sum, unnormalised O) through distributed shared memory, or (more than 16
+// splits) through the workspace and a separate merge kernel, as in the mma.sync kernel.
+#include "common.cuh"
+#include "kernels.h"
+#include "prof.h"
+
+namespace csa {
+namespace {
+
+constexpr int kD = 128;            // head dim
+constexpr int kM = 64;             // heads per CTA (MMA M)
+constexpr int kKC = 128;           // keys per chunk (N of QK^T, K of PV)
+constexpr int kHalf = kKC / 2;     // keys per softmax warp (and per O accumulator)
+constexpr int kStages = 3;         // K/V stages
+constexpr int kSoftmaxWarps = 8;   // warps 0-7: lane quarter w % 4, key half w / 4
+constexpr int kLoadWarp0 = 8;      // warps 8-11
+constexpr int kLoadWarps = 4;
+constexpr int kLoadThreads = 32 * kLoadWarps;
+constexpr int kMmaWarp = 12;
+constexpr int kThreads = 416;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kOCol = 256;    // O accumulators: key half 0 at [256, 384), half 1 at [384, 512)
+constexpr int kQBytes = kM * kD * 2;        // 16 KB
+constexpr int kTileBytes = kKC * kD * 2;    // 32 KB (one K or V tile)
+constexpr int kPBytes = kM * kKC * 2;       // 16 KB
+constexpr int kMaxClusterSplits = 16;
+constexpr int kPStride = kD + 4;            // padded row of a parked partial output (floats)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr int kNumBars = 16;
+constexpr size_t kSmemBytes = 1024 + kQBytes + (size_t)kStages * 2 * kTileBytes + kPBytes +
+                              kNumBars * 8 + 16 + kStages * 4 * 4 + 2 * kM * 2 * 4;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+struct TcParams {
+  const uint16_t* q;
+  const uint16_t* k_cmp;
+  const uint16_t* v_cmp;
+  const int32_t* topk_idx;
+  const int32_t* topk_cnt;
+  const uint16_t* k_raw;
+  const uint16_t* v_raw;
+  uint16_t* out;
+  float* lse;
+  float* ws_o;   // [n_splits, tokens, H, D] unnormalised partial outputs (workspace merge)
+  float* ws_ml;  // [n_splits, tokens, H, 2] reference maximum and sum
+  int64_t E, N, q_pos0;
+  int k, m, W, Nq, H, n_splits, tokens;
+  int sparse;
+  int cluster_merge;
+  uint32_t* status;
+};
+
+// Byte offset of 16-byte chunk c (0..15) of row r in a 128-byte-swizzled K-major tile of R rows
+// and 128 bf16 columns: two 64-column atoms of R x 128 B, chunk index XOR (row mod 8).
+CSA_DEV uint32_t sw128(int r, int c, int R) {
+  return (uint32_t)((c >> 3) * R * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+CSA_DEV long long shfl_i64(long long v, int src) {
+  const int lo = __shfl_sync(0xffffffffu, (int)(v & 0xffffffffLL), src);
+  const int hi = __shfl_sync(0xffffffffu, (int)(v >> 32), src);
+  return ((long long)hi << 32) | (unsigned int)lo;
+}
+
+CSA_DEV float f32(uint32_t u) { return __uint_as_float(u); }
+CSA_DEV uint32_t u32(float f) { return __float_as_uint(f); }
+
+__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* Qs = base;                                  // [2 atoms][64 rows][128 B]
+  uint8_t* KV = Qs + kQBytes;                          // stage s: K tile, then V tile
+  uint8_t* Ps = KV + kStages * 2 * kTileBytes;         // [2 atoms][64 rows][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(Ps + kPBytes);
+  uint64_t* kv_full = bars;        // [3] loaders' mask words + copies of a stage (2 x 128)
+  uint64_t* kv_empty = bars + 3;   // [3] the PV reading the stage finished (commit)
+  uint64_t* s_full = bars + 6;     // [2] QK^T into S buffer finished (commit)
+  uint64_t* s_free = bars + 8;     // [2] softmax warps have read the S buffer (8 arrivals)
+  uint64_t* p_full = bars + 10;    // P written and O rescaled (8 arrivals)
+  uint64_t* pv_done = bars + 11;   // PV finished (commit); P may be rewritten, O read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  uint32_t* kmask = tmem_slot + 4;                     // [3][4] validity bits of the 128 keys
+  float* xml = reinterpret_cast<float*>(kmask + kStages * 4);  // [2 halves][64 rows][2]
+
+  pdl_trigger();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int split = p.cluster_merge ? (int)cluster_ctarank() : (int)blockIdx.x;
+  const int64_t tok = blockIdx.y;
+  const int h_base = blockIdx.z * kM;
+  const int64_t b = tok / p.Nq;
+  const int64_t t = p.q_pos0 + tok % p.Nq;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 2 * kLoadThreads);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], kSoftmaxWarps);
+    }
+    mbar_init(p_full, kSoftmaxWarps);
+    mbar_init(pv_done, 1);
+    fence_mbar_init();
+  }
+  // Q tile of heads [h_base, h_base + 64) (zero rows past H); Q is an input of this call.
+  for (int x = threadIdx.x; x < kM * 16; x += kThreads) {
+    const int r = x >> 4, c = x & 15;
+    const bool ok = h_base + r < p.H;
+    cp_async_16(Qs + sw128(r, c, kM), ok ? p.q + (tok * p.H + h_base + r) * kD + c * 8 : p.q,
+                ok ? 16u : 0u);
+  }
+  cp_async_commit();
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  cp_async_wait<0>();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // top-k lists and entries come from the preceding kernels
+
+  int64_t n_sel;
+  if (p.sparse) {
+    n_sel = p.topk_cnt[tok];
+    if (n_sel < 0 || n_sel > p.k) {
+      if (threadIdx.x == 0) atomicOr(p.status, kFlagBadIndex);
+      n_sel = n_sel < 0 ? 0 : p.k;
+    }
+  } else {
+    n_sel = max((int64_t)0, min(p.E, (t + 1) / p.m));
+  }
+  const int64_t w0 = max((int64_t)0, t - p.W + 1);
+  const int64_t n_keys = n_sel + (p.W > 0 ? (t - w0 + 1) : 0);
+  const int64_t n_chunks = (n_keys + kKC - 1) / kKC;
+  const int c_begin = (int)(n_chunks * split / p.n_splits);
+  const int c_end = (int)(n_chunks * (split + 1) / p.n_splits);
+  // After a wait has timed out anywhere on the device, later CTAs skip their work instead of
+  // timing out one after another.
+  const bool dead = (*reinterpret_cast<volatile uint32_t*>(p.status) & kFlagTimeout) != 0;
+  const int nloc = dead ? 0 : c_end - c_begin;
+
+  // softmax-warp state: lane quarter q (rows 16q .. 16q + 15), key half hf; each thread holds
+  // rows r0 = 16q + g and r0 + 8
+  const int g = lane >> 2, tq = lane & 3;
+  const int q = warp & 3, hf = (warp >> 2) & 1;
+  const int r0 = q * 16 + g;
+  const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+  const uint32_t o_half = tmem + lane_base + kOCol + (uint32_t)(hf * kD);  // this half's O
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  bool sm_ok = true;
+
+  if (warp >= kLoadWarp0 && warp < kMmaWarp) {
+    // ------------------------------- loaders -------------------------------
+    // Warp wl copies rows [32 wl, 32 wl + 32) of each chunk, two rows per instruction: lanes
+    // 0-15 and 16-31 each copy the 16 chunks of one 256-byte row (coalesced).
+    const int wl = warp - kLoadWarp0;
+    const int h = lane >> 4, cc = lane & 15;
+    constexpr long long kRawBit = 1LL << 62;
+    for (int it = 0; it < nloc; ++it) {
+      const int s = it % kStages;
+      if (it >= kStages &&
+          !mbar_wait_warp(&kv_empty[s], (uint32_t)(it / kStages - 1) & 1u, p.status))
+        break;
+      // source row of row 32 wl + lane (element offset; bit 62 = raw window token, -1 = none)
+      const int i = wl * 32 + lane;
+      const int64_t key = (int64_t)(c_begin + it) * kKC + i;
+      long long cd = -1;
+      if (key < n_keys) {
+        if (key < n_sel) {
+          const int64_t j = p.sparse ? (int64_t)p.topk_idx[tok * p.k + key] : key;
+          if (j < 0 || j >= p.E)
+            atomicOr(p.status, kFlagBadIndex);  // flagged; the row is zero-filled and masked
+          else
+            cd = (b * p.E + j) * kD;
+        } else {
+          cd = ((b * p.N + w0 + (key - n_sel)) * kD) | kRawBit;
+        }
+      }
+      const uint32_t vbits = __ballot_sync(0xffffffffu, cd >= 0);
+      if (lane == 0) kmask[s * 4 + wl] = vbits;
+      uint8_t* kd = KV + s * 2 * kTileBytes;
+      uint8_t* vd = kd + kTileBytes;
+#pragma unroll
+      for (int st = 0; st < 16; ++st) {
+        const int r = 2 * st + h;  // row within this warp's 32
+        const long long c2 = shfl_i64(cd, r);
+        const uint32_t off = sw128(wl * 32 + r, cc, kKC);
+        const bool valid = c2 >= 0;
+        const int64_t e = c2 & (kRawBit - 1);
+        const bool raw = (c2 & kRawBit) != 0;
+        const uint16_t* ks = valid ? (raw ? p.k_raw : p.k_cmp) + e + cc * 8 : p.k_raw;
+        const uint16_t* vs = valid ? (raw ? p.v_raw : p.v_cmp) + e + cc * 8 : p.v_raw;
+        cp_async_16(kd + off, ks, valid ? 16u : 0u);
+        cp_async_16(vd + off, vs, valid ? 16u : 0u);
+      }
+      mbar_arrive(&kv_full[s]);                 // releases the mask word
+      cp_async_mbar_arrive_noinc(&kv_full[s]);  // arrives when the copies have landed
+    }
+    cp_async_wait<0>();  // never leave with copies in flight
+  } else if (warp == kMmaWarp) {
+    // ------------------------------- MMA issuer -------------------------------
+    // Issues whichever MMA is ready (PV of the oldest chunk with its P written, QK^T of the next
+    // chunk with its K/V landed and an S buffer free), so neither waits behind the other.
+    const uint32_t id_qk = idesc_bf16(kM, kKC, false, false);
+    const uint32_t id_pv = idesc_bf16(kM, kD, false, true);
+    int nq = 0, np = 0;
+    long long idle0 = clock64();
+    while (np < nloc) {
+      bool did = false;
+      if (np < nq) {
+        int ready = lane == 0 ? (int)mbar_test(p_full, (uint32_t)np & 1u) : 0;
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (ready) {
+          tc_fence_after();
+          const int s = np % kStages;
+          if (elect_one()) {
+            const uint32_t pt = smem_addr(Ps);
+            const uint32_t vt = smem_addr(KV + s * 2 * kTileBytes + kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kKC / 16; ++kk) {
+              const uint32_t atom = kk >> 2, kin = (kk & 3) * 32;
+              const uint64_t ad = smem_desc(pt + atom * kM * 128 + kin, 16, 1024, kSwizzle128B);
+              // V rows are keys (the K dimension) with d contiguous: MN-major B, 64-column
+              // atoms kKC * 128 bytes apart, 8-key groups 1024 bytes apart.
+              const uint64_t bd = smem_desc(vt + kk * 16 * 128, kKC * 128, 1024, kSwizzle128B);
+              // keys 0-63 accumulate into O half 0, keys 64-127 into O half 1
+              umma_bf16(tmem + kOCol + atom * kD, ad, bd, id_pv,
+                        (np > 0 || (kk & 3) > 0) ? 1u : 0u);
+            }
+            umma_commit(&kv_empty[s]);
+            umma_commit(pv_done);
+          }
+          __syncwarp();
+          ++np;
+          did = true;
+        }
+      }
+      if (nq < nloc) {
+        const int s = nq % kStages, sb = nq & 1;
+        int ready = 0;
+        if (lane == 0)
+          ready = mbar_test(&kv_full[s], (uint32_t)(nq / kStages) & 1u) &&
+                  (nq < 2 || mbar_test(&s_free[sb], (uint32_t)((nq >> 1) - 1) & 1u));
+        ready = __shfl_sync(0xffffffffu, ready, 0);
+        if (ready) {
+          fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
+          tc_fence_after();
+          if (elect_one()) {
+            const uint32_t kt = smem_addr(KV + s * 2 * kTileBytes);
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t atom = kk >> 2, kin = (kk & 3) * 32;
+              const uint64_t ad = smem_desc(smem_addr(Qs) + atom * kM * 128 + kin, 16, 1024,
+                                            kSwizzle128B);
+              const uint64_t bd = smem_desc(kt + atom * kKC * 128 + kin, 16, 1024, kSwizzle128B);
+              umma_bf16(tmem + (uint32_t)(sb * kKC), ad, bd, id_qk, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(&s_full[sb]);
+          }
+          __syncwarp();
+          ++nq;
+          did = true;
+        }
+      }
+      if (did) {
+        idle0 = clock64();
+      } else if (clock64() - idle0 > kWaitBudgetCycles) {
+        if (lane == 0) atomicOr(p.status, kFlagTimeout);
+        break;
+      }
+    }
+  } else {
+    // ------------------------------- softmax -------------------------------
+    // Keys [64 hf, 64 hf + 64) of every chunk, with their own running maximum and sum; the two
+    // key halves accumulate into separate O accumulators that are combined at the end.
+    for (int it = 0; it < nloc; ++it) {
+      const int sb = it & 1, s = it % kStages;
+      if (!mbar_wait_warp(&s_full[sb], (uint32_t)(it >> 1) & 1u, p.status)) {
+        sm_ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t r[32];  // r[4i + e]: row r0, key 8i + 2tq + e of the half; r[4i + 2 + e]: row r0 + 8
+      tmem_ld_16x256b_x8(tmem + lane_base + (uint32_t)(sb * kKC + hf * kHalf), r);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[sb]);
+      // the stage's mask words (the phase completed before S did; acquire the loaders' stores)
+      if (!mbar_wait_warp(&kv_full[s], (uint32_t)(it / kStages) & 1u, p.status)) {
+        sm_ok = false;
+        break;
+      }
+      const uint32_t mlo = kmask[s * 4 + 2 * hf], mhi = kmask[s * 4 + 2 * hf + 1];
+      if ((mlo & mhi) != 0xffffffffu) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const uint32_t bit = (((i < 4) ? mlo : mhi) >> ((8 * i + 2 * tq + e) & 31)) & 1u;
+            if (!bit) {
+              r[4 * i + e] = u32(-INFINITY);
+              r[4 * i + 2 + e] = u32(-INFINITY);
+            }
+          }
+        }
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        mx0 = fmaxf(mx0, fmaxf(f32(r[4 * i]), f32(r[4 * i + 1])));
+        mx1 = fmaxf(mx1, fmaxf(f32(r[4 * i + 2]), f32(r[4 * i + 3])));
+      }
+#pragma unroll
+      for (int x = 1; x < 4; x <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+      }
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      // true also when the old reference is -inf and the new one finite; false if both are -inf
+      const bool need0 = (mn0 - m0) * kLog2e > kRescaleLog2;
+      const bool need1 = (mn1 - m1) * kLog2e > kRescaleLog2;
+      const bool rescale = __any_sync(0xffffffffu, need0 || need1);
+      float c0 = 1.f, c1 = 1.f;
+      if (rescale) {
+        c0 = need0 ? exp2f((m0 - mn0) * kLog2e) : 1.f;
+        c1 = need1 ? exp2f((m1 - mn1) * kLog2e) : 1.f;
+        l0 *= c0;
+        l1 *= c1;
+        if (need0) m0 = mn0;
+        if (need1) m1 = mn1;
+      }
+      const float nb0 = m0 == -INFINITY ? 0.f : -m0 * kLog2e;
+      const float nb1 = m1 == -INFINITY ? 0.f : -m1 * kLog2e;
+      uint32_t pk[16];
+      float rs0 = 0.f, rs1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float p00 = exp2f(fmaf(f32(r[4 * i + 0]), kLog2e, nb0));
+        const float p01 = exp2f(fmaf(f32(r[4 * i + 1]), kLog2e, nb0));
+        const float p10 = exp2f(fmaf(f32(r[4 * i + 2]), kLog2e, nb1));
+        const float p11 = exp2f(fmaf(f32(r[4 * i + 3]), kLog2e, nb1));
+        rs0 += p00 + p01;
+        rs1 += p10 + p11;
+        pk[2 * i] = pack_bf16x2(p00, p01);
+        pk[2 * i + 1] = pack_bf16x2(p10, p11);
+      }
+      l0 += rs0;
+      l1 += rs1;
+      if (it > 0) {
+        // PV(it - 1) finished: P may be rewritten and O holds every PV so far
+        if (!mbar_wait_warp(pv_done, (uint32_t)(it - 1) & 1u, p.status)) {
+          sm_ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (rescale) {
+#pragma unroll
+          for (int part = 0; part < 4; ++part) {
+            uint32_t ov[16];
+            const uint32_t oa = o_half + (uint32_t)(part * 32);
+            tmem_ld_16x256b_x4(oa, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              ov[4 * i + 0] = u32(f32(ov[4 * i + 0]) * c0);
+              ov[4 * i + 1] = u32(f32(ov[4 * i + 1]) * c0);
+              ov[4 * i + 2] = u32(f32(ov[4 * i + 2]) * c1);
+              ov[4 * i + 3] = u32(f32(ov[4 * i + 3]) * c1);
+            }
+            tmem_st_16x256b_x4(oa, ov);
+          }
+          tmem_st_wait();
+        }
+      }
+      // rows r0 / r0 + 8, keys 64 hf + 8i + 2tq, +1: atom hf, 16-byte chunk i, word tq
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t w = (uint32_t)(tq * 4);
+        *reinterpret_cast<uint32_t*>(Ps + sw128(r0, 8 * hf + i, kM) + w) = pk[2 * i];
+        *reinterpret_cast<uint32_t*>(Ps + sw128(r0 + 8, 8 * hf + i, kM) + w) = pk[2 * i + 1];
+      }
+      fence_proxy_async_smem();  // P (generic stores) -> tensor-core reads
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (sm_ok && nloc > 0)
+      sm_ok = mbar_wait_warp(pv_done, (uint32_t)(nloc - 1) & 1u, p.status);
+#pragma unroll
+    for (int x = 1; x < 4; x <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, x);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, x);
+    }
+    if (tq == 0) {  // this half's (max, sum) of both rows, for the other half
+      xml[(hf * kM + r0) * 2 + 0] = m0;
+      xml[(hf * kM + r0) * 2 + 1] = l0;
+      xml[(hf * kM + r0 + 8) * 2 + 0] = m1;
+      xml[(hf * kM + r0 + 8) * 2 + 1] = l1;
+    }
+  }
+
+  __syncthreads();
+  // Combine the two key halves: warp (q, hf) produces output columns [64 hf, 64 hf + 64) of rows
+  // r0 and r0 + 8 from both O accumulators, weighted to the common maximum.
+  const bool smx = warp < kSoftmaxWarps;
+  uint32_t o[32];
+  float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
+  if (smx) {
+    const float ma0 = xml[(0 * kM + r0) * 2], la0 = xml[(0 * kM + r0) * 2 + 1];
+    const float mb0 = xml[(1 * kM + r0) * 2], lb0 = xml[(1 * kM + r0) * 2 + 1];
+    const float ma1 = xml[(0 * kM + r0 + 8) * 2], la1 = xml[(0 * kM + r0 + 8) * 2 + 1];
+    const float mb1 = xml[(1 * kM + r0 + 8) * 2], lb1 = xml[(1 * kM + r0 + 8) * 2 + 1];
+    M0 = fmaxf(ma0, mb0);
+    M1 = fmaxf(ma1, mb1);
+    const float wa0 = ma0 == -INFINITY ? 0.f : exp2f((ma0 - M0) * kLog2e);
+    const float wb0 = mb0 == -INFINITY ? 0.f : exp2f((mb0 - M0) * kLog2e);
+    const float wa1 = ma1 == -INFINITY ? 0.f : exp2f((ma1 - M1) * kLog2e);
+    const float wb1 = mb1 == -INFINITY ? 0.f : exp2f((mb1 - M1) * kLog2e);
+    L0 = wa0 * la0 + wb0 * lb0;
+    L1 = wa1 * la1 + wb1 * lb1;
+#pragma unroll
+    for (int x = 0; x < 32; ++x) o[x] = 0u;
+    if (sm_ok && nloc > 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t oa[16], ob[16];
+        const uint32_t col = tmem + lane_base + kOCol + (uint32_t)(hf * 64 + part * 32);
+        tmem_ld_16x256b_x4(col, oa);       // key half 0, output columns 64 hf + 32 part ..
+        tmem_ld_16x256b_x4(col + kD, ob);  // key half 1
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int x = 16 * part + 4 * i;
+          o[x + 0] = u32(wa0 * f32(oa[4 * i + 0]) + wb0 * f32(ob[4 * i + 0]));
+          o[x + 1] = u32(wa0 * f32(oa[4 * i + 1]) + wb0 * f32(ob[4 * i + 1]));
+          o[x + 2] = u32(wa1 * f32(oa[4 * i + 2]) + wb1 * f32(ob[4 * i + 2]));
+          o[x + 3] = u32(wa1 * f32(oa[4 * i + 3]) + wb1 * f32(ob[4 * i + 3]));
+        }
+      }
+    }
+  }
+  // Every role is done with tensor memory and the pipeline buffers.
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+
+  const int h0 = h_base + r0, h1 = h0 + 8;
+  const int dc = hf * 64;  // this warp's output columns
+  if (p.n_splits == 1) {
+    if (smx) {
+      const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f, inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int d0 = dc + 8 * i + 2 * tq;
+        if (h0 < p.H)
+          *reinterpret_cast<uint32_t*>(p.out + (tok * p.H + h0) * kD + d0) =
+              pack_bf16x2(f32(o[4 * i]) * inv0, f32(o[4 * i + 1]) * inv0);
+        if (h1 < p.H)
+          *reinterpret_cast<uint32_t*>(p.out + (tok * p.H + h1) * kD + d0) =
+              pack_bf16x2(f32(o[4 * i + 2]) * inv1, f32(o[4 * i + 3]) * inv1);
+      }
+      if (p.lse != nullptr && tq == 0 && hf == 0) {
+        if (h0 < p.H) p.lse[tok * p.H + h0] = L0 > 0.f ? M0 + logf(L0) : -INFINITY;
+        if (h1 < p.H) p.lse[tok * p.H + h1] = L1 > 0.f ? M1 + logf(L1) : -INFINITY;
+      }
+    }
+    return;
+  }
+  if (!p.cluster_merge) {
+    if (smx) {
+      const int64_t sbase = ((int64_t)split * p.tokens + tok) * p.H;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int d0 = dc + 8 * i + 2 * tq;
+        if (h0 < p.H)
+          *reinterpret_cast<float2*>(p.ws_o + (sbase + h0) * kD + d0) =
+              make_float2(f32(o[4 * i]), f32(o[4 * i + 1]));
+        if (h1 < p.H)
+          *reinterpret_cast<float2*>(p.ws_o + (sbase + h1) * kD + d0) =
+              make_float2(f32(o[4 * i + 2]), f32(o[4 * i + 3]));
+      }
+      if (tq == 0 && hf == 0) {
+        if (h0 < p.H) *reinterpret_cast<float2*>(p.ws_ml + (sbase + h0) * 2) = make_float2(M0, L0);
+        if (h1 < p.H) *reinterpret_cast<float2*>(p.ws_ml + (sbase + h1) * 2) = make_float2(M1, L1);
+      }
+    }
+    return;
+  }
+  // Cluster merge: park this split's partials in shared memory (the stage buffers are free).
+  float* po = reinterpret_cast<float*>(KV);  // [64][kPStride]
+  float* pml = po + kM * kPStride;           // [64][2]
+  if (smx) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int d0 = dc + 8 * i + 2 * tq;
+      *reinterpret_cast<float2*>(po + r0 * kPStride + d0) =
+          make_float2(f32(o[4 * i]), f32(o[4 * i + 1]));
+      *reinterpret_cast<float2*>(po + (r0 + 8) * kPStride + d0) =
+          make_float2(f32(o[4 * i + 2]), f32(o[4 * i + 3]));
+    }
+    if (tq == 0 && hf == 0) {
+      *reinterpret_cast<float2*>(pml + r0 * 2) = make_float2(M0, L0);
+      *reinterpret_cast<float2*>(pml + (r0 + 8) * 2) = make_float2(M1, L1);
+    }
+  }
+  __syncthreads();
+  cluster_sync();
+  const int S = p.n_splits;
+  const int rows_per = (kM + S - 1) / S;
+  const int rb = split * rows_per, re = min(kM, rb + rows_per);
+  constexpr int C4 = kD / 4;
+  for (int x = threadIdx.x; x < (re - rb) * C4; x += kThreads) {
+    const int row = rb + x / C4, c4 = x % C4;
+    const int h = h_base + row;
+    if (h >= p.H) continue;
+    float2 ml[kMaxClusterSplits];
+#pragma unroll
+    for (int sp = 0; sp < kMaxClusterSplits; ++sp)
+      ml[sp] = sp < S ? dsmem_ld_f32x2(pml + row * 2, sp) : make_float2(-INFINITY, 0.f);
+    float Mx = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < kMaxClusterSplits; ++sp) Mx = fmaxf(Mx, ml[sp].x);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float Lx = 0.f;
+    if (Mx != -INFINITY) {
+#pragma unroll
+      for (int sp = 0; sp < kMaxClusterSplits; ++sp) {
+        if (sp >= S || ml[sp].x == -INFINITY) continue;
+        const float4 v = dsmem_ld_f32x4(po + row * kPStride + c4 * 4, sp);
+        const float w = expf(ml[sp].x - Mx);
+        Lx += w * ml[sp].y;
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+    }
+    const float inv = Lx > 0.f ? 1.f / Lx : 0.f;
+    uint2 pk2;
+    pk2.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    pk2.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(p.out + (tok * p.H + h) * kD + c4 * 4) = pk2;
+    if (p.lse != nullptr && c4 == 0) p.lse[tok * p.H + h] = Lx > 0.f ? Mx + logf(Lx) : -INFINITY;
+  }
+  cluster_sync();  // no CTA leaves while another may still read its shared memory
+}
+
+}  // namespace
+
+int attend_tc_chunk_keys() { return kKC; }
+
+cudaError_t launch_attend_tc(const AttendArgs& a, int n_splits, int cluster, float* ws_o,
+                             float* ws_ml, uint32_t* status, cudaStream_t stream) {
+  TcParams prm;
+  prm.q = a.q;
+  prm.k_cmp = a.k_cmp;
+  prm.v_cmp = a.v_cmp;
+  prm.topk_idx = a.topk_idx;
+  prm.topk_cnt = a.topk_cnt;
+  prm.k_raw = a.k_raw;
+  prm.v_raw = a.v_raw;
+  prm.out = a.out;
+  prm.lse = a.lse;
+  prm.ws_o = ws_o;
+  prm.ws_ml = ws_ml;
+  prm.E = a.E;
+  prm.N = a.N;
+  prm.q_pos0 = a.q_pos0;
+  prm.k = a.k;
+  prm.m = a.m;
+  prm.W = a.W;
+  prm.Nq = a.Nq;
+  prm.H = a.H;
+  prm.n_splits = n_splits;
+  prm.tokens = a.B * a.Nq;
+  prm.sparse = a.topk_idx != nullptr;
+  prm.cluster_merge = cluster;
+  prm.status = status;
+  auto kern = attend_tc_kernel;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  if (cluster && n_splits > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  const int groups = (a.H + kM - 1) / kM;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_splits, (unsigned)prm.tokens, (unsigned)groups);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster ? (unsigned)n_splits : 1u;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cluster && n_splits > 8) {
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess || nclusters == 0) {
+      (void)cudaGetLastError();
+      return cudaErrorNotSupported;  // caller falls back to the workspace merge
+    }
+  }
+  ProfScope prof(stream, prm.sparse ? "csa_attend" : "hca_attend");
+  return cudaLaunchKernelEx(&cfg, kern, prm);
+}
+
+}  // namespace csa

@@ -83,9 +83,16 @@ struct AttendArgs {
   int64_t E, N, q_pos0;
   int k, m, W, B, Nq, H, d;
 };
-int plan_attend_splits(int tokens, int H, int64_t max_keys);
+int plan_attend_splits(int tokens, int H, int d, int64_t max_keys);
 size_t attend_workspace_bytes(int tokens, int H, int d, int64_t max_keys);
+// d = 128 runs the tcgen05 kernel (attend_tc.cu), d = 64 the mma.sync kernel (attend.cu).
 cudaError_t launch_attend(const AttendArgs& a, int64_t max_keys, void* ws, uint32_t* status,
                           cudaStream_t stream);
+int attend_tc_chunk_keys();
+// n_splits CTAs per (token, 64-head group); cluster = 1 merges the splits through distributed
+// shared memory (returns cudaErrorNotSupported if such a cluster cannot be scheduled), else the
+// splits write ws_o / ws_ml for the merge kernel.
+cudaError_t launch_attend_tc(const AttendArgs& a, int n_splits, int cluster, float* ws_o,
+                             float* ws_ml, uint32_t* status, cudaStream_t stream);
 
 }  // namespace csa

@@ -7,8 +7,8 @@ import torch
 import long_context_compressed_pooling_b300 as csa
 import oracle as O
 from synth import LayerShape, generate_layer
-from _helpers import (assert_attention_close, assert_entries_close, assert_lse_close, bits, f64,
-                      npy)
+from _helpers import (ATT_MAX_ABS, ATT_REL_L2, assert_attention_close, assert_entries_close,
+                      assert_lse_close, bits, f64, npy)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -23,9 +23,10 @@ def _clean_status():
         assert csa.device_status(reset=True) == 0
 
 
-def _shape(kind, B, N, Nq, q_pos0, H, d, m, W, k=0, H_I=0, d_I=0):
+def _shape(kind, B, N, Nq, q_pos0, H, d, m, W, k=0, H_I=0, d_I=0, q_scale=None):
     return LayerShape(kind, B=B, N=N, Nq=Nq, q_pos0=q_pos0, H=H, d=d, m=m, W=W, k=k, H_I=H_I,
-                      d_I=d_I, q_scale=1.0 / np.sqrt(d), compress_begin=0)
+                      d_I=d_I, q_scale=1.0 / np.sqrt(d) if q_scale is None else q_scale,
+                      compress_begin=0)
 
 
 # ---------------------------------------------------------------------------------------------
@@ -180,7 +181,9 @@ HCA_CASES = [
     (3, 1, 8191, 8192, 64, 128, 128, 128),   # decode, split-K over 64 entries + window
     (1, 50, 0, 300, 8, 64, 128, 64),         # config-1 shape: no entry visible for t < 127
     (1, 4, 996, 1000, 64, 64, 4, 0),         # no window at all
-    (2, 1, 131071, 131072, 64, 128, 128, 128),  # 18 splits per token: workspace merge
+    (2, 1, 131071, 131072, 64, 128, 128, 128),  # 9 splits per token: cluster merge
+    (1, 1, 262143, 262144, 64, 128, 128, 128),  # 17 splits: workspace merge
+    (1, 160, 3840, 4000, 64, 128, 4, 128),   # dense prefill rows: ~9 key chunks per CTA
 ]
 
 
@@ -201,6 +204,35 @@ def test_hca_attend_matches_oracle(B, Nq, q_pos0, N, H, d, m, W):
         assert_lse_close(npy(lse[b]), ref["lse"], f"b={b}")
         ref2 = O.hca_layer_seq(qb[b], kr[b], vr[b], npy(x["logits"][b]), m=m, W=W, q_pos0=q_pos0)
         assert_attention_close(f64(out[b]), ref2["out"], f"layer b={b}")
+
+
+@pytest.mark.parametrize("B,Nq,q_pos0,N,m,W", [(1, 160, 3840, 4000, 4, 128),
+                                               (2, 1, 65535, 65536, 128, 128)])
+def test_hca_attend_large_logits(B, Nq, q_pos0, N, m, W):
+    # Unscaled queries: logits spread over tens of nats, so the running maximum keeps rising
+    # across key chunks and the partial outputs are rescaled many times. The softmax is then
+    # nearly one-hot and outputs reach |o| ~ 4-5, where one bf16 rounding of the output alone is
+    # up to 2^-6 (above the workloads' 1e-2 max-abs bar, which holds for their 1/sqrt(d)-scaled
+    # queries), so each element gets 1e-2 plus one bf16 rounding (2^-8 relative) of its value.
+    H, d = 64, 128
+    s = _shape("hca", B, N, Nq, q_pos0, H, d, m, W, q_scale=1.0)
+    x = generate_layer(s, seed=17 + N, device=DEV)
+    E = N // m
+    kc = torch.empty((B, E, d), dtype=torch.bfloat16, device=DEV)
+    vc = torch.empty_like(kc)
+    csa.compress(x["k_raw"], x["v_raw"], x["logits"], m, kc, vc)
+    out, lse = csa.hca_attend(x["q"], kc, vc, m, x["k_raw"], x["v_raw"], W, q_pos0, want_lse=True)
+    qb, kr, vr = bits(x["q"]), bits(x["k_raw"]), bits(x["v_raw"])
+    for b in range(B):
+        ref = O.hca_layer_seq(qb[b], kr[b], vr[b], npy(x["logits"][b]), m=m, W=W, q_pos0=q_pos0,
+                              k_cmp=f64(kc[b]), v_cmp=f64(vc[b]))
+        got = f64(out[b])
+        err = np.abs(got - ref["out"])
+        lim = ATT_MAX_ABS + np.abs(ref["out"]) * 2.0 ** -8
+        assert np.all(err <= lim), f"b={b}: worst excess {float(np.max(err - lim)):.3e}"
+        rel = np.linalg.norm(got - ref["out"]) / np.linalg.norm(ref["out"])
+        assert rel <= ATT_REL_L2, f"b={b}: rel_l2={rel:.3e}"
+        assert_lse_close(npy(lse[b]), ref["lse"], f"b={b}")
 
 
 def test_empty_key_set_gives_zero_and_neg_inf():
