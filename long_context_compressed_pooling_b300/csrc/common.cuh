@@ -254,6 +254,11 @@ CSA_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// 32 lanes x 1 column: thread i writes lane (quarter*32 + i).
+CSA_DEV void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
 // 32 lanes x 8 consecutive columns, all set to the same 32-bit value.
 CSA_DEV void tmem_st8_fill(uint32_t taddr, uint32_t v) {
   asm volatile(

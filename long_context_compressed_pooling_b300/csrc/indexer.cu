@@ -28,7 +28,7 @@
 // after the MMAs that read its codes have completed AND every epilogue warp has finished the
 // slot's last group (the epilogue reads the slot's scale tile). The MMA warp issues
 // groups of G tiles (one elected lane of a converged warp) into the next accumulator group of a
-// ring in tensor memory (3 x 4 x 16 columns for decode, 3 x 2 x 64 for prefill) and commits
+// ring in tensor memory (3 x 4 x 16 columns for decode, 2 x 1 x 224 for prefill) and commits
 // once per group; eight epilogue warps (two per tensor-memory lane quarter) drain a group
 // together, so the commit -> epilogue round trip is paid once per group. Decode (one query per
 // sequence) runs persistent CTAs over all (sequence, tile) pairs; prefill gives each CTA one
@@ -50,12 +50,14 @@ constexpr int kScaleTileBytes = kTileM * 2;  // one tile's UE8M0 scales (NB = 2)
 constexpr int kEW = 2;                      // epilogue warps per tensor-memory lane quarter
 constexpr int kThreads = 64 + 128 * kEW;    // copy warp, MMA warp, 8 epilogue warps
 constexpr int kWorkThreads = kThreads - 32; // every warp but the copy warp
-constexpr int kMaxCols = 64;
+constexpr int kMaxCols = 224;    // MMA N of a prefill CTA (14 queries x 16 columns)
 constexpr int kMaxG = 4;
 constexpr int kMaxAcc = 8;  // accumulator groups in tensor memory (a ring)
-constexpr int kSfCols = 16;  // tensor-memory columns filled with scale 1.0 for each of A and B
+// Scale-factor regions in tensor memory (kind::mxf4 scale_vec::2X), each starting on a 16-column
+// boundary. A: row i in lane i, column i / 32 (all 1.0: the entries' scales are applied in the
+// epilogue). B: column n of the MMA in lane 32 q + n % 32 of every lane quarter q, column n / 32.
+constexpr int kSfCols = 16;
 constexpr int kMaxSeqPerCta = 8;  // decode: query operands of up to 8 sequences stay resident
-constexpr int kBRows = 128;       // B-operand rows held in shared memory (decode 8 x 16, prefill 64)
 
 struct IdxParams {
   const uint8_t* qi_codes;   // [B, Nq, H_I, NB*16]
@@ -70,10 +72,13 @@ struct IdxParams {
   uint32_t* status;
 };
 
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + kRingTiles * kATileBytes +
-                              kRingTiles * kScaleTileBytes + kBRows * kRowBytes +
-                              kBRows * sizeof(float) + kMaxCols * sizeof(int64_t) +
-                              (2 * kSlots + 2 * kMaxAcc + 3) * 8 + 64;
+// Shared memory for a launch whose B operand has `brows` rows (decode: 8 sequences x ncols;
+// prefill: ncols), so that decode CTAs stay small enough for two per SM.
+constexpr size_t smem_bytes(int brows) {
+  return 1024 /*align slack*/ + kRingTiles * kATileBytes + kRingTiles * kScaleTileBytes +
+         (size_t)brows * kRowBytes + (size_t)brows * sizeof(float) + kMaxCols * sizeof(int64_t) +
+         (2 * kSlots + 2 * kMaxAcc + 3) * 8 + 64;
+}
 
 // Named barrier over every warp but the copy warp (the copy warp never waits on set-up).
 CSA_DEV void work_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kWorkThreads) : "memory"); }
@@ -89,10 +94,11 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* atiles = base;                                    // kRingTiles x 4096, 1024-aligned
-  uint8_t* btile = atiles + kRingTiles * kATileBytes;        // kBRows x 32, 1024-aligned
-  uint8_t* stiles = btile + kBRows * kRowBytes;              // bulk path: kRingTiles x 256 B
-  float* qscale = reinterpret_cast<float*>(stiles + kRingTiles * kScaleTileBytes);
-  int64_t* qvis = reinterpret_cast<int64_t*>(qscale + kBRows);  // visible entries per query
+  const int brows = (p.Nq == 1 ? kMaxSeqPerCta : 1) * p.ncols;
+  uint8_t* btile = atiles + kRingTiles * kATileBytes;        // brows x 32, 1024-aligned
+  uint8_t* stiles = btile + brows * kRowBytes;               // bulk path: kRingTiles x 256 B
+  uint32_t* qbyte = reinterpret_cast<uint32_t*>(stiles + kRingTiles * kScaleTileBytes);
+  int64_t* qvis = reinterpret_cast<int64_t*>(qbyte + brows);  // visible entries per query
   uint64_t* bars = reinterpret_cast<uint64_t*>(qvis + kMaxCols);
   uint64_t* full = bars;                 // [kSlots]
   uint64_t* empty = bars + kSlots;       // [kSlots]
@@ -246,11 +252,10 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   for (int rr = wt; rr < n_seq * p.ncols; rr += kWorkThreads) {
     const int sl = rr / p.ncols, r = rr % p.ncols;
     const int ql = r / CPQ, h = (r / (NB * SW)) % H_I, blk = r % NB;
-    float s = 0.f;
+    uint32_t e = 127u;  // scale 1.0 for the zero rows of absent queries
     if (ql < nq)
-      s = exp2_int((int)p.qi_scales[(((int64_t)(b_first + sl) * p.Nq + i0 + ql) * H_I + h) * NB +
-                                    blk] - 127);
-    qscale[rr] = s;
+      e = p.qi_scales[(((int64_t)(b_first + sl) * p.Nq + i0 + ql) * H_I + h) * NB + blk];
+    qbyte[rr] = e;
   }
   for (int ql = wt; ql < nq; ql += kWorkThreads)
     qvis[ql] = min(p.E, (p.q_pos0 + i0 + ql + 1) / p.m);
@@ -266,11 +271,24 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   const uint32_t tmem = *tmem_slot;
   const uint32_t acc_cols = (uint32_t)(G * p.ncols);  // one accumulator group
   const uint32_t sfa_col = (uint32_t)p.nacc * acc_cols, sfb_col = sfa_col + kSfCols;
+  // Prefill (one sequence per CTA): every B column carries its query block's UE8M0 scale, so the
+  // MMA yields scale x (exact partial sum of e2m1 products), still exact. Decode CTAs may hold
+  // several sequences behind one scale region: their B scales stay 1.0 and the query scales are
+  // applied in the epilogue.
+  const bool q_in_mma = p.Nq > 1;
   if (warp >= 2 && warp < 6) {
-    // scale factors = 1.0 everywhere in the two scale regions (all lanes of this quarter)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 #pragma unroll
-    for (int c = 0; c < 2 * kSfCols; c += 8) tmem_st8_fill(tmem + lane_base + sfa_col + c, 0x7F7F7F7Fu);
+    for (int c = 0; c < 2 * kSfCols; c += 8)
+      tmem_st8_fill(tmem + lane_base + sfa_col + c, 0x7F7F7F7Fu);
+    if (q_in_mma) {
+      tmem_st_wait();
+      for (int c = 0; c < (p.ncols + 31) / 32; ++c) {
+        const int n = c * 32 + lane;
+        const uint32_t e = n < p.ncols ? qbyte[n] : 127u;
+        tmem_st1(tmem + lane_base + sfb_col + (uint32_t)c, e * 0x01010101u);
+      }
+    }
     tmem_st_wait();
   }
   __syncwarp();
@@ -337,14 +355,29 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
       tc_fence_after();
       const int nt = min(G, ntiles - g * G);
       const bool unit_done = (g + 1) * G >= min(ntiles, (unit + 1) * kSlotTiles);
-      for (int u = sub; u < nt * cchunks; u += kEW) {
-        const int i = u / cchunks, c0 = (u % cchunks) * 16;
-        const int it = g * G + i;
-        const int b = tile_seq(it);
-        const int64_t j = (int64_t)tile_row0(it) + row;
-        const float* qs = qscale + (b - b_first) * p.ncols;
-        uint32_t sbits = 0;
-        if (j < p.E) {
+      // units (tile i, 16-column chunk) of the group, split over the quarter's kEW warps; two
+      // units per tensor-memory round trip
+      const int nunits_g = nt * cchunks;
+      for (int u0 = sub; u0 < nunits_g; u0 += 2 * kEW) {
+        const int uu[2] = {u0, u0 + kEW};
+        uint32_t r[2][16];
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+          if (uu[x] < nunits_g)
+            tmem_ld16(tmem + lane_base +
+                          (uint32_t)(a * acc_cols + (uu[x] / cchunks) * p.ncols +
+                                     (uu[x] % cchunks) * 16),
+                      r[x]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (uu[x] >= nunits_g) break;
+          const int i = uu[x] / cchunks, c0 = (uu[x] % cchunks) * 16;
+          const int it = g * G + i;
+          const int b = tile_seq(it);
+          const int64_t j = (int64_t)tile_row0(it) + row;
+          if (j >= p.E) continue;
+          uint32_t sbits;
           if (SW == 2)
             sbits = *reinterpret_cast<const uint16_t*>(stiles + ring_tile(it) * kScaleTileBytes +
                                                        row * 2);
@@ -352,34 +385,33 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
             sbits = NB == 2
                 ? (uint32_t)*reinterpret_cast<const uint16_t*>(p.ki_scales + ((int64_t)b * p.E + j) * 2)
                 : (uint32_t)p.ki_scales[(int64_t)b * p.E + j];
-        }
-        float sk[NB];
-        sk[0] = exp2_int((int)(sbits & 0xFF) - 127);
-        if (NB == 2) sk[NB - 1] = exp2_int((int)((sbits >> 8) & 0xFF) - 127);
-        uint32_t r[16];
-        tmem_ld16(tmem + lane_base + (uint32_t)(a * acc_cols + i * p.ncols + c0), r);
-        tmem_ld_wait();
-        if (j < p.E) {
+          float sk[NB];
+          sk[0] = exp2_int((int)(sbits & 0xFF) - 127);
+          if (NB == 2) sk[NB - 1] = exp2_int((int)((sbits >> 8) & 0xFF) - 127);
+          uint16_t* srow = p.scores + ((int64_t)b * p.Nq + i0) * p.E + j;
 #pragma unroll
           for (int cc = 0; cc < 16; cc += CPQ) {
             const int ql = (c0 + cc) / CPQ;
             if (ql < nq) {
-              float s = 0.f;
+              float sc = 0.f;
 #pragma unroll
               for (int h = 0; h < H_I; ++h) {
                 float dot = 0.f;
 #pragma unroll
                 for (int blk = 0; blk < NB; ++blk) {
-                  const int c_in = cc + h * NB * SW + blk;             // blocks in place
+                  const int c_in = cc + h * NB * SW + blk;                  // blocks in place
                   const int c_sw = cc + h * NB * SW + (SW - 1) * NB + blk;  // blocks swapped
-                  const float d = swapped ? __uint_as_float(r[c_sw]) : __uint_as_float(r[c_in]);
-                  dot += (d * qs[c0 + c_in]) * sk[blk];
+                  const float d = swapped ? __uint_as_float(r[x][c_sw])
+                                          : __uint_as_float(r[x][c_in]);
+                  const float qm =
+                      q_in_mma ? 1.f
+                               : exp2_int((int)qbyte[(b - b_first) * p.ncols + c0 + c_in] - 127);
+                  dot = fmaf(d * qm, sk[blk], dot);
                 }
-                s += fmaxf(dot, 0.f);
+                sc += fmaxf(dot, 0.f);
               }
-              s += 0.0f;  // -0 -> +0
-              if (j < qvis[ql])
-                p.scores[((int64_t)b * p.Nq + i0 + ql) * p.E + j] = f32_to_bf16_bits(s);
+              sc += 0.0f;  // -0 -> +0
+              if (j < qvis[ql]) srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
             }
           }
         }
@@ -411,13 +443,14 @@ template <int H_I, int NB, int SW>
 cudaError_t launch_t(const CUtensorMap* kmap, const IdxParams& prm, const IndexerPlan& plan, int B,
                      cudaStream_t stream) {
   auto kern = indexer_kernel<H_I, NB, SW>;
+  const size_t smem = smem_bytes((prm.Nq == 1 ? kMaxSeqPerCta : 1) * prm.ncols);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+                                       (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((unsigned)plan.n_splits, (unsigned)plan.n_groups,
             (unsigned)(prm.Nq == 1 ? 1 : B));
   ProfScope prof(stream, "indexer_mxf4");
-  return launch_ex(kern, grid, dim3(kThreads), kSmemBytes, stream, 1, *kmap, prm);
+  return launch_ex(kern, grid, dim3(kThreads), smem, stream, 1, *kmap, prm);
 }
 
 int next_pow2_at_least32(int x) {
@@ -429,21 +462,23 @@ int next_pow2_at_least32(int x) {
 }  // namespace
 
 // Bulk-copy path: 32-byte key rows, each head doubled into 16 columns, 16-byte aligned scale runs.
-bool indexer_bulk_path(int H_I, int d_I, int64_t E) { return d_I == 64 && H_I <= 4 && E % 8 == 0; }
+bool indexer_bulk_path(int H_I, int d_I, int64_t E, int Nq) {
+  return Nq == 1 && d_I == 64 && H_I <= 4 && E % 8 == 0;
+}
 
 IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I) {
   IndexerPlan pl{};
-  const int cpq = H_I * (d_I / 32) * (indexer_bulk_path(H_I, d_I, E) ? 2 : 1);
+  const int cpq = H_I * (d_I / 32) * (indexer_bulk_path(H_I, d_I, E, Nq) ? 2 : 1);
   if (Nq == 1) {  // two CTAs per SM: 3 x 64 + 32 scale columns fit in 256
     pl.QN = 1;
     pl.ncols = cpq > 16 ? 32 : 16;
     pl.G = kMaxG;
     pl.nacc = 3;
-  } else {         // one CTA per SM: 3 x (2 x 64) + 32 columns fit in 512
-    pl.ncols = kMaxCols;
+  } else {         // one CTA per SM: 2 x 224 + 32 columns fit in 512
     pl.QN = kMaxCols / cpq;
-    pl.G = 2;
-    pl.nacc = 3;
+    pl.ncols = pl.QN * cpq;
+    pl.G = 1;
+    pl.nacc = 2;
   }
   pl.n_groups = (Nq + pl.QN - 1) / pl.QN;
   const int64_t tiles = (E + kTileM - 1) / kTileM;
@@ -494,7 +529,7 @@ cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, con
   prm.ki_codes = ki_codes;
   prm.status = status;
   const int NB = d_I / 32;
-  const int SW = indexer_bulk_path(H_I, d_I, E) ? 2 : 1;
+  const int SW = indexer_bulk_path(H_I, d_I, E, Nq) ? 2 : 1;
 #define CSA_IDX_CASE(HH, NN, SS) \
   if (H_I == HH && NB == NN && SW == SS) return launch_t<HH, NN, SS>(kmap, prm, plan, B, stream);
   CSA_IDX_CASE(1, 1, 1) CSA_IDX_CASE(2, 1, 1) CSA_IDX_CASE(4, 1, 1) CSA_IDX_CASE(8, 1, 1)

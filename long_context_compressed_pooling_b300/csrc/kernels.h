@@ -59,7 +59,7 @@ struct IndexerPlan {
   int tmem_cols; // tensor-memory columns allocated per CTA
 };
 IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I);
-bool indexer_bulk_path(int H_I, int d_I, int64_t E);
+bool indexer_bulk_path(int H_I, int d_I, int64_t E, int Nq);
 cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, const uint8_t* qi_codes,
                            const uint8_t* qi_scales, const uint8_t* ki_scales, uint16_t* scores,
                            int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I, int d_I,

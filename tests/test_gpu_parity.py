@@ -78,6 +78,7 @@ INDEX_CASES = [
     (1, 5, 95, 128, 1, 1, 32, 7),        # block size 1, one head
     (1, 12, 60000, 64000, 4, 4, 64, 100),  # prefill, ~120 tiles per CTA: the copy ring wraps
     (4, 1, 1048575, 1048576, 4, 4, 64, 512),  # decode at 1M: ~28 tiles per CTA, ring wraps
+    (3, 1, 159999, 160000, 4, 4, 64, 300),  # decode: CTAs span two sequences, ragged tiles
 ]
 
 
