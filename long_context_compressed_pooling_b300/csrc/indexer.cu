@@ -29,7 +29,8 @@
 // slot's last group (the epilogue reads the slot's scale tile). The MMA warp issues
 // groups of G tiles (one elected lane of a converged warp) into the next accumulator group of a
 // ring in tensor memory (3 x 4 x 16 columns for decode, 2 x 1 x 224 for prefill) and commits
-// once per group; eight epilogue warps (two per tensor-memory lane quarter) drain a group
+// once per group; the epilogue warps (two per tensor-memory lane quarter for decode, four for
+// prefill) drain a group
 // together, so the commit -> epilogue round trip is paid once per group. Decode (one query per
 // sequence) runs persistent CTAs over all (sequence, tile) pairs; prefill gives each CTA one
 // (sequence, query group). Every mbarrier wait is bounded (kFlagTimeout on expiry).
@@ -47,9 +48,9 @@ constexpr int kSlotTiles = 8;   // tiles per copy slot (one code copy + one scal
 constexpr int kSlots = 3;       // slots in the ring
 constexpr int kRingTiles = kSlotTiles * kSlots;
 constexpr int kScaleTileBytes = kTileM * 2;  // one tile's UE8M0 scales (NB = 2)
-constexpr int kEW = 2;                      // epilogue warps per tensor-memory lane quarter
-constexpr int kThreads = 64 + 128 * kEW;    // copy warp, MMA warp, 8 epilogue warps
-constexpr int kWorkThreads = kThreads - 32; // every warp but the copy warp
+// Copy warp, MMA warp and EW epilogue warps per tensor-memory lane quarter (2 for decode, whose
+// CTAs run two per SM; 4 for prefill, whose epilogue is the critical path).
+constexpr int threads_for(int ew) { return 64 + 128 * ew; }
 constexpr int kMaxCols = 224;    // MMA N of a prefill CTA (14 queries x 16 columns)
 constexpr int kMaxG = 4;
 constexpr int kMaxAcc = 8;  // accumulator groups in tensor memory (a ring)
@@ -81,12 +82,12 @@ constexpr size_t smem_bytes(int brows) {
 }
 
 // Named barrier over every warp but the copy warp (the copy warp never waits on set-up).
-CSA_DEV void work_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kWorkThreads) : "memory"); }
+CSA_DEV void work_sync(int n) { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
 
 // H_I heads, NB = d_I / 32 scale blocks per vector, SW = 2 for the bulk-copy path (each head's
 // blocks in place and swapped), else 1; CPQ = H_I * NB * SW MMA columns per query.
-template <int H_I, int NB, int SW>
-__global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
+template <int H_I, int NB, int SW, bool PREFILL, int EW = PREFILL ? 4 : 2>
+__global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                                                            const IdxParams p) {
   constexpr int CPQ = H_I * NB * SW;
   static_assert(16 % CPQ == 0, "columns per query must divide 16");
@@ -113,7 +114,11 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   // Work: prefill (Nq > 1) -> one (sequence, query group) per grid (y, z) and a range of entry
   // tiles per x. Decode (Nq == 1) -> CTA x walks the flattened (sequence, tile) range
   // [tb, te) of all sequences; the query operands of the sequences it touches stay resident.
-  const bool decode = p.Nq == 1;
+  constexpr bool decode = !PREFILL;  // the launch picks PREFILL = (Nq > 1)
+  // The entries' UE8M0 scales (two per entry) travel with their codes into the slot ring (bulk
+  // copies need 16-byte aligned runs: E % 8 == 0, always true on the bulk-copy path); otherwise
+  // the epilogue reads them from global memory.
+  const bool scales_in_smem = SW == 2 || (NB == 2 && (p.E % 8) == 0);
   const int split = blockIdx.x, group = blockIdx.y;
   const int i0 = decode ? 0 : group * p.QN;
   const int nq = decode ? 1 : min(p.QN, p.Nq - i0);
@@ -157,17 +162,18 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWork = threads_for(EW) - 32;  // every warp but the copy warp
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 4 * kEW);  // the MMAs' commit + every epilogue warp
+      mbar_init(&empty[s], 1 + 4 * EW);  // the MMAs' commit + every epilogue warp
     }
     for (int a = 0; a < p.nacc; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4 * kEW);
+      mbar_init(&tempty[a], 4 * EW);
     }
     mbar_init(drain, 1);
-    mbar_init(done, 4 * kEW);
+    mbar_init(done, 4 * EW);
     *aborted = 0;
     fence_mbar_init();
     prefetch_tensormap(&kmap);
@@ -210,10 +216,28 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
           a = b;
         }
       } else {
-        mbar_arrive_expect_tx(&full[slot], (uint32_t)((t1 - t0) * kATileBytes));
+        uint32_t bytes = (uint32_t)((t1 - t0) * kATileBytes);
+        if (scales_in_smem)
+          for (int it = t0; it < t1; ++it) bytes += tile_bytes(it) / 16;
+        mbar_arrive_expect_tx(&full[slot], bytes);
         for (int it = t0; it < t1; ++it)
           tma_load_3d(atiles + ring_tile(it) * kATileBytes, &kmap, &full[slot], 0, tile_row0(it),
                       tile_seq(it));
+        if (scales_in_smem) {  // the tiles' scale bytes, one copy per contiguous run
+          int a = t0;
+          while (a < t1) {
+            const int64_t e0 = tile_addr(a);
+            uint32_t rows = tile_bytes(a) / kRowBytes;
+            int b = a + 1;
+            while (b < t1 && rows == (uint32_t)(b - a) * kTileM && tile_addr(b) == e0 + rows) {
+              rows += tile_bytes(b) / kRowBytes;
+              ++b;
+            }
+            bulk_load(stiles + ring_tile(a) * kScaleTileBytes, p.ki_scales + e0 * 2, rows * 2,
+                      &full[slot]);
+            a = b;
+          }
+        }
       }
     };
     int issued = 0;
@@ -236,7 +260,7 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   // ---- set-up of the work warps: B operand, query scales, visibility, TMEM, scale factors ----
   // Sequence sl of this CTA owns B rows [sl * ncols, (sl + 1) * ncols).
   const int wt = threadIdx.x - 32;
-  for (int idx = wt; idx < n_seq * p.ncols * 2; idx += kWorkThreads) {
+  for (int idx = wt; idx < n_seq * p.ncols * 2; idx += kWork) {
     const int rr = idx >> 1, c = idx & 1;
     const int sl = rr / p.ncols, r = rr % p.ncols;
     const int ql = r / CPQ, h = (r / (NB * SW)) % H_I, sw = (r / NB) % SW, blk = r % NB;
@@ -249,7 +273,7 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
     const int phys = rr * kRowBytes + ((c ^ ((rr >> 2) & 1)) << 4);  // 32-byte swizzle
     *reinterpret_cast<uint4*>(btile + phys) = v;
   }
-  for (int rr = wt; rr < n_seq * p.ncols; rr += kWorkThreads) {
+  for (int rr = wt; rr < n_seq * p.ncols; rr += kWork) {
     const int sl = rr / p.ncols, r = rr % p.ncols;
     const int ql = r / CPQ, h = (r / (NB * SW)) % H_I, blk = r % NB;
     uint32_t e = 127u;  // scale 1.0 for the zero rows of absent queries
@@ -257,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
       e = p.qi_scales[(((int64_t)(b_first + sl) * p.Nq + i0 + ql) * H_I + h) * NB + blk];
     qbyte[rr] = e;
   }
-  for (int ql = wt; ql < nq; ql += kWorkThreads)
+  for (int ql = wt; ql < nq; ql += kWork)
     qvis[ql] = min(p.E, (p.q_pos0 + i0 + ql + 1) / p.m);
   fence_proxy_async_smem();
   if (warp == 1) {
@@ -266,7 +290,7 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   }
   __syncwarp();
   tc_fence_before();
-  work_sync();
+  work_sync(kWork);
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t acc_cols = (uint32_t)(G * p.ncols);  // one accumulator group
@@ -275,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   // MMA yields scale x (exact partial sum of e2m1 products), still exact. Decode CTAs may hold
   // several sequences behind one scale region: their B scales stay 1.0 and the query scales are
   // applied in the epilogue.
-  const bool q_in_mma = p.Nq > 1;
+  constexpr bool q_in_mma = PREFILL;
   if (warp >= 2 && warp < 6) {
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 #pragma unroll
@@ -293,7 +317,7 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   }
   __syncwarp();
   tc_fence_before();
-  work_sync();
+  work_sync(kWork);
   tc_fence_after();
   pdl_wait();  // the predecessor may still read the score buffer this kernel writes
 
@@ -348,37 +372,44 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
       // The slot's scale tile is read below: acquire the copy that filled it (its phase is
       // complete, and it cannot be refilled before this warp releases it).
       if (!mbar_wait_warp(&tfull[a], aph, p.status) ||
-          (SW == 2 && !mbar_wait_warp(&full[slot], (uint32_t)(unit / kSlots) & 1u, p.status))) {
+          (scales_in_smem && !mbar_wait_warp(&full[slot], (uint32_t)(unit / kSlots) & 1u,
+                                             p.status))) {
         if (lane == 0) *aborted = 1;
         break;
       }
       tc_fence_after();
       const int nt = min(G, ntiles - g * G);
       const bool unit_done = (g + 1) * G >= min(ntiles, (unit + 1) * kSlotTiles);
-      // units (tile i, 16-column chunk) of the group, split over the quarter's kEW warps; two
+      // units (tile i, 16-column chunk) of the group, split over the quarter's EW warps; two
       // units per tensor-memory round trip
+      // (prefill groups hold one tile; decode tiles have one or two chunks: no divisions)
       const int nunits_g = nt * cchunks;
-      for (int u0 = sub; u0 < nunits_g; u0 += 2 * kEW) {
-        const int uu[2] = {u0, u0 + kEW};
+      const int csh = cchunks == 2 ? 1 : 0;
+      for (int u0 = sub; u0 < nunits_g; u0 += 2 * EW) {
+        const int uu[2] = {u0, u0 + EW};
+        int ui[2], uc[2];
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          ui[x] = PREFILL ? 0 : uu[x] >> csh;
+          uc[x] = PREFILL ? uu[x] : uu[x] & csh;
+        }
         uint32_t r[2][16];
 #pragma unroll
         for (int x = 0; x < 2; ++x)
           if (uu[x] < nunits_g)
-            tmem_ld16(tmem + lane_base +
-                          (uint32_t)(a * acc_cols + (uu[x] / cchunks) * p.ncols +
-                                     (uu[x] % cchunks) * 16),
+            tmem_ld16(tmem + lane_base + (uint32_t)(a * acc_cols + ui[x] * p.ncols + uc[x] * 16),
                       r[x]);
         tmem_ld_wait();
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
           if (uu[x] >= nunits_g) break;
-          const int i = uu[x] / cchunks, c0 = (uu[x] % cchunks) * 16;
+          const int i = ui[x], c0 = uc[x] * 16;
           const int it = g * G + i;
           const int b = tile_seq(it);
           const int64_t j = (int64_t)tile_row0(it) + row;
           if (j >= p.E) continue;
           uint32_t sbits;
-          if (SW == 2)
+          if (scales_in_smem && NB == 2)
             sbits = *reinterpret_cast<const uint16_t*>(stiles + ring_tile(it) * kScaleTileBytes +
                                                        row * 2);
           else
@@ -439,10 +470,11 @@ __global__ void __launch_bounds__(kThreads) indexer_kernel(const __grid_constant
   }
 }
 
-template <int H_I, int NB, int SW>
+template <int H_I, int NB, int SW, bool PREFILL>
 cudaError_t launch_t(const CUtensorMap* kmap, const IdxParams& prm, const IndexerPlan& plan, int B,
                      cudaStream_t stream) {
-  auto kern = indexer_kernel<H_I, NB, SW>;
+  auto kern = indexer_kernel<H_I, NB, SW, PREFILL>;
+  constexpr int EW = PREFILL ? 4 : 2;
   const size_t smem = smem_bytes((prm.Nq == 1 ? kMaxSeqPerCta : 1) * prm.ncols);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
@@ -450,7 +482,7 @@ cudaError_t launch_t(const CUtensorMap* kmap, const IdxParams& prm, const Indexe
   dim3 grid((unsigned)plan.n_splits, (unsigned)plan.n_groups,
             (unsigned)(prm.Nq == 1 ? 1 : B));
   ProfScope prof(stream, "indexer_mxf4");
-  return launch_ex(kern, grid, dim3(kThreads), smem, stream, 1, *kmap, prm);
+  return launch_ex(kern, grid, dim3(threads_for(EW)), smem, stream, 1, *kmap, prm);
 }
 
 int next_pow2_at_least32(int x) {
@@ -530,11 +562,17 @@ cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, con
   prm.status = status;
   const int NB = d_I / 32;
   const int SW = indexer_bulk_path(H_I, d_I, E, Nq) ? 2 : 1;
-#define CSA_IDX_CASE(HH, NN, SS) \
-  if (H_I == HH && NB == NN && SW == SS) return launch_t<HH, NN, SS>(kmap, prm, plan, B, stream);
-  CSA_IDX_CASE(1, 1, 1) CSA_IDX_CASE(2, 1, 1) CSA_IDX_CASE(4, 1, 1) CSA_IDX_CASE(8, 1, 1)
-  CSA_IDX_CASE(1, 2, 2) CSA_IDX_CASE(2, 2, 2) CSA_IDX_CASE(4, 2, 2) CSA_IDX_CASE(8, 2, 1)
-  CSA_IDX_CASE(1, 2, 1) CSA_IDX_CASE(2, 2, 1) CSA_IDX_CASE(4, 2, 1)
+#define CSA_IDX_CASE(HH, NN, SS, PP)                                          \
+  if (H_I == HH && NB == NN && SW == SS && prefill == PP)                     \
+    return launch_t<HH, NN, SS, PP>(kmap, prm, plan, B, stream);
+  const bool prefill = Nq > 1;
+  CSA_IDX_CASE(1, 1, 1, false) CSA_IDX_CASE(2, 1, 1, false) CSA_IDX_CASE(4, 1, 1, false)
+  CSA_IDX_CASE(8, 1, 1, false) CSA_IDX_CASE(1, 2, 2, false) CSA_IDX_CASE(2, 2, 2, false)
+  CSA_IDX_CASE(4, 2, 2, false) CSA_IDX_CASE(8, 2, 1, false) CSA_IDX_CASE(1, 2, 1, false)
+  CSA_IDX_CASE(2, 2, 1, false) CSA_IDX_CASE(4, 2, 1, false)
+  CSA_IDX_CASE(1, 1, 1, true) CSA_IDX_CASE(2, 1, 1, true) CSA_IDX_CASE(4, 1, 1, true)
+  CSA_IDX_CASE(8, 1, 1, true) CSA_IDX_CASE(8, 2, 1, true) CSA_IDX_CASE(1, 2, 1, true)
+  CSA_IDX_CASE(2, 2, 1, true) CSA_IDX_CASE(4, 2, 1, true)
 #undef CSA_IDX_CASE
   return cudaErrorInvalidValue;
 }
