@@ -380,69 +380,126 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
       tc_fence_after();
       const int nt = min(G, ntiles - g * G);
       const bool unit_done = (g + 1) * G >= min(ntiles, (unit + 1) * kSlotTiles);
-      // units (tile i, 16-column chunk) of the group, split over the quarter's EW warps; two
-      // units per tensor-memory round trip
-      // (prefill groups hold one tile; decode tiles have one or two chunks: no divisions)
-      const int nunits_g = nt * cchunks;
-      const int csh = cchunks == 2 ? 1 : 0;
-      for (int u0 = sub; u0 < nunits_g; u0 += 2 * EW) {
-        const int uu[2] = {u0, u0 + EW};
-        int ui[2], uc[2];
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          ui[x] = PREFILL ? 0 : uu[x] >> csh;
-          uc[x] = PREFILL ? uu[x] : uu[x] & csh;
-        }
-        uint32_t r[2][16];
-#pragma unroll
-        for (int x = 0; x < 2; ++x)
-          if (uu[x] < nunits_g)
-            tmem_ld16(tmem + lane_base + (uint32_t)(a * acc_cols + ui[x] * p.ncols + uc[x] * 16),
-                      r[x]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (uu[x] >= nunits_g) break;
-          const int i = ui[x], c0 = uc[x] * 16;
-          const int it = g * G + i;
-          const int b = tile_seq(it);
-          const int64_t j = (int64_t)tile_row0(it) + row;
-          if (j >= p.E) continue;
-          uint32_t sbits;
+      if constexpr (PREFILL) {
+        // One tile per group (G = 1); warp `sub` of the quarter owns the 16-column chunks
+        // sub, sub + EW, ..., read two per tensor-memory round trip.
+        constexpr int kChunksPerWarp = (kMaxCols / 16 + EW - 1) / EW;
+        const int it = g;
+        const int64_t j = (int64_t)tile_row0(it) + row;
+        uint32_t sbits = 0;
+        if (j < p.E) {
           if (scales_in_smem && NB == 2)
             sbits = *reinterpret_cast<const uint16_t*>(stiles + ring_tile(it) * kScaleTileBytes +
                                                        row * 2);
           else
             sbits = NB == 2
-                ? (uint32_t)*reinterpret_cast<const uint16_t*>(p.ki_scales + ((int64_t)b * p.E + j) * 2)
-                : (uint32_t)p.ki_scales[(int64_t)b * p.E + j];
-          float sk[NB];
-          sk[0] = exp2_int((int)(sbits & 0xFF) - 127);
-          if (NB == 2) sk[NB - 1] = exp2_int((int)((sbits >> 8) & 0xFF) - 127);
-          uint16_t* srow = p.scores + ((int64_t)b * p.Nq + i0) * p.E + j;
+                ? (uint32_t)*reinterpret_cast<const uint16_t*>(p.ki_scales + ((int64_t)b_first * p.E + j) * 2)
+                : (uint32_t)p.ki_scales[(int64_t)b_first * p.E + j];
+        }
+        float sk[NB];
+        sk[0] = exp2_int((int)(sbits & 0xFF) - 127);
+        if (NB == 2) sk[NB - 1] = exp2_int((int)((sbits >> 8) & 0xFF) - 127);
+        uint16_t* srow = p.scores + ((int64_t)b_first * p.Nq + i0) * p.E + j;
 #pragma unroll
-          for (int cc = 0; cc < 16; cc += CPQ) {
-            const int ql = (c0 + cc) / CPQ;
-            if (ql < nq) {
-              float sc = 0.f;
+        for (int k0 = 0; k0 < kChunksPerWarp; k0 += 2) {
+          uint32_t r[2][16];
 #pragma unroll
-              for (int h = 0; h < H_I; ++h) {
-                float dot = 0.f;
+          for (int k = 0; k < 2; ++k) {
+            const int c = sub + (k0 + k) * EW;
+            if (c < cchunks)
+              tmem_ld16(tmem + lane_base + (uint32_t)(a * acc_cols + c * 16), r[k]);
+          }
+          tmem_ld_wait();
+          if (j >= p.E) continue;
 #pragma unroll
-                for (int blk = 0; blk < NB; ++blk) {
-                  const int c_in = cc + h * NB * SW + blk;                  // blocks in place
-                  const int c_sw = cc + h * NB * SW + (SW - 1) * NB + blk;  // blocks swapped
-                  const float d = swapped ? __uint_as_float(r[x][c_sw])
-                                          : __uint_as_float(r[x][c_in]);
-                  const float qm =
-                      q_in_mma ? 1.f
-                               : exp2_int((int)qbyte[(b - b_first) * p.ncols + c0 + c_in] - 127);
-                  dot = fmaf(d * qm, sk[blk], dot);
+          for (int k = 0; k < 2; ++k) {
+            const int c = sub + (k0 + k) * EW;
+            if (c < cchunks) {
+#pragma unroll
+              for (int cc = 0; cc < 16; cc += CPQ) {
+                const int ql = (c * 16 + cc) / CPQ;
+                if (ql < nq) {
+                  float sc = 0.f;
+#pragma unroll
+                  for (int h = 0; h < H_I; ++h) {
+                    float dot = 0.f;
+#pragma unroll
+                    for (int blk = 0; blk < NB; ++blk)
+                      dot = fmaf(__uint_as_float(r[k][cc + h * NB + blk]), sk[blk], dot);
+                    sc += fmaxf(dot, 0.f);
+                  }
+                  sc += 0.0f;  // -0 -> +0
+                  if (j < qvis[ql]) srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
                 }
-                sc += fmaxf(dot, 0.f);
               }
-              sc += 0.0f;  // -0 -> +0
-              if (j < qvis[ql]) srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
+            }
+          }
+        }
+      } else {
+        // units (tile i, 16-column chunk) of the group, split over the quarter's EW warps; two
+        // units per tensor-memory round trip
+        // (prefill groups hold one tile; decode tiles have one or two chunks: no divisions)
+        const int nunits_g = nt * cchunks;
+        const int csh = cchunks == 2 ? 1 : 0;
+        for (int u0 = sub; u0 < nunits_g; u0 += 2 * EW) {
+          const int uu[2] = {u0, u0 + EW};
+          int ui[2], uc[2];
+  #pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            ui[x] = PREFILL ? 0 : uu[x] >> csh;
+            uc[x] = PREFILL ? uu[x] : uu[x] & csh;
+          }
+          uint32_t r[2][16];
+  #pragma unroll
+          for (int x = 0; x < 2; ++x)
+            if (uu[x] < nunits_g)
+              tmem_ld16(tmem + lane_base + (uint32_t)(a * acc_cols + ui[x] * p.ncols + uc[x] * 16),
+                        r[x]);
+          tmem_ld_wait();
+  #pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (uu[x] >= nunits_g) break;
+            const int i = ui[x], c0 = uc[x] * 16;
+            const int it = g * G + i;
+            const int b = tile_seq(it);
+            const int64_t j = (int64_t)tile_row0(it) + row;
+            if (j >= p.E) continue;
+            uint32_t sbits;
+            if (scales_in_smem && NB == 2)
+              sbits = *reinterpret_cast<const uint16_t*>(stiles + ring_tile(it) * kScaleTileBytes +
+                                                         row * 2);
+            else
+              sbits = NB == 2
+                  ? (uint32_t)*reinterpret_cast<const uint16_t*>(p.ki_scales + ((int64_t)b * p.E + j) * 2)
+                  : (uint32_t)p.ki_scales[(int64_t)b * p.E + j];
+            float sk[NB];
+            sk[0] = exp2_int((int)(sbits & 0xFF) - 127);
+            if (NB == 2) sk[NB - 1] = exp2_int((int)((sbits >> 8) & 0xFF) - 127);
+            uint16_t* srow = p.scores + ((int64_t)b * p.Nq + i0) * p.E + j;
+  #pragma unroll
+            for (int cc = 0; cc < 16; cc += CPQ) {
+              const int ql = (c0 + cc) / CPQ;
+              if (ql < nq) {
+                float sc = 0.f;
+  #pragma unroll
+                for (int h = 0; h < H_I; ++h) {
+                  float dot = 0.f;
+  #pragma unroll
+                  for (int blk = 0; blk < NB; ++blk) {
+                    const int c_in = cc + h * NB * SW + blk;                  // blocks in place
+                    const int c_sw = cc + h * NB * SW + (SW - 1) * NB + blk;  // blocks swapped
+                    const float d = swapped ? __uint_as_float(r[x][c_sw])
+                                            : __uint_as_float(r[x][c_in]);
+                    const float qm =
+                        q_in_mma ? 1.f
+                                 : exp2_int((int)qbyte[(b - b_first) * p.ncols + c0 + c_in] - 127);
+                    dot = fmaf(d * qm, sk[blk], dot);
+                  }
+                  sc += fmaxf(dot, 0.f);
+                }
+                sc += 0.0f;  // -0 -> +0
+                if (j < qvis[ql]) srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
+              }
             }
           }
         }
