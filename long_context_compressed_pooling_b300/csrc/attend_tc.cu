@@ -375,10 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
       float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float p00 = exp2f(fmaf(f32(r[4 * i + 0]), kLog2e, nb0));
-        const float p01 = exp2f(fmaf(f32(r[4 * i + 1]), kLog2e, nb0));
-        const float p10 = exp2f(fmaf(f32(r[4 * i + 2]), kLog2e, nb1));
-        const float p11 = exp2f(fmaf(f32(r[4 * i + 3]), kLog2e, nb1));
+        const float p00 = ex2_approx(fmaf(f32(r[4 * i + 0]), kLog2e, nb0));
+        const float p01 = ex2_approx(fmaf(f32(r[4 * i + 1]), kLog2e, nb0));
+        const float p10 = ex2_approx(fmaf(f32(r[4 * i + 2]), kLog2e, nb1));
+        const float p11 = ex2_approx(fmaf(f32(r[4 * i + 3]), kLog2e, nb1));
         rs0 += p00 + p01;
         rs1 += p10 + p11;
         pk[2 * i] = pack_bf16x2(p00, p01);
@@ -412,12 +412,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
           tmem_st_wait();
         }
       }
-      // rows r0 / r0 + 8, keys 64 hf + 8i + 2tq, +1: atom hf, 16-byte chunk i, word tq
+      // P rows 16q .. 16q + 15, keys 64 hf .. 64 hf + 63 (atom hf, 16-byte chunks 0-7): each
+      // stmatrix.x4 stores two chunks x two 8-row halves; lane l addresses row l % 8 (+ 8 for
+      // the odd matrices) of chunk 2c + l / 16.
+      {
+        const int mrow = q * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int mchunk = lane >> 4;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t w = (uint32_t)(tq * 4);
-        *reinterpret_cast<uint32_t*>(Ps + sw128(r0, 8 * hf + i, kM) + w) = pk[2 * i];
-        *reinterpret_cast<uint32_t*>(Ps + sw128(r0 + 8, 8 * hf + i, kM) + w) = pk[2 * i + 1];
+        for (int c = 0; c < 4; ++c)
+          stmatrix_x4(smem_addr(Ps + sw128(mrow, 8 * hf + 2 * c + mchunk, kM)), pk[4 * c],
+                      pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       }
       fence_proxy_async_smem();  // P (generic stores) -> tensor-core reads
       tc_fence_before();

@@ -23,8 +23,26 @@ CSA_DEV uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// Two floats rounded to bf16 (round-to-nearest-even) in one 32-bit word, lo in the low half.
 CSA_DEV uint32_t pack_bf16x2(float lo, float hi) {
-  return (uint32_t)f32_to_bf16_bits(lo) | ((uint32_t)f32_to_bf16_bits(hi) << 16);
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22; results below 2^-126 flush to
+// zero): used where the value is rounded to bf16 next.
+CSA_DEV float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Stores four 8x8 b16 matrices from the m16n8 fragment layout: lane l supplies the shared-memory
+// address of row l % 8 of matrix l / 8; register i holds this thread's pair of matrix i.
+CSA_DEV void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+               "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
 }
 
 CSA_DEV uint32_t smem_addr(const void* p) {
