@@ -46,11 +46,11 @@ constexpr int kKC = 128;           // keys per chunk (N of QK^T, K of PV)
 constexpr int kHalf = kKC / 2;     // keys per softmax warp (and per O accumulator)
 constexpr int kStages = 3;         // K/V stages
 constexpr int kSoftmaxWarps = 8;   // warps 0-7: lane quarter w % 4, key half w / 4
-constexpr int kLoadWarp0 = 8;      // warps 8-11
-constexpr int kLoadWarps = 4;
+constexpr int kLoadWarp0 = 8;      // warps 8-15
+constexpr int kLoadWarps = 8;
 constexpr int kLoadThreads = 32 * kLoadWarps;
-constexpr int kMmaWarp = 12;
-constexpr int kThreads = 416;
+constexpr int kMmaWarp = 16;
+constexpr int kThreads = 544;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;    // O accumulators: key half 0 at [256, 384), half 1 at [384, 512)
 constexpr int kQBytes = kM * kD * 2;        // 16 KB
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
 
   if (warp >= kLoadWarp0 && warp < kMmaWarp) {
     // ------------------------------- loaders -------------------------------
-    // Warp wl copies rows [32 wl, 32 wl + 32) of each chunk, two rows per instruction: lanes
+    // Warp wl copies rows [16 wl, 16 wl + 16) of each chunk, two rows per instruction: lanes
     // 0-15 and 16-31 each copy the 16 chunks of one 256-byte row (coalesced).
     const int wl = warp - kLoadWarp0;
     const int h = lane >> 4, cc = lane & 15;
@@ -200,8 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
       if (it >= kStages &&
           !mbar_wait_warp(&kv_empty[s], (uint32_t)(it / kStages - 1) & 1u, p.status))
         break;
-      // source row of row 32 wl + lane (element offset; bit 62 = raw window token, -1 = none)
-      const int i = wl * 32 + lane;
+      // source row of row 16 wl + lane % 16 (element offset; bit 62 = raw window token, -1 =
+      // none); lanes 16-31 repeat lanes 0-15
+      const int i = wl * 16 + (lane & 15);
       const int64_t key = (int64_t)(c_begin + it) * kKC + i;
       long long cd = -1;
       if (key < n_keys) {
@@ -216,14 +217,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
         }
       }
       const uint32_t vbits = __ballot_sync(0xffffffffu, cd >= 0);
-      if (lane == 0) kmask[s * 4 + wl] = vbits;
+      if (lane == 0) reinterpret_cast<uint16_t*>(kmask)[s * 8 + wl] = (uint16_t)(vbits & 0xFFFFu);
       uint8_t* kd = KV + s * 2 * kTileBytes;
       uint8_t* vd = kd + kTileBytes;
 #pragma unroll
-      for (int st = 0; st < 16; ++st) {
-        const int r = 2 * st + h;  // row within this warp's 32
+      for (int st = 0; st < 8; ++st) {
+        const int r = 2 * st + h;  // row within this warp's 16
         const long long c2 = shfl_i64(cd, r);
-        const uint32_t off = sw128(wl * 32 + r, cc, kKC);
+        const uint32_t off = sw128(wl * 16 + r, cc, kKC);
         const bool valid = c2 >= 0;
         const int64_t e = c2 & (kRawBit - 1);
         const bool raw = (c2 & kRawBit) != 0;
