@@ -93,11 +93,12 @@ def layer_work(s):
         else:
             sel_keys += nv
     if s.kind == "csa":
-        # keys are read once per query group (decode: once per sequence)
+        # unique bytes: the visible index keys once per sequence, the queries, the BF16 scores
+        # written (read back by the top-k)
         nv_max = _vis(s.q_pos0 + Nq - 1, m, E)
-        groups = 1 if Nq == 1 else math.ceil(Nq / max(1, 64 // (s.H_I * (s.d_I // 32))))
-        idx_bytes = B * groups * nv_max * (s.d_I // 2 + s.d_I // 32) + \
-            B * Nq * s.H_I * (s.d_I // 2 + s.d_I // 32)
+        idx_bytes = B * nv_max * (s.d_I // 2 + s.d_I // 32) + \
+            B * Nq * s.H_I * (s.d_I // 2 + s.d_I // 32) + B * sum(
+                _vis(s.q_pos0 + i, m, E) for i in range(Nq)) * 2
         k["indexer_mxf4"] = dict(bytes=idx_bytes, flops=B * idx_flops)
         k["topk"] = dict(bytes=B * top_bytes, flops=0)
     name = "csa_attend" if s.kind == "csa" else "hca_attend"
@@ -408,12 +409,24 @@ def run_native(args, rank, world):
         dom = max(kern, key=lambda n: kern[n]["share"]) if kern else None
         if dom is not None:
             d = kern[dom]
-            ab = d["alg_bytes_per_launch"] or 0
-            achieved = ab / (d["ms_per_launch"] * 1e-3) / 1e9
-            out["roofline"] = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm,
-                               "unit": "GB/s", "frac": achieved / hbm,
-                               "traffic": load_traffic(dom, wl.name),
-                               "peak_source": f"{src} hbm_gbs (STREAM-style copy)"}
+            lpp = d["launches_per_step"]
+            if wl.mode == "prefill" and dom.endswith("_attend"):
+                # prefill attention is a dense bf16 contraction on the tensor pipe
+                fl = work[dom]["flops"] / max(lpp, 1e-9)
+                achieved = fl / (d["ms_per_launch"] * 1e-3) / 1e12
+                out["roofline"] = {"kernel": dom, "bound": "tensor", "achieved": achieved,
+                                   "peak": bf16_sus, "unit": "TFLOP/s",
+                                   "frac": achieved / bf16_sus,
+                                   "traffic": load_traffic(dom, wl.name),
+                                   "peak_source": f"{src} bf16_tflops_sustained (cuBLAS, timed "
+                                                  f"inside a long step)"}
+            else:
+                ab = d["alg_bytes_per_launch"] or 0
+                achieved = ab / (d["ms_per_launch"] * 1e-3) / 1e9
+                out["roofline"] = {"kernel": dom, "bound": "hbm", "achieved": achieved,
+                                   "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                                   "traffic": load_traffic(dom, wl.name),
+                                   "peak_source": f"{src} hbm_gbs (STREAM-style copy)"}
         out["kernels"] = kern
         out["gpu_launches"] = int(round(sum(v["launches_per_step"] for v in kern.values()) * K))
     out["clocks"] = clk.summary()

@@ -166,6 +166,13 @@ size_t hca_attend_workspace_size(int B, int Nq, int H, int d, int64_t E, int m, 
  * [compress_begin, N) into its entry cache, then (CSA) index + top-k and attend, or (HCA)
  * attend densely. The two layers get independent inputs; either descriptor may be NULL.
  * Fields follow the single calls above.
+ * Concurrency: with both layers present, the HCA layer runs on a side stream owned by the
+ * library (one per device, created on the first call that is not being captured into a CUDA
+ * graph), forked from `stream` and joined back into it with events; work enqueued on `stream`
+ * afterwards sees both layers complete. Without the side stream (a graph capture before any
+ * eager call) everything runs on `stream`.
+ * Workspace: csa_hca_layer_pair_workspace_size() = a CSA region (scores, then the CSA
+ * attention's split-K partials) followed by a disjoint HCA region.
  * ---------------------------------------------------------------------------------------- */
 typedef struct csa_layer_desc {
   const uint16_t* q;            /* [B, Nq, H, d] */

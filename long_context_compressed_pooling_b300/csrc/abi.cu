@@ -31,6 +31,41 @@ uint32_t* status_word() {
   return g_status_ptr[dev];
 }
 
+// Side stream of the layer-pair driver, one per device, created on the first call that is not
+// being captured into a CUDA graph (creating streams during a capture is not allowed). The HCA
+// layer runs on it, joined back with an event; without it (a capture before any eager call) the
+// driver runs everything on the caller's stream.
+struct SideStreams {
+  cudaStream_t s[2];
+  cudaEvent_t ev[3];
+};
+SideStreams* g_side[kMaxDevices] = {};
+bool g_side_failed[kMaxDevices] = {};
+
+SideStreams* side_streams(cudaStream_t st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_side[dev] != nullptr || g_side_failed[dev]) return g_side[dev];
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone)
+    return nullptr;  // try again on an eager call
+  SideStreams* ss = new SideStreams();
+  bool ok = true;
+  for (int i = 0; i < 2; ++i)
+    ok = ok && cudaStreamCreateWithFlags(&ss->s[i], cudaStreamNonBlocking) == cudaSuccess;
+  for (int i = 0; i < 3; ++i)
+    ok = ok && cudaEventCreateWithFlags(&ss->ev[i], cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    (void)cudaGetLastError();
+    delete ss;
+    g_side_failed[dev] = true;
+    return nullptr;
+  }
+  g_side[dev] = ss;
+  return ss;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -154,6 +189,21 @@ namespace csa {
 uint32_t* device_status_word() { return status_word(); }
 }  // namespace csa
 
+namespace {
+size_t pair_csa_ws(const csa_layer_desc* c) {
+  if (!c) return 0;
+  const int64_t E = c->N / (c->m > 0 ? c->m : 1);
+  const size_t a = index_ws_bytes(c->B, c->Nq, E, c->scores != nullptr);
+  const size_t b = attend_workspace_bytes(c->B * c->Nq, c->H, c->d, (int64_t)c->k + c->W);
+  return round_up(a > b ? a : b, 256);
+}
+size_t pair_hca_ws(const hca_layer_desc* h) {
+  if (!h) return 0;
+  const int64_t E = h->N / (h->m > 0 ? h->m : 1);
+  return round_up(attend_workspace_bytes(h->B * h->Nq, h->H, h->d, E + h->W), 256);
+}
+}  // namespace
+
 extern "C" {
 
 int csa_abi_version(void) { return 1; }
@@ -262,20 +312,9 @@ csa_status hca_attend(const uint16_t* q, const uint16_t* k_cmp, const uint16_t* 
 }
 
 size_t csa_hca_layer_pair_workspace_size(const csa_layer_desc* c, const hca_layer_desc* h) {
-  size_t need = 0;
-  if (c) {
-    const int64_t E = c->N / (c->m > 0 ? c->m : 1);
-    const size_t a = index_ws_bytes(c->B, c->Nq, E, c->scores != nullptr);
-    const size_t b = attend_workspace_bytes(c->B * c->Nq, c->H, c->d, (int64_t)c->k + c->W);
-    need = a > need ? a : need;
-    need = b > need ? b : need;
-  }
-  if (h) {
-    const int64_t E = h->N / (h->m > 0 ? h->m : 1);
-    const size_t b = attend_workspace_bytes(h->B * h->Nq, h->H, h->d, E + h->W);
-    need = b > need ? b : need;
-  }
-  return need;
+  // [CSA region: scores, then the CSA attention's partials][HCA region]: the two layers may run
+  // concurrently, so their regions never overlap.
+  return pair_csa_ws(c) + pair_hca_ws(h);
 }
 
 csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, void* ws,
@@ -311,6 +350,16 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
   uint32_t* status = status_word();
   if (!status) return CSA_ERR_CUDA;
 
+  // Fork: with both layers present the HCA layer runs on a side stream beside the CSA layer
+  // (a fork costs more than it saves for a single layer).
+  SideStreams* ss = (c && h) ? side_streams(st) : nullptr;
+  if (ss) {
+    if (cudaEventRecord(ss->ev[0], st) != cudaSuccess ||
+        cudaStreamWaitEvent(ss->s[0], ss->ev[0], 0) != cudaSuccess)
+      return CSA_ERR_CUDA;
+  }
+  uint8_t* ws_c = static_cast<uint8_t*>(ws);
+  uint8_t* ws_h = ws_c + pair_csa_ws(c);
   if (c) {
     const int64_t E = c->N / c->m;
     const int64_t j0 = c->compress_begin / c->m;
@@ -319,21 +368,27 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
       return CSA_ERR_CUDA;
     csa_status s = run_index_topk(c->qi_codes, c->qi_scales, c->ki_codes, c->ki_scales, c->B,
                                   c->Nq, c->q_pos0, E, c->m, c->H_I, c->d_I, c->k, c->topk_idx,
-                                  c->topk_cnt, c->scores, ws, st);
+                                  c->topk_cnt, c->scores, ws_c, st);
     if (s != CSA_OK) return s;
     AttendArgs a{c->q, c->k_cmp, c->v_cmp, c->topk_idx, c->topk_cnt, c->k_raw, c->v_raw, c->out,
                  c->lse, E, c->N, c->q_pos0, c->k, c->m, c->W, c->B, c->Nq, c->H, c->d};
-    if (launch_attend(a, (int64_t)c->k + c->W, ws, status, st) != cudaSuccess) return CSA_ERR_CUDA;
+    if (launch_attend(a, (int64_t)c->k + c->W, ws_c, status, st) != cudaSuccess) return CSA_ERR_CUDA;
   }
   if (h) {
     const int64_t E = h->N / h->m;
     const int64_t j0 = h->compress_begin / h->m;
+    cudaStream_t sh = ss ? ss->s[0] : st;
     if (launch_compress(h->k_raw, h->v_raw, h->logits, h->B, h->N, h->d, h->m, j0, E - j0,
-                        h->k_cmp, h->v_cmp, st) != cudaSuccess)
+                        h->k_cmp, h->v_cmp, sh) != cudaSuccess)
       return CSA_ERR_CUDA;
     AttendArgs a{h->q, h->k_cmp, h->v_cmp, nullptr, nullptr, h->k_raw, h->v_raw, h->out, h->lse,
                  E, h->N, h->q_pos0, 0, h->m, h->W, h->B, h->Nq, h->H, h->d};
-    if (launch_attend(a, hca_max_keys(E, h->m, h->N, h->W), ws, status, st) != cudaSuccess)
+    if (launch_attend(a, hca_max_keys(E, h->m, h->N, h->W), ws_h, status, sh) != cudaSuccess)
+      return CSA_ERR_CUDA;
+  }
+  if (ss) {  // join: the caller's stream continues after both side streams
+    if (cudaEventRecord(ss->ev[2], ss->s[0]) != cudaSuccess ||
+        cudaStreamWaitEvent(st, ss->ev[2], 0) != cudaSuccess)
       return CSA_ERR_CUDA;
   }
   return CSA_OK;

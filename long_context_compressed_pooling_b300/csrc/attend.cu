@@ -359,6 +359,9 @@ __global__ void __launch_bounds__(NW * 32) attend_kernel(const AttnParams p) {
 }
 
 // Combines workspace split-K partials: out = sum_s w_s O_s / sum_s w_s l_s, w_s = exp(m_s - max m).
+// One warp per (token, head); every split's (max, sum) is read once by one lane, the weights are
+// broadcast with shuffles, and the partial outputs are read eight splits at a time so that their
+// loads overlap.
 template <int D>
 __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ ws_o,
                                                   const float* __restrict__ ws_ml, int n_splits,
@@ -368,22 +371,37 @@ __global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ ws_
   pdl_wait();
   const int64_t th = blockIdx.x;  // tok * H + h
   const int lane = threadIdx.x;
+  const int64_t stride = tokens * H;
   float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, ws_ml[((int64_t)s * tokens * H + th) * 2]);
+  for (int s = lane; s < n_splits; s += 32) M = fmaxf(M, ws_ml[(s * stride + th) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   constexpr int PER = D / 32;
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
   float L = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const int64_t base = (int64_t)s * tokens * H + th;
-      const float ms = ws_ml[base * 2], ls = ws_ml[base * 2 + 1];
-      if (ms == -INFINITY) continue;
-      const float w = expf(ms - M);
-      L += w * ls;
+    for (int s0 = 0; s0 < n_splits; s0 += 32) {
+      // lane s of this group of 32 splits computes w_s and w_s * l_s
+      const int sl = s0 + lane;
+      float w = 0.f, wl = 0.f;
+      if (sl < n_splits) {
+        const float2 ml = *reinterpret_cast<const float2*>(ws_ml + (sl * stride + th) * 2);
+        w = ml.x == -INFINITY ? 0.f : expf(ml.x - M);
+        wl = w * ml.y;
+      }
 #pragma unroll
-      for (int i = 0; i < PER; ++i) acc[i] += w * ws_o[base * D + lane * PER + i];
+      for (int o = 16; o > 0; o >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o);
+      L += wl;
+      const int ng = min(32, n_splits - s0);
+#pragma unroll 8
+      for (int x = 0; x < ng; ++x) {
+        const float wx = __shfl_sync(0xffffffffu, w, x);
+        const float* src = ws_o + ((int64_t)(s0 + x) * stride + th) * D + lane * PER;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) acc[i] = fmaf(wx, src[i], acc[i]);
+      }
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
