@@ -38,8 +38,8 @@ if ROOT not in sys.path:
 METRIC = "CSA/HCA decode tok/s + HBM GB/s at 128K-1M ctx; prefill TFLOP/s"
 DEFAULT_CONFIG = "csa_decode_128k"
 KERNEL_SOURCES = {
-    "indexer_mxf4": "indexer.cu", "topk": "topk.cu", "csa_attend": "attend.cu",
-    "hca_attend": "attend.cu", "lse_merge": "attend.cu", "compress": "compress.cu",
+    "indexer_mxf4": "indexer.cu", "topk": "topk.cu", "csa_attend": "attend_tc.cu",
+    "hca_attend": "attend_tc.cu", "lse_merge": "attend.cu", "compress": "compress.cu",
 }
 
 
