@@ -554,49 +554,90 @@ def cpu_baseline(wl, states, budget_s=12.0):
 
 
 def run_reference(args, rank, world):
-    """The fp64 oracle timed on the host cores: each step decodes one sequence of the workload."""
+    """The fp64 oracle timed on the host cores, one thread. Decode: each step decodes one
+    sequence of the workload (tok/s). Prefill: each step computes one query row of the chunk
+    (indexer scores, top-k, attention over the pooled entries; TFLOP/s from that row's
+    algorithmic FLOPs). The timed steps stop early once they have used the time budget, so the
+    run stays within minutes whatever --steps is; the line states how many steps ran."""
     import numpy as np
     import torch
     import oracle as O
     from synth import get_config, generate_layer
     if rank != 0:
         return None
+    budget_s = 90.0
     wl = get_config(args.config)
-    if wl.mode != "decode":
-        return {"impl": "reference", "unavailable": "the reference arm times decode workloads only"}
     seqs = []
     for li, s in enumerate(wl.layers):
         x = generate_layer(s.scaled(B=1), wl.seed, li, device="cpu")
-        kr = O.bf16_to_f64(x["k_raw"][0].view(torch.int16).numpy().view(np.uint16))
-        vr = O.bf16_to_f64(x["v_raw"][0].view(torch.int16).numpy().view(np.uint16))
+        bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        kr, vr = O.bf16_to_f64(bits(x["k_raw"][0])), O.bf16_to_f64(bits(x["v_raw"][0]))
         w = x["logits"][0].numpy().astype(np.float64)
-        lo = raw_lo(s)
-        seq = {"lo": lo, "q": x["q"][0].view(torch.int16).numpy().view(np.uint16),
-               "k_raw": x["k_raw"][0, lo:].view(torch.int16).numpy().view(np.uint16),
-               "v_raw": x["v_raw"][0, lo:].view(torch.int16).numpy().view(np.uint16),
-               "logits": w[lo:], "k_cmp": O.compress(kr, w, s.m), "v_cmp": O.compress(vr, w, s.m)}
+        if wl.mode == "decode":
+            lo = raw_lo(s)
+            seq = {"lo": lo, "q": bits(x["q"][0]), "k_raw": bits(x["k_raw"][0, lo:]),
+                   "v_raw": bits(x["v_raw"][0, lo:]), "logits": w[lo:],
+                   "k_cmp": O.compress(kr, w, s.m), "v_cmp": O.compress(vr, w, s.m)}
+        else:
+            seq = {"q": bits(x["q"][0]), "k_raw": bits(x["k_raw"][0]), "v_raw": bits(x["v_raw"][0]),
+                   "logits": w, "k_cmp": O.compress(kr, w, s.m), "v_cmp": O.compress(vr, w, s.m)}
         if s.kind == "csa":
             for n in ("qi_codes", "qi_scales", "ki_codes", "ki_scales"):
                 seq[n] = x[n][0].numpy()
         seqs.append((s, seq))
-    for _ in range(max(1, args.warmup)):
+
+    def one_step(i):
+        if wl.mode == "decode":
+            for s, seq in seqs:
+                oracle_decode_sequence(s, seq)
+            return 0.0
+        flops = 0.0
         for s, seq in seqs:
-            oracle_decode_sequence(s, seq)
+            row = i % s.Nq
+            t = s.q_pos0 + row
+            nv = O.visible_entries(t, s.m, s.E)
+            keys = nv + (t - max(0, t - s.W + 1) + 1 if s.W > 0 else 0)
+            if s.kind == "csa":
+                O.csa_layer_seq(seq["q"], seq["k_raw"], seq["v_raw"], seq["logits"],
+                                seq["qi_codes"], seq["qi_scales"], seq["ki_codes"],
+                                seq["ki_scales"], m=s.m, W=s.W, k=s.k, d_I=s.d_I,
+                                q_pos0=s.q_pos0, query_rows=[row], k_cmp=seq["k_cmp"],
+                                v_cmp=seq["v_cmp"])
+                keys = min(s.k, nv) + (keys - nv)
+                flops += 2 * s.H_I * s.d_I * nv
+            else:
+                O.hca_layer_seq(seq["q"], seq["k_raw"], seq["v_raw"], seq["logits"], m=s.m,
+                                W=s.W, q_pos0=s.q_pos0, query_rows=[row], k_cmp=seq["k_cmp"],
+                                v_cmp=seq["v_cmp"])
+            flops += 4 * s.H * s.d * keys
+        return flops
+
+    for i in range(min(max(1, args.warmup), 3)):
+        one_step(i)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        for s, seq in seqs:
-            oracle_decode_sequence(s, seq)
+    done, flops = 0, 0.0
+    for i in range(args.steps):
+        flops += one_step(i)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
     el = time.perf_counter() - t0
-    ms = el * 1e3 / args.steps
-    v = 1.0 / (ms * 1e-3)
-    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tok/s", "n_gpus": world,
+    ms = el * 1e3 / done
+    if wl.mode == "decode":
+        v, unit = done / el, "tok/s"
+        sample = f"{done} of {args.steps} steps x one {wl.name} sequence (budget {budget_s:.0f} s)"
+    else:
+        v, unit = flops / el / 1e12, "TFLOP/s"
+        sample = (f"{done} of {args.steps} steps x one query row of the {wl.name} chunk "
+                  f"(budget {budget_s:.0f} s)")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": wl.name, "description": wl.description,
-                                            "sample": "one sequence per step"},
-            "cpu_baseline": {"value": v, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{args.steps} steps x one {wl.name} sequence"},
-            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+                                            "sample": sample},
+            "cpu_baseline": {"value": v, "unit": unit, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
 def main(argv=None):
