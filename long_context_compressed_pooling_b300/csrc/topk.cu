@@ -402,7 +402,8 @@ __global__ void __launch_bounds__(NT) topk_kernel(const uint16_t* __restrict__ s
 // Rows of up to 32768 entries: one CTA of 1024 threads; thread t owns the contiguous keys
 // [t*KPT, t*KPT + KPT) in registers (KPT = 32), loaded with four 16-byte loads when the row is
 // 16-byte aligned. Max, near-max histogram, counts and the ordered write all run on registers;
-// one block scan orders the output because every thread's segment is contiguous.
+// one block scan of per-thread selection masks orders the output because every thread's segment
+// is contiguous.
 constexpr int kKPT = 32;
 __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const uint16_t* __restrict__ scores,
                                                                int Nq, int64_t q_pos0, int64_t E,
@@ -504,27 +505,31 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const uint16_t* _
     T = (hi_byte << 8) | (uint32_t)sh_bin;
     need_eq = (uint32_t)k - (above_hi + sh_above);
   }
-  // ---- ordered write: one scan over the threads' contiguous segments ----
-  uint32_t c_gt = 0, c_eq = 0;
+  // ---- ordered write: bit masks of the selected keys, one scan of their counts; only the set
+  // bits are visited ----
+  uint32_t gt = 0u, eq = 0u;
 #pragma unroll
   for (int j = 0; j < kKPT; ++j) {
-    c_gt += (seg0 + j < n) && key[j] > T;
-    c_eq += (seg0 + j < n) && key[j] == T;
+    const bool ok = seg0 + j < n;
+    gt |= (ok && key[j] > T) ? (1u << j) : 0u;
+    eq |= (ok && key[j] == T) ? (1u << j) : 0u;
   }
   uint32_t gb, eb, tg, te;
-  block_scan2(c_gt, c_eq, &gb, &eb, &tg, &te, wa, wb);
-#pragma unroll
-  for (int j = 0; j < kKPT; ++j) {
-    const uint32_t kk = key[j];
-    if (seg0 + j >= n) {
-    } else if (kk > T) {
-      const uint32_t pos = gb + min(eb, need_eq);
-      if (pos < (uint32_t)k) out[pos] = seg0 + j;
-      ++gb;
-    } else if (kk == T) {
-      if (eb < need_eq && gb + eb < (uint32_t)k) out[gb + eb] = seg0 + j;
-      ++eb;
-    }
+  block_scan2((uint32_t)__popc(gt), (uint32_t)__popc(eq), &gb, &eb, &tg, &te, wa, wb);
+  // this thread takes its lowest-index T-equal keys while the running count is below need_eq
+  uint32_t sel = gt;
+  for (uint32_t e = eq, take = eb < need_eq ? min(need_eq - eb, (uint32_t)__popc(eq)) : 0u;
+       take > 0; --take) {
+    const uint32_t low = e & (0u - e);
+    sel |= low;
+    e ^= low;
+  }
+  uint32_t pos = gb + min(eb, need_eq);
+  while (sel) {
+    const int j = __ffs(sel) - 1;
+    if (pos < (uint32_t)k) out[pos] = seg0 + j;
+    ++pos;
+    sel &= sel - 1u;
   }
   if (tid == 0) topk_cnt[row] = k;
 }
