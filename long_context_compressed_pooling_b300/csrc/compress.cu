@@ -64,21 +64,30 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restric
     const int64_t tok0 = b * N + j * m;
     const float* wl = logits + tok0;
 
+    const uint16_t* kp = k_raw + tok0 * D + c * 8;
+    const uint16_t* vp = v_raw + tok0 * D + c * 8;
+    // the first four rows are requested before the logits' maximum is known
+    uint4 kv[4], vv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (u < m) {
+        kv[u] = ldg_stream(kp + (int64_t)u * D);
+        vv[u] = ldg_stream(vp + (int64_t)u * D);
+      }
     float mx = -INFINITY;
     for (int i = 0; i < m; ++i) mx = fmaxf(mx, __ldg(wl + i));
 
     float acc_k[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float acc_v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float sum = 0.f;
-    const uint16_t* kp = k_raw + tok0 * D + c * 8;
-    const uint16_t* vp = v_raw + tok0 * D + c * 8;
     int i = 0;
     for (; i + 4 <= m; i += 4) {
-      uint4 kv[4], vv[4];
+      if (i > 0) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        kv[u] = ldg_stream(kp + (int64_t)(i + u) * D);
-        vv[u] = ldg_stream(vp + (int64_t)(i + u) * D);
+        for (int u = 0; u < 4; ++u) {
+          kv[u] = ldg_stream(kp + (int64_t)(i + u) * D);
+          vv[u] = ldg_stream(vp + (int64_t)(i + u) * D);
+        }
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
@@ -88,11 +97,22 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restric
         acc8(acc_v, vv[u], p);
       }
     }
-    for (; i < m; ++i) {
-      const float p = expf(__ldg(wl + i) - mx);
-      sum += p;
-      acc8(acc_k, ldg_stream(kp + (int64_t)i * D), p);
-      acc8(acc_v, ldg_stream(vp + (int64_t)i * D), p);
+    if (m < 4) {  // blocks shorter than four rows: all of them are already loaded
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (u < m) {
+          const float p = expf(__ldg(wl + u) - mx);
+          sum += p;
+          acc8(acc_k, kv[u], p);
+          acc8(acc_v, vv[u], p);
+        }
+    } else {
+      for (; i < m; ++i) {  // ragged tail of m >= 4 (not a multiple of 4)
+        const float p = expf(__ldg(wl + i) - mx);
+        sum += p;
+        acc8(acc_k, ldg_stream(kp + (int64_t)i * D), p);
+        acc8(acc_v, ldg_stream(vp + (int64_t)i * D), p);
+      }
     }
     const float inv = 1.0f / sum;
     const int64_t o = (b * E + j) * D + c * 8;
@@ -126,6 +146,20 @@ __global__ void __launch_bounds__(256) compress_large_kernel(const uint16_t* __r
   for (int64_t w = blockIdx.x; w < (int64_t)B * n_entries; w += gridDim.x) {
     const int64_t b = w / n_entries, j = j_begin + w % n_entries;
     const int64_t tok0 = b * N + j * m;
+    // The first kBatch of this thread's tokens (ts, ts + TS, ...) are loaded before the softmax
+    // weights are formed: their loads do not depend on the weights and overlap the reductions.
+    constexpr int kBatch = 8;
+    const uint16_t* kp = k_raw + tok0 * D + c * 8;
+    const uint16_t* vp = v_raw + tok0 * D + c * 8;
+    uint4 kv[kBatch], vv[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = ts + u * TS;
+      if (i < m) {
+        kv[u] = ldg_stream(kp + (int64_t)i * D);
+        vv[u] = ldg_stream(vp + (int64_t)i * D);
+      }
+    }
     // softmax weights of the block (m <= 256)
     const float x = tid < m ? __ldg(logits + tok0 + tid) : -INFINITY;
     float mx = x;
@@ -157,23 +191,15 @@ __global__ void __launch_bounds__(256) compress_large_kernel(const uint16_t* __r
 
     float acc_k[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     float acc_v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const uint16_t* kp = k_raw + tok0 * D + c * 8;
-    const uint16_t* vp = v_raw + tok0 * D + c * 8;
-    int i = ts;
-    for (; i + 3 * TS < m; i += 4 * TS) {
-      uint4 kv[4], vv[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        kv[u] = ldg_stream(kp + (int64_t)(i + u * TS) * D);
-        vv[u] = ldg_stream(vp + (int64_t)(i + u * TS) * D);
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        acc8(acc_k, kv[u], wexp[i + u * TS]);
-        acc8(acc_v, vv[u], wexp[i + u * TS]);
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = ts + u * TS;
+      if (i < m) {
+        acc8(acc_k, kv[u], wexp[i]);
+        acc8(acc_v, vv[u], wexp[i]);
       }
     }
-    for (; i < m; i += TS) {
+    for (int i = ts + kBatch * TS; i < m; i += TS) {  // blocks longer than kBatch * TS tokens
       acc8(acc_k, ldg_stream(kp + (int64_t)i * D), wexp[i]);
       acc8(acc_v, ldg_stream(vp + (int64_t)i * D), wexp[i]);
     }
