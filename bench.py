@@ -443,17 +443,54 @@ def run_e2e(wl, states, call, flush, K, dev, world, barrier):
     pinned host memory, runs the layer pair, and reads the outputs back."""
     import torch
     import torch.distributed as dist
-    ups, downs = [], []
+    # The step's new inputs travel packed in one pinned host buffer (one upload per step) into a
+    # device staging buffer, from which they are placed into the layer buffers on the device.
+    views, off = [], 0
     for s in wl.layers:
         d = states[s.kind]
         for name, view in step_inputs(s, d):
-            host = torch.empty(view.shape, dtype=view.dtype, pin_memory=True)
-            host.copy_(view)
-            ups.append((view, host))
-        o = d["out"]
+            nb = view.numel() * view.element_size()
+            views.append((view, off, nb))
+            off += (nb + 255) // 256 * 256
+    hbuf = torch.empty(off, dtype=torch.uint8, pin_memory=True)
+    dbuf = torch.empty(off, dtype=torch.uint8, device=dev)
+    for view, o, nb in views:
+        hbuf[o:o + nb].copy_(view.contiguous().view(-1).view(torch.uint8).cpu())
+    downs = []
+    for s in wl.layers:
+        o = states[s.kind]["out"]
         downs.append((o, torch.empty(o.shape, dtype=o.dtype, pin_memory=True)))
-    h2d = sum(h.numel() * h.element_size() for _, h in ups)
+    h2d = sum(nb for _, _, nb in views)
     d2h = sum(h.numel() * h.element_size() for _, h in downs)
+    ups = [(view, dbuf[o:o + nb].view(view.dtype).view(view.shape)) for view, o, nb in views]
+    def step():
+        dbuf.copy_(hbuf, non_blocking=True)
+        for dv, staged in ups:
+            dv.copy_(staged)
+        call()
+        for dv, h in downs:
+            h.copy_(dv, non_blocking=True)
+
+    # The step (uploads from pinned memory, the layer-pair call, the download) is captured once
+    # into a CUDA graph and replayed: every replay moves the bytes over the bus again, without the
+    # host's per-call launch cost. Eager launches if the capture is refused.
+    api = "csa_hca_layer_pair with one packed pinned-host upload and the download (CUDA graph replay)"
+    run = step
+    try:
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        g.replay()
+        torch.cuda.synchronize()
+        run = g.replay
+    except Exception as e:  # keep eager launches
+        api = "csa_hca_layer_pair with one packed pinned-host upload and the download (eager launches)"
+        print(f"# e2e graph capture unavailable, launching eagerly: {e}", file=sys.stderr)
     e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     barrier()
@@ -461,11 +498,7 @@ def run_e2e(wl, states, call, flush, K, dev, world, barrier):
     for i in range(K):
         flush.zero_()
         e0[i].record()
-        for dv, h in ups:
-            dv.copy_(h, non_blocking=True)
-        call()
-        for dv, h in downs:
-            h.copy_(dv, non_blocking=True)
+        run()
         e1[i].record()
     torch.cuda.synchronize()
     barrier()
@@ -477,7 +510,7 @@ def run_e2e(wl, states, call, flush, K, dev, world, barrier):
     else:
         v = sum(w["flops"] for w in work.values()) * world / (ms * 1e-3) / 1e12
     return {"value": v, "unit": unit, "ms_per_step": ms, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "api": "csa_hca_layer_pair (eager launches)"}
+            "d2h_bytes_per_step": d2h, "api": api}
 
 
 # ----------------------------------------------------------------------------------------------
