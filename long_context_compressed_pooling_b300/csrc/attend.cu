@@ -359,57 +359,95 @@ __global__ void __launch_bounds__(NW * 32) attend_kernel(const AttnParams p) {
 }
 
 // Combines workspace split-K partials: out = sum_s w_s O_s / sum_s w_s l_s, w_s = exp(m_s - max m).
-// One warp per (token, head); every split's (max, sum) is read once by one lane, the weights are
-// broadcast with shuffles, and the partial outputs are read eight splits at a time so that their
-// loads overlap.
+// One CTA of 8 warps per (token, head). Warp g takes splits g, g + 8, ... in batches of eight,
+// all of whose (max, sum) pairs and partial rows are loaded before any is used, and keeps its own
+// running maximum (an online merge); the eight warp results are combined through shared memory.
+// Every load of a batch is in flight at once, so a merge of up to 64 splits costs one round trip.
+constexpr int kMergeWarps = 8, kMergeBatch = 8;
 template <int D>
-__global__ void __launch_bounds__(32) merge_kernel(const float* __restrict__ ws_o,
-                                                  const float* __restrict__ ws_ml, int n_splits,
-                                                  int64_t tokens, int H, uint16_t* out,
-                                                  float* lse) {
+__global__ void __launch_bounds__(kMergeWarps * 32) merge_kernel(const float* __restrict__ ws_o,
+                                                                 const float* __restrict__ ws_ml,
+                                                                 int n_splits, int64_t tokens,
+                                                                 int H, uint16_t* out, float* lse) {
+  constexpr int PER = D / 32;  // 4 (D = 128) or 2 (D = 64) consecutive floats per lane
+  __shared__ float s_acc[kMergeWarps][D];
+  __shared__ float s_m[kMergeWarps], s_l[kMergeWarps];
   pdl_trigger();
   pdl_wait();
   const int64_t th = blockIdx.x;  // tok * H + h
-  const int lane = threadIdx.x;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t stride = tokens * H;
-  float M = -INFINITY;
-  for (int s = lane; s < n_splits; s += 32) M = fmaxf(M, ws_ml[(s * stride + th) * 2]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  constexpr int PER = D / 32;
-  float acc[PER];
+  float Mw = -INFINITY, Lw = 0.f, acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  float L = 0.f;
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < n_splits; s0 += 32) {
-      // lane s of this group of 32 splits computes w_s and w_s * l_s
-      const int sl = s0 + lane;
-      float w = 0.f, wl = 0.f;
-      if (sl < n_splits) {
-        const float2 ml = *reinterpret_cast<const float2*>(ws_ml + (sl * stride + th) * 2);
-        w = ml.x == -INFINITY ? 0.f : expf(ml.x - M);
-        wl = w * ml.y;
-      }
+  for (int s0 = w; s0 < n_splits; s0 += kMergeWarps * kMergeBatch) {
+    float2 ml[kMergeBatch];
+    float o[kMergeBatch][PER];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) wl += __shfl_xor_sync(0xffffffffu, wl, o);
-      L += wl;
-      const int ng = min(32, n_splits - s0);
-#pragma unroll 8
-      for (int x = 0; x < ng; ++x) {
-        const float wx = __shfl_sync(0xffffffffu, w, x);
-        const float* src = ws_o + ((int64_t)(s0 + x) * stride + th) * D + lane * PER;
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int sp = s0 + u * kMergeWarps;
+      ml[u] = make_float2(-INFINITY, 0.f);
 #pragma unroll
-        for (int i = 0; i < PER; ++i) acc[i] = fmaf(wx, src[i], acc[i]);
+      for (int i = 0; i < PER; ++i) o[u][i] = 0.f;
+      if (sp < n_splits) {
+        ml[u] = *reinterpret_cast<const float2*>(ws_ml + ((int64_t)sp * stride + th) * 2);
+        const float* src = ws_o + ((int64_t)sp * stride + th) * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src);
+          o[u][0] = v.x;
+          o[u][1] = v.y;
+          o[u][2] = v.z;
+          o[u][3] = v.w;
+        } else {
+          const float2 v = *reinterpret_cast<const float2*>(src);
+          o[u][0] = v.x;
+          o[u][1] = v.y;
+        }
       }
     }
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+    float bm = Mw;
 #pragma unroll
-  for (int i = 0; i < PER; i += 2)
-    *reinterpret_cast<uint32_t*>(out + th * D + lane * PER + i) =
-        pack_bf16x2(acc[i] * inv, acc[i + 1] * inv);
-  if (lse != nullptr && lane == 0) lse[th] = L > 0.f ? M + logf(L) : -INFINITY;
+    for (int u = 0; u < kMergeBatch; ++u) bm = fmaxf(bm, ml[u].x);
+    if (bm == -INFINITY) continue;
+    const float sc = Mw == -INFINITY ? 0.f : expf(Mw - bm);
+    Lw *= sc;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] *= sc;
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const float wt = ml[u].x == -INFINITY ? 0.f : expf(ml[u].x - bm);
+      Lw = fmaf(wt, ml[u].y, Lw);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(wt, o[u][i], acc[i]);
+    }
+    Mw = bm;
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) s_acc[w][lane * PER + i] = acc[i];
+  if (lane == 0) {
+    s_m[w] = Mw;
+    s_l[w] = Lw;
+  }
+  __syncthreads();
+  if (threadIdx.x < D / 2) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < kMergeWarps; ++g) M = fmaxf(M, s_m[g]);
+    float L = 0.f, a0 = 0.f, a1 = 0.f;
+    if (M != -INFINITY) {
+      const int d = 2 * threadIdx.x;
+#pragma unroll
+      for (int g = 0; g < kMergeWarps; ++g) {
+        const float wt = s_m[g] == -INFINITY ? 0.f : expf(s_m[g] - M);
+        L = fmaf(wt, s_l[g], L);
+        a0 = fmaf(wt, s_acc[g][d], a0);
+        a1 = fmaf(wt, s_acc[g][d + 1], a1);
+      }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    *reinterpret_cast<uint32_t*>(out + th * D + 2 * threadIdx.x) = pack_bf16x2(a0 * inv, a1 * inv);
+    if (lse != nullptr && threadIdx.x == 0) lse[th] = L > 0.f ? M + logf(L) : -INFINITY;
+  }
 }
 
 struct SplitPlan {
@@ -472,8 +510,8 @@ cudaError_t launch_attend_t(AttnParams prm, int groups, cudaStream_t stream) {
   }
   if (e != cudaSuccess || prm.n_splits == 1 || prm.cluster_merge) return e;
   ProfScope prof(stream, "lse_merge");
-  return launch_ex(merge_kernel<D>, dim3((unsigned)((int64_t)prm.tokens * prm.H)), dim3(32), 0,
-                   stream, 1, (const float*)prm.ws_o, (const float*)prm.ws_ml, prm.n_splits,
+  return launch_ex(merge_kernel<D>, dim3((unsigned)((int64_t)prm.tokens * prm.H)),
+                   dim3(kMergeWarps * 32), 0, stream, 1, (const float*)prm.ws_o, (const float*)prm.ws_ml, prm.n_splits,
                    (int64_t)prm.tokens, prm.H, prm.out, prm.lse);
 }
 
@@ -503,10 +541,10 @@ cudaError_t launch_merge(int D, const float* ws_o, const float* ws_ml, int n_spl
   ProfScope prof(stream, "lse_merge");
   const dim3 grid((unsigned)((int64_t)tokens * H));
   if (D == 128)
-    return launch_ex(merge_kernel<128>, grid, dim3(32), 0, stream, 1, ws_o, ws_ml, n_splits,
-                     (int64_t)tokens, H, out, lse);
-  return launch_ex(merge_kernel<64>, grid, dim3(32), 0, stream, 1, ws_o, ws_ml, n_splits,
-                   (int64_t)tokens, H, out, lse);
+    return launch_ex(merge_kernel<128>, grid, dim3(kMergeWarps * 32), 0, stream, 1, ws_o, ws_ml,
+                     n_splits, (int64_t)tokens, H, out, lse);
+  return launch_ex(merge_kernel<64>, grid, dim3(kMergeWarps * 32), 0, stream, 1, ws_o, ws_ml,
+                   n_splits, (int64_t)tokens, H, out, lse);
 }
 }  // namespace
 

@@ -403,6 +403,10 @@ CSA_DEV void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
 }
+// The two halves of cluster_sync: arrive (release) and wait (acquire), with independent work
+// between them.
+CSA_DEV void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+CSA_DEV void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 // Reads a 32-bit word at the same shared-memory offset in CTA `cta` of this cluster.
 CSA_DEV uint32_t dsmem_ld_u32(const void* local_ptr, uint32_t cta) {
   uint32_t ra, v;

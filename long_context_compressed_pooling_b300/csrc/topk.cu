@@ -7,16 +7,16 @@
 // select (high byte, then low byte) followed by an ordered compaction: every key above the
 // threshold T, plus the lowest-index keys equal to T until k are taken.
 //
-// One thread-block cluster per query row. The row is split into C contiguous chunks, one per
-// CTA, staged in shared memory. Each CTA builds its chunk's 256-bin histograms with
-// warp-aggregated shared atomics; the cluster sums them through distributed shared memory
-// after a hardware cluster barrier, and every CTA derives the same threshold. For the
-// compaction each CTA counts its keys above / equal to T, reads the counts of the lower-ranked
-// CTAs of its cluster, and writes its selected indices at their final, ascending positions.
-// Rows of up to 32768 entries (decode at 128K context, every prefill row) take one CTA of 1024
-// threads holding the row in registers (32 contiguous keys per thread) and no cluster phase at
-// all; longer rows (decode at 1M context) use clusters of up to 16 CTAs. No grid-wide
-// synchronisation and no spin waits are involved.
+// One CTA or thread-block cluster per query row, holding the row in registers: CTA rank r of
+// a cluster of C owns a contiguous chunk of NT x KPT keys, every thread KPT contiguous keys of
+// it. The shape is picked per launch: rows of up to 32768 keys with enough rows to fill the GPU
+// (prefill) take one CTA of 1024 threads x 32 keys; few rows (decode) are spread over clusters
+// of 256-1024-thread CTAs so that the grid covers the SMs (a 32768-key row: 8 CTAs of 4096
+// keys; a 262144-key row at 1M context: 16 CTAs of 16384). The cluster exchanges only the CTA
+// maxima, 256-bin histograms and selected-key counts through distributed shared memory after
+// hardware cluster barriers; every CTA derives the same threshold and writes its selected
+// indices at their final, ascending positions. Rows longer than 16 x 32768 keys stage their
+// chunks in shared memory instead. No grid-wide synchronisation and no spin waits are involved.
 //
 // Fast threshold: scores sit on the BF16 grid, so most of a row's top k lie within 255 grid
 // steps of the row maximum. One histogram of (max - key) over those 255 steps finds T in a
@@ -30,9 +30,7 @@ namespace csa {
 namespace {
 
 constexpr int kClusterThreads = 256;   // threads per CTA of a multi-CTA (cluster) row
-constexpr int kRowThreads = 1024;      // threads of a one-CTA row
 constexpr int kMaxChunkKeys = 16384;   // keys one cluster CTA stages in shared memory (32 KB)
-constexpr int kMaxRowKeys = 32768;     // keys a one-CTA row stages in shared memory (64 KB)
 
 CSA_DEV uint32_t order_key(uint32_t bits) {
   if (bits == 0x8000u) bits = 0u;  // -0 counts as +0
@@ -399,47 +397,52 @@ __global__ void __launch_bounds__(NT) topk_kernel(const uint16_t* __restrict__ s
 }
 
 
-// Rows of up to 32768 entries: one CTA of 1024 threads; thread t owns the contiguous keys
-// [t*KPT, t*KPT + KPT) in registers (KPT = 32), loaded with four 16-byte loads when the row is
+// Register-resident selection. A row is split over a cluster of C CTAs (C = 1 for rows that
+// fit one CTA); CTA rank r owns the contiguous keys [r*NT*KPT, (r+1)*NT*KPT) and thread t of it
+// the KPT keys starting at t*KPT inside that range, loaded with 16-byte loads when the row is
 // 16-byte aligned. Max, near-max histogram, counts and the ordered write all run on registers;
-// one block scan of per-thread selection masks orders the output because every thread's segment
-// is contiguous.
-constexpr int kKPT = 32;
-__global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const uint16_t* __restrict__ scores,
-                                                               int Nq, int64_t q_pos0, int64_t E,
-                                                               int m, int k,
-                                                               int32_t* __restrict__ topk_idx,
-                                                               int32_t* __restrict__ topk_cnt) {
-  constexpr int NW = kRowThreads / 32;
+// the cluster exchanges only its CTAs' maxima, histograms and counts through distributed shared
+// memory (three hardware cluster barriers), and one block scan of per-thread selection masks
+// orders the output because every thread's keys are contiguous and ranks follow key order.
+template <int NT, int KPT>
+__global__ void __launch_bounds__(NT) topk_reg_kernel(const uint16_t* __restrict__ scores, int Nq,
+                                                      int64_t q_pos0, int64_t E, int m, int k,
+                                                      int32_t* __restrict__ topk_idx,
+                                                      int32_t* __restrict__ topk_cnt) {
+  constexpr int NW = NT / 32;
   __shared__ uint32_t whist[NW * 256];
-  __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist1[256], hist2[256], gsum[256];
   __shared__ uint32_t wmax[NW];
   __shared__ uint32_t wa[33], wb[33];
+  __shared__ uint32_t cta_val[3];  // this CTA's maximum, keys above T, keys equal to T
+  __shared__ uint32_t bcast[2];
   __shared__ int sh_bin;
   __shared__ uint32_t sh_above;
   pdl_trigger();
   pdl_wait();
-  const int64_t row = blockIdx.x;
+  const uint32_t C = cluster_nctarank();
+  const uint32_t rank = cluster_ctarank();
+  const int64_t row = blockIdx.x / C;
   const int64_t t = q_pos0 + (row % Nq);
   const int n = (int)max((int64_t)0, min(E, (t + 1) / m));
   const uint16_t* src = scores + row * E;
   int32_t* out = topk_idx + row * (int64_t)k;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  if (n <= k) {
-    for (int r = tid; r < k; r += kRowThreads) out[r] = (r < n) ? r : -1;
-    if (tid == 0) topk_cnt[row] = n;
+  if (n <= k) {  // uniform over the cluster
+    for (int r = (int)rank * NT + tid; r < k; r += (int)C * NT) out[r] = (r < n) ? r : -1;
+    if (rank == 0 && tid == 0) topk_cnt[row] = n;
     return;
   }
-  // ---- keys of this thread's segment -----------------------------------------------------------
-  const int seg0 = tid * kKPT;
-  uint32_t key[kKPT];
-  const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) && seg0 + kKPT <= n;
+  // ---- keys of this thread ---------------------------------------------------------------------
+  const int seg0 = ((int)rank * NT + tid) * KPT;
+  uint32_t key[KPT];
+  const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) && seg0 + KPT <= n;
   if (vec) {
-    uint4 v[kKPT / 8];
+    uint4 v[KPT / 8];
 #pragma unroll
-    for (int q = 0; q < kKPT / 8; ++q) v[q] = __ldg(reinterpret_cast<const uint4*>(src + seg0) + q);
+    for (int q = 0; q < KPT / 8; ++q) v[q] = __ldg(reinterpret_cast<const uint4*>(src + seg0) + q);
 #pragma unroll
-    for (int q = 0; q < kKPT / 8; ++q) {
+    for (int q = 0; q < KPT / 8; ++q) {
       const uint32_t u[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
@@ -449,58 +452,77 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const uint16_t* _
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < kKPT; ++j) key[j] = seg0 + j < n ? order_key(src[seg0 + j]) : 0u;
+    for (int j = 0; j < KPT; ++j) key[j] = seg0 + j < n ? order_key(src[seg0 + j]) : 0u;
   }
   // slots past the row end hold 0 and are excluded by index, never by value
   // ---- row maximum ----
   uint32_t mx = 0;
 #pragma unroll
-  for (int j = 0; j < kKPT; ++j) mx = max(mx, key[j]);
+  for (int j = 0; j < KPT; ++j) mx = max(mx, key[j]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (lane == 0) wmax[w] = mx;
-  for (int q = tid; q < NW * 256; q += kRowThreads) whist[q] = 0u;
+  for (int q = tid; q < NW * 256; q += NT) whist[q] = 0u;
   __syncthreads();
   uint32_t row_max = 0;
 #pragma unroll
   for (int q = 0; q < NW; ++q) row_max = max(row_max, wmax[q]);
+  if (C > 1) {
+    if (tid == 0) cta_val[0] = row_max;
+    cluster_sync();
+    if (w == 0) {
+      uint32_t v = (uint32_t)lane < C ? dsmem_ld_u32(&cta_val[0], (uint32_t)lane) : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+      if (lane == 0) bcast[0] = v;
+    }
+    __syncthreads();
+    row_max = bcast[0];
+  }
   // ---- near-max histogram (one bin per BF16 step below the maximum) ----
   uint32_t* wh = whist + w * 256;
 #pragma unroll
-  for (int j = 0; j < kKPT; ++j) {
+  for (int j = 0; j < KPT; ++j) {
     const uint32_t dd = row_max - key[j];
     if (dd < 255u && seg0 + j < n) atomicAdd(&wh[dd], 1u);
   }
   __syncthreads();
-  reduce_warp_hists<NW>(whist, hist);
-  __syncthreads();
-  select_prefix(hist, (uint32_t)k, &sh_bin, &sh_above);
+  auto sum_hist = [&](uint32_t* hist) {  // per-warp histograms -> hist -> cluster sum in gsum
+    reduce_warp_hists<NW>(whist, hist);
+    __syncthreads();
+    for (int q = tid; q < NW * 256; q += NT) whist[q] = 0u;
+    if (C > 1) {
+      cluster_sync();
+      for (int q = tid; q < 256; q += NT) gsum[q] = cluster_sum(&hist[q], C);
+    } else {
+      for (int q = tid; q < 256; q += NT) gsum[q] = hist[q];
+    }
+    __syncthreads();
+  };
+  sum_hist(hist1);
+  select_prefix(gsum, (uint32_t)k, &sh_bin, &sh_above);
   __syncthreads();
   uint32_t T, need_eq;
   if (sh_bin >= 0) {
     T = row_max - (uint32_t)sh_bin;
     need_eq = (uint32_t)k - sh_above;
   } else {
-    // fallback: exact two-digit radix select on the registers
-    for (int q = tid; q < NW * 256; q += kRowThreads) whist[q] = 0u;
-    __syncthreads();
+    // fallback: exact two-digit radix select on the registers (hist2, then hist1 again: every
+    // CTA of the cluster has read hist1 before it arrives at the digit-1 cluster barrier)
 #pragma unroll
-    for (int j = 0; j < kKPT; ++j)
+    for (int j = 0; j < KPT; ++j)
       if (seg0 + j < n) atomicAdd(&wh[key[j] >> 8], 1u);
     __syncthreads();
-    reduce_warp_hists<NW>(whist, hist);
-    __syncthreads();
-    for (int q = tid; q < NW * 256; q += kRowThreads) whist[q] = 0u;
-    select_bin(hist, (uint32_t)k, &sh_bin, &sh_above);
+    sum_hist(hist2);
+    select_bin(gsum, (uint32_t)k, &sh_bin, &sh_above);
     __syncthreads();
     const uint32_t hi_byte = (uint32_t)sh_bin, above_hi = sh_above;
 #pragma unroll
-    for (int j = 0; j < kKPT; ++j)
+    for (int j = 0; j < KPT; ++j)
       if (seg0 + j < n && (key[j] >> 8) == hi_byte) atomicAdd(&wh[key[j] & 0xFFu], 1u);
     __syncthreads();
-    reduce_warp_hists<NW>(whist, hist);
-    __syncthreads();
-    select_bin(hist, (uint32_t)k - above_hi, &sh_bin, &sh_above);
+    sum_hist(hist1);
+    select_bin(gsum, (uint32_t)k - above_hi, &sh_bin, &sh_above);
     __syncthreads();
     T = (hi_byte << 8) | (uint32_t)sh_bin;
     need_eq = (uint32_t)k - (above_hi + sh_above);
@@ -509,13 +531,37 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const uint16_t* _
   // bits are visited ----
   uint32_t gt = 0u, eq = 0u;
 #pragma unroll
-  for (int j = 0; j < kKPT; ++j) {
+  for (int j = 0; j < KPT; ++j) {
     const bool ok = seg0 + j < n;
     gt |= (ok && key[j] > T) ? (1u << j) : 0u;
     eq |= (ok && key[j] == T) ? (1u << j) : 0u;
   }
   uint32_t gb, eb, tg, te;
   block_scan2((uint32_t)__popc(gt), (uint32_t)__popc(eq), &gb, &eb, &tg, &te, wa, wb);
+  if (C > 1) {  // keys of the lower-ranked CTAs of this row
+    if (tid == 0) {
+      cta_val[1] = tg;
+      cta_val[2] = te;
+    }
+    cluster_sync();
+    if (w == 0) {
+      uint32_t a = (uint32_t)lane < rank ? dsmem_ld_u32(&cta_val[1], (uint32_t)lane) : 0u;
+      uint32_t b = (uint32_t)lane < rank ? dsmem_ld_u32(&cta_val[2], (uint32_t)lane) : 0u;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        a += __shfl_xor_sync(0xffffffffu, a, o);
+        b += __shfl_xor_sync(0xffffffffu, b, o);
+      }
+      if (lane == 0) {
+        bcast[0] = a;
+        bcast[1] = b;
+      }
+    }
+    cluster_arrive();  // this CTA's remote reads are done; it waits for the others' before exit
+    __syncthreads();
+    gb += bcast[0];
+    eb += bcast[1];
+  }
   // this thread takes its lowest-index T-equal keys while the running count is below need_eq
   uint32_t sel = gt;
   for (uint32_t e = eq, take = eb < need_eq ? min(need_eq - eb, (uint32_t)__popc(eq)) : 0u;
@@ -531,15 +577,100 @@ __global__ void __launch_bounds__(kRowThreads) topk_row_kernel(const uint16_t* _
     ++pos;
     sel &= sel - 1u;
   }
-  if (tid == 0) topk_cnt[row] = k;
+  if (rank == 0 && tid == 0) topk_cnt[row] = k;
+  if (C > 1) cluster_wait();  // no CTA leaves while another may still read its shared memory
 }
 
-int pick_cluster(int64_t rows, int64_t n_max) {
-  if (n_max <= kMaxRowKeys) return 1;
-  int C = 1;
-  while (C < 16 && rows * C < kNumSMs && n_max / (2 * C) >= 2048) C <<= 1;
-  while (C < 16 && (n_max + C - 1) / C > kMaxChunkKeys) C <<= 1;
-  return C;
+// Register-resident shapes: keys per CTA = threads x keys per thread.
+struct RegShape {
+  int nt, kpt;
+  int chunk() const { return nt * kpt; }
+};
+constexpr RegShape kRegShapes[] = {{256, 16}, {512, 16}, {1024, 16}, {1024, 32}};
+constexpr int kMaxRegCluster = 16;
+
+template <int NT, int KPT>
+cudaError_t launch_reg(const uint16_t* scores, int Nq, int64_t q_pos0, int64_t E, int m, int k,
+                       int32_t* topk_idx, int32_t* topk_cnt, int64_t rows, int C,
+                       cudaStream_t stream) {
+  auto kern = topk_reg_kernel<NT, KPT>;
+  if (C > 8) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  ProfScope prof(stream, "topk");
+  return launch_ex(kern, dim3((unsigned)(rows * C)), dim3(NT), 0, stream, (unsigned)C, scores,
+                   Nq, q_pos0, E, m, k, topk_idx, topk_cnt);
+}
+
+// Whether clusters of C CTAs of this shape can be resident (sizes above 8 are non-portable).
+template <int NT, int KPT>
+bool reg_cluster_fits(int C) {
+  if (C <= 8) return true;
+  auto kern = topk_reg_kernel<NT, KPT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)C);
+  cfg.blockDim = dim3(NT);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int nclusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return nclusters > 0;
+}
+
+bool reg_fits_query(int shape, int C) {
+  switch (shape) {
+    case 0: return reg_cluster_fits<256, 16>(C);
+    case 1: return reg_cluster_fits<512, 16>(C);
+    case 2: return reg_cluster_fits<1024, 16>(C);
+    default: return reg_cluster_fits<1024, 32>(C);
+  }
+}
+
+// Answers are cached per (shape, cluster size): 0 unknown, 1 fits, 2 does not.
+bool reg_fits(int shape, int C) {
+  static volatile int8_t cache[4][kMaxRegCluster + 1] = {};
+  if (C <= 8) return true;
+  if (cache[shape][C] == 0) cache[shape][C] = reg_fits_query(shape, C) ? 1 : 2;
+  return cache[shape][C] == 1;
+}
+
+// Picks the register-resident shape and cluster size for rows of up to n_max keys: one CTA of
+// 32768 keys per row when there are enough rows to fill the GPU; otherwise the smallest chunk
+// whose cluster (at most 16 CTAs) covers the row while the grid stays within two CTAs per SM.
+// Returns false when no shape covers the row (more than 16 x 32768 keys).
+bool pick_reg(int64_t rows, int64_t n_max, int* shape, int* C) {
+  constexpr int nshapes = (int)(sizeof(kRegShapes) / sizeof(kRegShapes[0]));
+  if (n_max <= kRegShapes[nshapes - 1].chunk() && rows >= kNumSMs) {
+    *shape = nshapes - 1;
+    *C = 1;
+    return true;
+  }
+  int best = -1, best_c = 0;
+  for (int i = 0; i < nshapes; ++i) {
+    const int64_t c = (n_max + kRegShapes[i].chunk() - 1) / kRegShapes[i].chunk();
+    if (c > kMaxRegCluster || !reg_fits(i, (int)max((int64_t)1, c))) continue;
+    best = i;
+    best_c = (int)max((int64_t)1, c);
+    if (rows * best_c <= 2 * kNumSMs) break;
+  }
+  if (best < 0) return false;
+  *shape = best;
+  *C = best_c;
+  return true;
 }
 
 template <int NT>
@@ -589,14 +720,27 @@ cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, i
   if (rows <= 0) return cudaSuccess;
   int64_t n_max = min(E, (q_pos0 + Nq) / m);
   if (n_max < 0) n_max = 0;
-  const int C = pick_cluster(rows, n_max);
-  if (C == 1) {
-    ProfScope prof(stream, "topk");
-    return launch_ex(topk_row_kernel, dim3((unsigned)rows), dim3(kRowThreads), 0, stream, 1,
-                     scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt);
+  int shape = 0, C = 1;
+  if (pick_reg(rows, n_max, &shape, &C)) {
+    switch (shape) {
+      case 0:
+        return launch_reg<256, 16>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C, stream);
+      case 1:
+        return launch_reg<512, 16>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C, stream);
+      case 2:
+        return launch_reg<1024, 16>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
+                                    stream);
+      default:
+        return launch_reg<1024, 32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
+                                    stream);
+    }
   }
+  // rows longer than 16 x 32768 keys: clusters of up to 16 CTAs staging their chunks in
+  // shared memory
+  int Cs = 1;
+  while (Cs < 16 && (n_max + Cs - 1) / Cs > kMaxChunkKeys) Cs <<= 1;
   return launch_topk_t<kClusterThreads>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows,
-                                        n_max, C, kMaxChunkKeys, stream);
+                                        n_max, Cs, kMaxChunkKeys, stream);
 }
 
 }  // namespace csa

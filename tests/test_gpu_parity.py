@@ -112,7 +112,13 @@ def _tie_scores(rng, shape):
                                              (5000, 2, 19999, 4, 700), (60000, 1, 239999, 4, 300),
                                              (1000, 1, 3999, 4, 999),
                                              (6000, 150, 23850, 4, 100),   # one CTA, 2 rounds
-                                             (300000, 1, 1199999, 4, 2048)])  # unstaged chunks
+                                             (300000, 1, 1199999, 4, 2048),  # cluster of 10
+                                             (600000, 1, 2399999, 4, 2048),  # staged chunks
+                                             (32768, 1, 131071, 4, 512),     # cluster of 8
+                                             (262144, 1, 1048575, 4, 2048),  # cluster of 16
+                                             (33001, 1, 132007, 4, 400),     # odd rows, C = 9
+                                             (40000, 5, 159000, 4, 300),     # C = 10, 5 rows
+                                             (5000, 3, 4094, 1, 40)])  # CTAs past the row end
 def test_topk_ties_and_negative_scores(E, Nq, q_pos0, m, k):
     rng = np.random.default_rng(E + k)
     sc_np = _tie_scores(rng, (2, Nq, E))
@@ -137,6 +143,8 @@ ATT_CASES = [
     (2, 3, 700, 703, 16, 64, 4, 5, 100),     # k above visible, short window
     (1, 2, 4000, 4096, 128, 128, 4, 128, 40),  # two head groups
     (16, 1, 4095, 4096, 64, 128, 4, 128, 512),  # decode batch 16: 10-CTA cluster merge
+    (1, 1, 32767, 32768, 64, 128, 4, 128, 8192),  # 65 splits: two merge batches per warp
+    (1, 1, 32767, 32768, 16, 64, 4, 64, 4096),    # d = 64, workspace merge
 ]
 
 
