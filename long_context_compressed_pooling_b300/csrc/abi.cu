@@ -383,6 +383,9 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
       return CSA_ERR_CUDA;
     AttendArgs a{h->q, h->k_cmp, h->v_cmp, nullptr, nullptr, h->k_raw, h->v_raw, h->out, h->lse,
                  E, h->N, h->q_pos0, 0, h->m, h->W, h->B, h->Nq, h->H, h->d};
+    // The compress launch just above is the attention's predecessor; it waits for its own
+    // predecessor before letting the attention start, so the entries below j0 are complete.
+    a.fresh_from = j0;
     if (launch_attend(a, hca_max_keys(E, h->m, h->N, h->W), ws_h, status, sh) != cudaSuccess)
       return CSA_ERR_CUDA;
   }

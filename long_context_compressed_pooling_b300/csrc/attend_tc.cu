@@ -78,6 +78,7 @@ struct TcParams {
   float* ws_o;   // [n_splits, tokens, H, D] unnormalised partial outputs (workspace merge)
   float* ws_ml;  // [n_splits, tokens, H, 2] reference maximum and sum
   int64_t E, N, q_pos0;
+  int64_t fresh_from;  // dense: entries below it may be read before the predecessor completes
   int k, m, W, Nq, H, n_splits, tokens;
   int sparse;
   int cluster_merge;
@@ -156,7 +157,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_wait();  // top-k lists and entries come from the preceding kernels
+  // Top-k lists come from the preceding kernels; a dense launch defers the wait until its
+  // loaders reach an entry at or above fresh_from (raw window rows and Q are inputs).
+  const bool early = !p.sparse && p.fresh_from > 0;
+  if (!early) pdl_wait();
 
   int64_t n_sel;
   if (p.sparse) {
@@ -195,8 +199,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
     const int wl = warp - kLoadWarp0;
     const int h = lane >> 4, cc = lane & 15;
     constexpr long long kRawBit = 1LL << 62;
+    bool waited = !early;
     for (int it = 0; it < nloc; ++it) {
       const int s = it % kStages;
+      const int64_t k0 = (int64_t)(c_begin + it) * kKC;
+      if (!waited && k0 < n_sel && k0 + kKC > p.fresh_from) {
+        pdl_wait();
+        waited = true;
+      }
       if (it >= kStages &&
           !mbar_wait_warp(&kv_empty[s], (uint32_t)(it / kStages - 1) & 1u, p.status))
         break;
@@ -445,6 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
   }
 
   __syncthreads();
+  if (early) pdl_wait();  // outputs are written only once the predecessor has completed
   // Combine the two key halves: warp (q, hf) produces output columns [64 hf, 64 hf + 64) of rows
   // r0 and r0 + 8 from both O accumulators, weighted to the common maximum.
   const bool smx = warp < kSoftmaxWarps;
@@ -615,6 +626,7 @@ cudaError_t launch_attend_tc(const AttendArgs& a, int n_splits, int cluster, flo
   prm.E = a.E;
   prm.N = a.N;
   prm.q_pos0 = a.q_pos0;
+  prm.fresh_from = a.fresh_from;
   prm.k = a.k;
   prm.m = a.m;
   prm.W = a.W;

@@ -51,8 +51,10 @@ __global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restric
                                                        int64_t N, int m, int64_t j_begin,
                                                        int64_t n_entries) {
   constexpr int D = CH * 8;
-  pdl_trigger();
+  // wait before letting the successor start: a successor that reads entries this launch does
+  // not write, before its own wait, then also sees every earlier kernel complete
   pdl_wait();
+  pdl_trigger();
   const int64_t E = N / m;
   const int64_t total = (int64_t)B * n_entries * CH;
   for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < total;
@@ -141,8 +143,8 @@ __global__ void __launch_bounds__(256) compress_large_kernel(const uint16_t* __r
   const int tid = threadIdx.x;
   const int c = tid % CH, ts = tid / CH;
   const int64_t E = N / m;
+  pdl_wait();  // before the trigger, as in compress_kernel
   pdl_trigger();
-  pdl_wait();
   for (int64_t w = blockIdx.x; w < (int64_t)B * n_entries; w += gridDim.x) {
     const int64_t b = w / n_entries, j = j_begin + w % n_entries;
     const int64_t tok0 = b * N + j * m;

@@ -82,6 +82,10 @@ struct AttendArgs {
   float* lse;
   int64_t E, N, q_pos0;
   int k, m, W, B, Nq, H, d;
+  // Dense attention only: entries [0, fresh_from) are inputs of this launch, and every kernel
+  // before the one that precedes it on the stream has completed, so they may be read before
+  // waiting for that predecessor; entries from fresh_from on may be its output. 0: wait first.
+  int64_t fresh_from = 0;
 };
 int plan_attend_splits(int tokens, int H, int d, int64_t max_keys);
 size_t attend_workspace_bytes(int tokens, int H, int d, int64_t max_keys);
