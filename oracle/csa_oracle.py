@@ -31,6 +31,10 @@ the design notes of the repository):
      ascending, padded with -1.
   R8 logits are q.k with no extra scale (1/sqrt(d) is folded into Q).
   R9 an empty attention set (W = 0 and no visible entry) gives output 0 and LSE = -inf.
+  R14 the indexer's own keys are pooled from per-token index-key rows with the KV entries'
+     block pooling (R2), rounded to bf16, and converted to MX FP4 with the OCP MX v1.0 rule
+     (block scale 2^(floor(log2 amax) - 2), elements rounded to nearest-even on the e2m1 grid,
+     saturating at 6).
 
 Everything is plain numpy in float64; bf16 tensors arrive as uint16 bit arrays.
 """
@@ -98,6 +102,63 @@ def mx_fp4_dequant(codes, scales, n: int) -> np.ndarray:
     return v * sc
 
 
+def f64_to_bf16_rne_any(x) -> np.ndarray:
+    """Round arbitrary finite float64 values straight to bf16 bits (8 significant bits) with
+    round-to-nearest, ties-to-even; one rounding, no detour through fp32. Values must be 0 or
+    at least 2^-126 in magnitude (no bf16 subnormals) and below the bf16 maximum."""
+    x = np.asarray(x, dtype=np.float64)
+    f, k = np.frexp(x)                      # x = f * 2^k, 0.5 <= |f| < 1
+    if np.any((x != 0) & (np.abs(x) < 2.0 ** -126)):
+        raise ValueError("bf16 subnormal result")
+    r = np.ldexp(np.rint(np.ldexp(f, 8)), k - 8)  # np.rint rounds half to even
+    r = r + 0.0                              # -0 -> +0
+    f32 = r.astype(np.float32)
+    if not np.all(np.isfinite(f32)):
+        raise ValueError("bf16 overflow")
+    return (f32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+# MX FP4 conversion (OCP Microscaling Formats v1.0, section 6.3, "conversion to MX": the shared
+# scale of a 32-element block is X = 2^(floor(log2(max_i |V_i|)) - emax_elem), with emax_elem = 2
+# for FP4 E2M1 (largest normal 6 = 1.5 * 2^2); each element is V_i / X rounded to the element
+# format with round-to-nearest-even, magnitudes above the largest normal clamped to it).
+E2M1_EMAX = 2
+
+
+def e2m1_round(y) -> np.ndarray:
+    """float64 -> 4-bit e2m1 codes: the nearest of the 8 magnitudes, a tie going to the even
+    code (mantissa bit 0), magnitudes beyond 6 saturating to 6; the sign bit copies the sign of
+    the input (a negative value that rounds to zero gives code 8, -0)."""
+    y = np.asarray(y, dtype=np.float64)
+    a = np.minimum(np.abs(y), E2M1_MAGNITUDES[-1])
+    dist = np.abs(a[..., None] - E2M1_MAGNITUDES)          # [..., 8]
+    best = dist.min(axis=-1, keepdims=True)
+    cand = dist == best                                     # one or two nearest magnitudes
+    even = cand & (np.arange(8) % 2 == 0)
+    idx = np.where(even.any(axis=-1), even.argmax(axis=-1), cand.argmax(axis=-1))
+    sign = np.signbit(y).astype(np.int64)
+    return (idx + 8 * sign).astype(np.uint8)
+
+
+def mx_fp4_quantize(x) -> Tuple[np.ndarray, np.ndarray]:
+    """x [..., n] float64, n % 32 == 0 -> (packed e2m1 codes [..., n/2] uint8, UE8M0 scale bytes
+    [..., n/32] uint8); MX FP4 conversion as stated above. An all-zero block gets the smallest
+    scale (byte 0, 2^-127) and zero codes; the exponent is clamped to the UE8M0 range
+    [-127, 127]."""
+    x = np.asarray(x, dtype=np.float64)
+    n = x.shape[-1]
+    assert n % MX_BLOCK == 0
+    blk = x.reshape(x.shape[:-1] + (n // MX_BLOCK, MX_BLOCK))
+    amax = np.abs(blk).max(axis=-1)
+    _, k = np.frexp(amax)                                   # amax = f * 2^k, f in [0.5, 1)
+    e = np.where(amax > 0, (k - 1) - E2M1_EMAX, -127)       # floor(log2(amax)) - emax_elem
+    e = np.clip(e, -127, 127)
+    y = blk / np.ldexp(1.0, e)[..., None]
+    codes = e2m1_round(y).reshape(x.shape)
+    packed = (codes[..., 0::2] | (codes[..., 1::2] << np.uint8(4))).astype(np.uint8)
+    return packed, (e + 127).astype(np.uint8)
+
+
 # ----------------------------------------------------------------------------------------------
 # compression (CSA m=4, HCA m=128)
 # ----------------------------------------------------------------------------------------------
@@ -121,6 +182,19 @@ def compress(raw: np.ndarray, logits: np.ndarray, m: int) -> np.ndarray:
     E = entry_count(N, m)
     p = pooling_weights(np.asarray(logits, dtype=np.float64)[: E * m].reshape(E, m))
     return np.einsum("ji,jid->jd", p, raw[: E * m].reshape(E, m, d))
+
+
+def index_key_entries(xi_bits, logits, m: int):
+    """The Lightning Indexer's own compressed keys (Lighthouse 八.7 lists them beside the CSA and
+    HCA entries; 9fzt.com item 4 puts the indexer's QK path in FP4): one sequence's raw index-key
+    rows [N, d_I] (bf16 bits) are pooled with the block-pooling operator of the KV entries (R2,
+    the same per-token logits), each pooled value is rounded to bf16, and every entry is
+    converted to MX FP4 (R14). Returns (codes [E, d_I/2], scales [E, d_I/32], pooled bf16 bits
+    [E, d_I], pooled float64 [E, d_I])."""
+    pooled = compress(bf16_to_f64(xi_bits), logits, m)
+    pb = f64_to_bf16_rne_any(pooled)
+    codes, scales = mx_fp4_quantize(bf16_to_f64(pb))
+    return codes, scales, pb, pooled
 
 
 # ----------------------------------------------------------------------------------------------

@@ -367,3 +367,119 @@ def test_csa_layer_topk_visible_and_sorted():
         sel = res["idx"][t][:cnt]
         assert np.all(np.diff(sel) > 0) and (cnt == 0 or sel[-1] < n_vis)
         assert np.all(res["idx"][t][cnt:] == -1)
+
+
+# ---------------------------------------------------------------------------------------------
+# R14: the indexer's own compressed keys, MX FP4 conversion (OCP MX v1.0, section 6.3)
+# ---------------------------------------------------------------------------------------------
+def _mx_fixture():
+    rounds, blocks = [], []
+    for line in open(os.path.join(GOLDEN, "mx_fp4_conversion.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        if line.startswith("round "):
+            _, y, c = line.split()
+            rounds.append((float(y), int(c, 16)))
+        else:
+            head, _, tail = line.partition("|")
+            _, rest, scale, rest_code = head.split()
+            vals = [tuple(t.split(":")) for t in tail.split()]
+            blocks.append((float(rest), int(scale), int(rest_code, 16),
+                           [(float(v), int(c, 16)) for v, c in vals]))
+    return rounds, blocks
+
+
+def test_mx_fp4_element_rounding_worked_values():
+    rounds, _ = _mx_fixture()
+    y = np.array([r[0] for r in rounds])
+    np.testing.assert_array_equal(O.e2m1_round(y), np.array([r[1] for r in rounds], np.uint8))
+
+
+def test_mx_fp4_block_conversion_worked_examples():
+    _, blocks = _mx_fixture()
+    for rest, scale, rest_code, vals in blocks:
+        x = np.full(32, rest)
+        for i, (v, _) in enumerate(vals):
+            x[i] = v
+        codes, scales = O.mx_fp4_quantize(x[None, :])
+        nib = np.stack([codes[0] & 0xF, codes[0] >> 4], axis=-1).reshape(32)
+        assert int(scales[0, 0]) == scale, (rest, vals, int(scales[0, 0]))
+        want = [c for _, c in vals] + [rest_code] * (32 - len(vals))
+        np.testing.assert_array_equal(nib, np.array(want, np.uint8), err_msg=str((rest, vals)))
+
+
+def test_mx_fp4_every_element_is_a_nearest_grid_point():
+    """Property of the conversion for random blocks spanning many binades: every dequantized
+    element is a grid point no farther from V/X than any other grid point (saturated elements
+    sit at +-6), and the block maximum lands in [4, 8) X, the top binade of the grid."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((400, 64)) * np.ldexp(1.0, rng.integers(-20, 20, (400, 1)))
+    x[::7, 3] = 0.0
+    codes, scales = O.mx_fp4_quantize(x)
+    X = np.repeat(O.ue8m0_to_f64(scales), 32, axis=-1)
+    deq = O.mx_fp4_dequant(codes, scales, 64)
+    y = x / X
+    grid = np.concatenate([-O.E2M1_MAGNITUDES[::-1], O.E2M1_MAGNITUDES])
+    d_best = np.abs(y[..., None] - grid).min(axis=-1)
+    d_got = np.abs(y - deq / X)
+    sat = np.abs(y) > 6.0
+    assert np.all(d_got[~sat] <= d_best[~sat])
+    assert np.all(np.abs(deq[sat] / X[sat]) == 6.0)
+    amax = np.abs(x.reshape(400, 2, 32)).max(axis=-1)
+    ratio = amax / O.ue8m0_to_f64(scales)
+    assert np.all((ratio >= 4.0) & (ratio < 8.0))
+
+
+def test_mx_fp4_grid_values_round_trip():
+    """Blocks whose values already lie on the e2m1 grid times 2^e, with a maximum of 4 or 6
+    times 2^e, convert back to themselves exactly."""
+    rng = np.random.default_rng(6)
+    for e in (-10, -2, 0, 3):
+        vals = O.E2M1_MAGNITUDES[rng.integers(0, 8, (50, 32))] * \
+            np.where(rng.random((50, 32)) < 0.5, -1.0, 1.0)
+        vals[:, 0] = rng.choice([4.0, 6.0, -6.0], 50)
+        x = np.ldexp(vals, e)
+        codes, scales = O.mx_fp4_quantize(x)
+        assert np.all(scales == 127 + e)
+        np.testing.assert_array_equal(O.mx_fp4_dequant(codes, scales, 32), x + 0.0)
+
+
+def test_bf16_rounding_paths_agree():
+    """The direct float64 -> bf16 rounding used for pooled index keys agrees with the fp32-bit
+    rounding of the index-score path on every fp32 value, ties included."""
+    rng = np.random.default_rng(7)
+    f = (rng.integers(0x00800000, 0x7F000000, 20000, dtype=np.uint32)).view(np.float32)
+    f = np.concatenate([f, -f, np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 0.0], np.float32)])
+    x = f.astype(np.float64)
+    np.testing.assert_array_equal(O.f64_to_bf16_rne_any(x), O.f64_to_bf16_rne(x))
+
+
+def test_index_key_entries_block_one_equals_direct_conversion():
+    """With m = 1 every entry is its raw row (the weights of one token are 1), so the compressed
+    index keys are the MX FP4 conversion of the raw bf16 rows themselves; with equal logits an
+    entry is the block mean."""
+    rng = np.random.default_rng(8)
+    xi = O.f64_to_bf16_rne_any(rng.standard_normal((12, 64)))
+    codes, scales, pb, _ = O.index_key_entries(xi, rng.standard_normal(12), 1)
+    c2, s2 = O.mx_fp4_quantize(O.bf16_to_f64(xi))
+    np.testing.assert_array_equal(pb, xi)
+    np.testing.assert_array_equal(codes, c2)
+    np.testing.assert_array_equal(scales, s2)
+    _, _, _, pooled = O.index_key_entries(xi, np.zeros(12), 4)
+    np.testing.assert_allclose(pooled, O.bf16_to_f64(xi).reshape(3, 4, 64).mean(axis=1),
+                               rtol=0, atol=1e-15)
+
+
+def test_index_key_entries_follow_the_dominant_logit():
+    """The pooling weights are a softmax over the block's logits: a token whose logit exceeds
+    the others' by 60 takes all the weight (to 1e-26), so its raw row is the pooled key."""
+    rng = np.random.default_rng(9)
+    xi = O.f64_to_bf16_rne_any(rng.standard_normal((16, 64)))
+    logits = np.full(16, -30.0)
+    pick = rng.integers(0, 4, 4)
+    logits[np.arange(4) * 4 + pick] = 30.0
+    codes, scales, pb, pooled = O.index_key_entries(xi, logits, 4)
+    np.testing.assert_allclose(pooled, O.bf16_to_f64(xi)[np.arange(4) * 4 + pick], rtol=1e-20,
+                               atol=1e-20)
+    np.testing.assert_array_equal(pb, xi[np.arange(4) * 4 + pick])
