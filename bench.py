@@ -40,6 +40,7 @@ DEFAULT_CONFIG = "csa_decode_128k"
 KERNEL_SOURCES = {
     "indexer_mxf4": "indexer.cu", "topk": "topk.cu", "csa_attend": "attend_tc.cu",
     "hca_attend": "attend_tc.cu", "lse_merge": "attend.cu", "compress": "compress.cu",
+    "index_keys": "compress.cu",
 }
 
 
@@ -53,6 +54,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
+    ap.add_argument("--index-keys", action="store_true",
+                    help="CSA layers pool the new entries' FP4 index keys from per-token bf16 "
+                         "index-key rows inside the step (instead of taking them as inputs)")
     ap.add_argument("--context", type=int, default=None,
                     help="override the workload's context length (smaller ncu captures)")
     ap.add_argument("--quick", action="store_true",
@@ -67,7 +71,7 @@ def _vis(t, m, E):
     return max(0, min(E, (t + 1) // m))
 
 
-def layer_work(s):
+def layer_work(s, index_keys=False):
     """Per-kernel algorithmic bytes and FLOPs of one step of one layer."""
     B, Nq, H, d, m, W = s.B, s.Nq, s.H, s.d, s.m, s.W
     E = s.E
@@ -76,6 +80,11 @@ def layer_work(s):
     n_new = E - j0
     k = {}
     k["compress"] = dict(bytes=B * n_new * m * (row + 4) + B * n_new * row, flops=B * n_new * m * 4 * d)
+    if index_keys and s.kind == "csa":
+        # index-key rows and logits of the new blocks read, FP4 codes + scales written
+        k["index_keys"] = dict(bytes=B * n_new * m * (2 * s.d_I + 4) +
+                               B * n_new * (s.d_I // 2 + s.d_I // 32),
+                               flops=B * n_new * m * 2 * s.d_I)
     qo = B * Nq * H * d * 2 * 2
     sel_keys = 0
     win_keys = 0
@@ -108,10 +117,10 @@ def layer_work(s):
     return k
 
 
-def step_work(wl):
+def step_work(wl, index_keys=False):
     kernels = {}
     for s in wl.layers:
-        for n, v in layer_work(s).items():
+        for n, v in layer_work(s, index_keys).items():
             a = kernels.setdefault(n, dict(bytes=0, flops=0))
             a["bytes"] += v["bytes"]
             a["flops"] += v["flops"]
@@ -241,11 +250,18 @@ class ClockSampler:
 # ----------------------------------------------------------------------------------------------
 # native arm
 # ----------------------------------------------------------------------------------------------
-def setup_layer(s, seed, layer_id, dev):
+def setup_layer(s, seed, layer_id, dev, index_keys=False):
     import torch
     import long_context_compressed_pooling_b300 as csa
-    from synth import generate_layer
+    from synth import generate_layer, index_key_rows
     x = generate_layer(s, seed, layer_id, device=dev)
+    if index_keys and s.kind == "csa":
+        # the layer pools its own index keys: per-token rows, with the cached prefix's keys
+        # pooled once here
+        x["xi_raw"] = index_key_rows(s, seed, layer_id, device=dev)
+        if s.compress_begin > 0:
+            csa.compress_index_keys(x["xi_raw"], x["logits"], s.m, x["ki_codes"], x["ki_scales"],
+                                    0, s.compress_begin)
     kc = torch.empty((s.B, s.E, s.d), dtype=torch.bfloat16, device=dev)
     vc = torch.empty_like(kc)
     if s.compress_begin > 0:  # the context before this step is already in the entry cache
@@ -267,8 +283,11 @@ def step_inputs(s, d):
              ("w_new", d["logits"][:, s.N - n_new:])]
     if s.kind == "csa":
         j0 = s.compress_begin // s.m
-        items += [("qi_codes", d["qi_codes"]), ("qi_scales", d["qi_scales"]),
-                  ("ki_new", d["ki_codes"][:, j0:]), ("kis_new", d["ki_scales"][:, j0:])]
+        items += [("qi_codes", d["qi_codes"]), ("qi_scales", d["qi_scales"])]
+        if d.get("xi_raw") is not None:
+            items += [("xi_new", d["xi_raw"][:, s.N - n_new:])]
+        else:
+            items += [("ki_new", d["ki_codes"][:, j0:]), ("kis_new", d["ki_scales"][:, j0:])]
     return items
 
 
@@ -316,7 +335,8 @@ def run_native(args, rank, world):
     if args.context:
         wl = resize_context(wl, args.context)
     seed = rank_seed(wl, rank)             # every rank decodes its own sequences (weak scaling)
-    states = {s.kind: setup_layer(s, seed, li, dev) for li, s in enumerate(wl.layers)}
+    states = {s.kind: setup_layer(s, seed, li, dev, args.index_keys)
+              for li, s in enumerate(wl.layers)}
     call = csa.PreparedLayerPair(states.get("csa"), states.get("hca"))
     torch.cuda.synchronize()
 
@@ -371,7 +391,7 @@ def run_native(args, rank, world):
     assert csa.device_status(reset=True) == 0, "device status flags after the timed loop"
 
     units, unit = units_per_step(wl)
-    work = step_work(wl)
+    work = step_work(wl, args.index_keys)
     step_bytes = sum(v["bytes"] for v in work.values())
     step_flops = sum(v["flops"] for v in work.values())
     if units is not None:
@@ -387,7 +407,9 @@ def run_native(args, rank, world):
                       "batch_per_gpu": wl.layers[0].B, "context": wl.layers[0].N,
                       "l2": "flushed between timed steps (256 MB write outside the events)",
                       "launch": "cuda_graph" if graph is not None else "eager",
-                      "parallelism": f"replicas x{world} (independent sequences per GPU)"},
+                      "parallelism": f"replicas x{world} (independent sequences per GPU)",
+                      "index_keys": ("pooled in the step from bf16 index-key rows"
+                                     if args.index_keys else "inputs (FP4 codes + UE8M0)")},
            "step_alg_bytes": step_bytes, "step_alg_gbs": step_bytes / (ms_step * 1e-3) / 1e9,
            "step_alg_flops": step_flops}
     if not args.quick:
@@ -432,13 +454,15 @@ def run_native(args, rank, world):
     out["clocks"] = clk.summary()
 
     if not args.no_e2e and not args.quick:
-        out["e2e"] = run_e2e(wl, states, call, flush, K, dev, world, barrier)
-    if not args.no_cpu_baseline and not args.quick and rank == 0 and world == 1:
+        out["e2e"] = run_e2e(wl, states, call, flush, K, dev, world, barrier, args.index_keys)
+    # (with --index-keys the CSA keys are the library's output, which the oracle never reads)
+    if not args.no_cpu_baseline and not args.quick and rank == 0 and world == 1 \
+            and not args.index_keys:
         out["cpu_baseline"] = cpu_baseline(wl, states, budget_s=12.0)
     return out
 
 
-def run_e2e(wl, states, call, flush, K, dev, world, barrier):
+def run_e2e(wl, states, call, flush, K, dev, world, barrier, index_keys=False):
     """Same metric through the public API with host buffers: every step uploads its inputs from
     pinned host memory, runs the layer pair, and reads the outputs back."""
     import torch
@@ -504,7 +528,7 @@ def run_e2e(wl, states, call, flush, K, dev, world, barrier):
     barrier()
     ms = max_over_ranks(statistics.mean(e0[i].elapsed_time(e1[i]) for i in range(K)), world, dev)
     units, unit = units_per_step(wl)
-    work = step_work(wl)
+    work = step_work(wl, index_keys)
     if units is not None:
         v = units * world / (ms * 1e-3)
     else:

@@ -71,6 +71,36 @@ csa_status csa_compress(const uint16_t* k_raw, const uint16_t* v_raw, const floa
                         uint16_t* k_cmp, uint16_t* v_cmp, void* stream);
 
 /* ----------------------------------------------------------------------------------------
+ * csa_compress_index_keys -- the Lightning Indexer's own compressed keys.
+ * Lighthouse "deep deepseek v4 release" 八.7 lists them as a KV form of their own beside the
+ * CSA / HCA entries; 9fzt.com item 4 puts the indexer's QK path in FP4. Pages give no
+ * conversion rule; this library pools per-token index-key rows with the block pooling of
+ * csa_compress (same softmax over the block's logits), rounds each pooled value to bf16
+ * (round-to-nearest-even; a zero is +0) and converts every 32-element block to MX FP4 with the
+ * OCP Microscaling Formats v1.0 rule (section 6.3): scale X = 2^(floor(log2 max|v|) - 2) as a
+ * UE8M0 byte (0 for an all-zero block, exponent clamped to [-127, 127]), elements v / X rounded
+ * to nearest-even on the E2M1 grid, magnitudes above 6 clamped to 6.
+ *   xi_raw    : [B, N, d_I] bf16 index-key rows      logits : [B, N] fp32
+ *   ki_codes  : [B, N/m, d_I/2] packed e2m1 (low nibble = even element), written in place
+ *   ki_scales : [B, N/m, d_I/32] UE8M0
+ * Writes entries j with tok_begin <= j*m and (j+1)*m <= tok_end, as csa_compress.
+ * Supported: d_I in {32, 64, 128}, m a power of two in [1, 32]. xi_raw and ki_codes 16-byte
+ * aligned. Inputs must be finite.
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_compress_index_keys(const uint16_t* xi_raw, const float* logits, int B, int64_t N,
+                                   int d_I, int m, int64_t tok_begin, int64_t tok_end,
+                                   uint8_t* ki_codes, uint8_t* ki_scales, void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * csa_quantize_mxfp4 -- MX FP4 conversion of bf16 rows (the indexer's queries), the rule of
+ * csa_compress_index_keys applied to each row as given (the sign of -0 is kept: code 8).
+ *   x : [rows, d] bf16     codes : [rows, d/2] packed e2m1     scales : [rows, d/32] UE8M0
+ * Supported: d in {32, 64, 128}; x and codes 16-byte aligned; finite inputs.
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_quantize_mxfp4(const uint16_t* x, int64_t rows, int d, uint8_t* codes,
+                              uint8_t* scales, void* stream);
+
+/* ----------------------------------------------------------------------------------------
  * csa_index_topk -- Lightning Indexer scores + per-query top-k.
  * 9fzt.com DeepSeek-V4 summary item 4 (FP4 indexer QK path; index scores rounded from FP32 to
  * BF16), Lighthouse 八.3 (top-k over compressed entries), 八.7 (the indexer keeps its own
@@ -181,8 +211,8 @@ typedef struct csa_layer_desc {
   const float* logits;          /* [B, N] */
   const uint8_t* qi_codes;      /* [B, Nq, H_I, d_I/2] */
   const uint8_t* qi_scales;     /* [B, Nq, H_I, d_I/32] */
-  const uint8_t* ki_codes;      /* [B, N/m, d_I/2] */
-  const uint8_t* ki_scales;     /* [B, N/m, d_I/32] */
+  const uint8_t* ki_codes;      /* [B, N/m, d_I/2] (written for new entries when xi_raw set) */
+  const uint8_t* ki_scales;     /* [B, N/m, d_I/32] (likewise) */
   uint16_t* k_cmp;              /* [B, N/m, d] entry cache (in/out) */
   uint16_t* v_cmp;              /* [B, N/m, d] entry cache (in/out) */
   uint16_t* out;                /* [B, Nq, H, d] */
@@ -192,6 +222,10 @@ typedef struct csa_layer_desc {
   uint16_t* scores;             /* optional [B, Nq, N/m] */
   int B, Nq, H, d, m, W, k, H_I, d_I;
   int64_t N, q_pos0, compress_begin;
+  /* optional [B, N, d_I] bf16 index-key rows: when set, the layer also writes the indexer keys
+   * of the entries it compresses (csa_compress_index_keys over [compress_begin, N)) before
+   * scoring; when NULL, ki_codes / ki_scales are inputs. */
+  const uint16_t* xi_raw;
 } csa_layer_desc;
 
 typedef struct hca_layer_desc {

@@ -12,6 +12,7 @@ from ._native import (  # noqa: F401
     LIB_PATH,
     PreparedLayerPair,
     compress,
+    compress_index_keys,
     csa_attend,
     device_status,
     exported_symbols,
@@ -21,6 +22,7 @@ from ._native import (  # noqa: F401
     load_library,
     profiler_collect,
     profiler_enable,
+    quantize_mxfp4,
     topk,
     workspace_sizes,
 )

@@ -40,7 +40,7 @@ class CsaLayerDesc(ctypes.Structure):
                                   "ki_codes", "ki_scales", "k_cmp", "v_cmp", "out", "lse",
                                   "topk_idx", "topk_cnt", "scores")] + \
                [(n, _I) for n in ("B", "Nq", "H", "d", "m", "W", "k", "H_I", "d_I")] + \
-               [(n, _L) for n in ("N", "q_pos0", "compress_begin")]
+               [(n, _L) for n in ("N", "q_pos0", "compress_begin")] + [("xi_raw", _P)]
 
 
 class HcaLayerDesc(ctypes.Structure):
@@ -58,6 +58,8 @@ _SIGS = {
     "csa_profiler_enable": (_I, [_I]),
     "csa_profiler_collect": (_I, [ctypes.POINTER(KernelTime), _I, ctypes.POINTER(_I), _I]),
     "csa_compress": (_I, [_P, _P, _P, _I, _L, _I, _I, _L, _L, _P, _P, _P]),
+    "csa_compress_index_keys": (_I, [_P, _P, _I, _L, _I, _I, _L, _L, _P, _P, _P]),
+    "csa_quantize_mxfp4": (_I, [_P, _L, _I, _P, _P, _P]),
     "csa_index_topk": (_I, [_P, _P, _P, _P, _I, _I, _L, _L, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "csa_index_topk_workspace_size": (_Z, [_I, _I, _L, _I, _I]),
     "csa_index_topk_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _L, _L, _I, _I, _I, _I, _P, _P, _P]),
@@ -151,6 +153,42 @@ def compress(k_raw, v_raw, logits, m: int, k_cmp, v_cmp, tok_begin: int = 0,
         _ptr(_u16(k_cmp)), _ptr(_u16(v_cmp)), _stream(k_raw.device)))
 
 
+def compress_index_keys(xi_raw, logits, m: int, ki_codes=None, ki_scales=None,
+                        tok_begin: int = 0, tok_end: Optional[int] = None):
+    """The indexer's own compressed keys: pool the index-key rows xi_raw [B, N, d_I] (bf16) of
+    the blocks in [tok_begin, tok_end) and convert them to MX FP4. Returns (ki_codes
+    [B, N/m, d_I/2] uint8, ki_scales [B, N/m, d_I/32] uint8); given buffers are written in
+    place (entries outside the range are left untouched)."""
+    lib = load_library()
+    B, N, d_I = xi_raw.shape
+    E = N // m
+    dev = xi_raw.device
+    if ki_codes is None:
+        ki_codes = torch.zeros((B, E, d_I // 2), dtype=torch.uint8, device=dev)
+    if ki_scales is None:
+        ki_scales = torch.zeros((B, E, d_I // 32), dtype=torch.uint8, device=dev)
+    tok_end = N if tok_end is None else tok_end
+    _check("csa_compress_index_keys", lib.csa_compress_index_keys(
+        _ptr(_u16(xi_raw)), _ptr(logits), B, N, d_I, m, tok_begin, tok_end, _ptr(ki_codes),
+        _ptr(ki_scales), _stream(dev)))
+    return ki_codes, ki_scales
+
+
+def quantize_mxfp4(x, codes=None, scales=None):
+    """MX FP4 conversion of bf16 rows x [..., d]. Returns (codes [..., d/2] uint8, scales
+    [..., d/32] uint8)."""
+    lib = load_library()
+    d = x.shape[-1]
+    rows = x.numel() // d if d else 0
+    if codes is None:
+        codes = torch.empty(x.shape[:-1] + (d // 2,), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(x.shape[:-1] + (d // 32,), dtype=torch.uint8, device=x.device)
+    _check("csa_quantize_mxfp4", lib.csa_quantize_mxfp4(
+        _ptr(_u16(x)), rows, d, _ptr(codes), _ptr(scales), _stream(x.device)))
+    return codes, scales
+
+
 def index_topk(qi_codes, qi_scales, ki_codes, ki_scales, q_pos0: int, m: int, k: int,
                topk_idx=None, topk_cnt=None, scores=None, want_scores: bool = False,
                ws: Optional[torch.Tensor] = None):
@@ -238,7 +276,7 @@ def _csa_desc(c: Dict) -> CsaLayerDesc:
     H_I, half = c["qi_codes"].shape[2], c["qi_codes"].shape[3]
     dsc = CsaLayerDesc()
     for f in ("q", "k_raw", "v_raw", "logits", "qi_codes", "qi_scales", "ki_codes", "ki_scales",
-              "k_cmp", "v_cmp", "out", "lse", "topk_idx", "topk_cnt", "scores"):
+              "k_cmp", "v_cmp", "out", "lse", "topk_idx", "topk_cnt", "scores", "xi_raw"):
         setattr(dsc, f, _ptr(c.get(f)))
     dsc.B, dsc.Nq, dsc.H, dsc.d = B, Nq, H, d
     dsc.m, dsc.W, dsc.k, dsc.H_I, dsc.d_I = c["m"], c["W"], c["k"], H_I, 2 * half

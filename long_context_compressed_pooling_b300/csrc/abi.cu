@@ -143,6 +143,19 @@ csa_status check_attend(const uint16_t* q, const uint16_t* k_cmp, const uint16_t
   return CSA_OK;
 }
 
+csa_status check_index_keys(const uint16_t* xi_raw, const float* logits, int B, int64_t N,
+                            int d_I, int m, int64_t tok_begin, int64_t tok_end,
+                            const uint8_t* ki_codes, const uint8_t* ki_scales) {
+  if (!xi_raw || !logits || !ki_codes || !ki_scales) return CSA_ERR_INVALID_ARG;
+  if (!al16(xi_raw) || !al16(ki_codes) || (uintptr_t)logits % 4) return CSA_ERR_ALIGN;
+  if (B < 1 || N < 1 || m < 1) return CSA_ERR_INVALID_ARG;
+  if (tok_begin < 0 || tok_end < tok_begin || tok_end > N || tok_begin % m != 0)
+    return CSA_ERR_SHAPE;
+  if (d_I != 32 && d_I != 64 && d_I != 128) return CSA_ERR_UNSUPPORTED;
+  if (m > 32 || (m & (m - 1)) != 0) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
 // ---- internal runners (arguments already validated) -----------------------------------------
 csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
                           const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
@@ -206,7 +219,7 @@ size_t pair_hca_ws(const hca_layer_desc* h) {
 
 extern "C" {
 
-int csa_abi_version(void) { return 1; }
+int csa_abi_version(void) { return 2; }
 
 const char* csa_status_string(csa_status s) {
   switch (s) {
@@ -230,6 +243,27 @@ csa_status csa_compress(const uint16_t* k_raw, const uint16_t* v_raw, const floa
   const int64_t j0 = tok_begin / m, j1 = tok_end / m;
   return from_cuda(launch_compress(k_raw, v_raw, logits, B, N, d, m, j0, j1 - j0, k_cmp, v_cmp,
                                    static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_compress_index_keys(const uint16_t* xi_raw, const float* logits, int B, int64_t N,
+                                   int d_I, int m, int64_t tok_begin, int64_t tok_end,
+                                   uint8_t* ki_codes, uint8_t* ki_scales, void* stream) {
+  csa_status s = check_index_keys(xi_raw, logits, B, N, d_I, m, tok_begin, tok_end, ki_codes,
+                                  ki_scales);
+  if (s != CSA_OK) return s;
+  const int64_t j0 = tok_begin / m, j1 = tok_end / m;
+  return from_cuda(launch_index_keys(xi_raw, logits, B, N, d_I, m, j0, j1 - j0, ki_codes,
+                                     ki_scales, static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_quantize_mxfp4(const uint16_t* x, int64_t rows, int d, uint8_t* codes,
+                              uint8_t* scales, void* stream) {
+  if (!x || !codes || !scales) return CSA_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(codes)) return CSA_ERR_ALIGN;
+  if (rows < 0) return CSA_ERR_SHAPE;
+  if (d != 32 && d != 64 && d != 128) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(launch_mxfp4_quantize(x, rows, d, codes, scales,
+                                         static_cast<cudaStream_t>(stream)));
 }
 
 size_t csa_index_topk_workspace_size(int B, int Nq, int64_t E, int k, int scores_given) {
@@ -331,6 +365,11 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
     s = check_index(c->qi_codes, c->qi_scales, c->ki_codes, c->ki_scales, c->B, c->Nq, c->q_pos0,
                     E, c->m, c->H_I, c->d_I, c->k, c->topk_idx, c->topk_cnt, c->scores);
     if (s != CSA_OK) return s;
+    if (c->xi_raw) {
+      s = check_index_keys(c->xi_raw, c->logits, c->B, c->N, c->d_I, c->m, c->compress_begin,
+                           c->N, c->ki_codes, c->ki_scales);
+      if (s != CSA_OK) return s;
+    }
     s = check_attend(c->q, c->k_cmp, c->v_cmp, E, c->k_raw, c->v_raw, c->N, c->W, c->B, c->Nq,
                      c->q_pos0, c->H, c->d, c->out, c->lse);
     if (s != CSA_OK) return s;
@@ -365,6 +404,11 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
     const int64_t j0 = c->compress_begin / c->m;
     if (launch_compress(c->k_raw, c->v_raw, c->logits, c->B, c->N, c->d, c->m, j0, E - j0,
                         c->k_cmp, c->v_cmp, st) != cudaSuccess)
+      return CSA_ERR_CUDA;
+    if (c->xi_raw &&
+        launch_index_keys(c->xi_raw, c->logits, c->B, c->N, c->d_I, c->m, j0, E - j0,
+                          const_cast<uint8_t*>(c->ki_codes), const_cast<uint8_t*>(c->ki_scales),
+                          st) != cudaSuccess)
       return CSA_ERR_CUDA;
     csa_status s = run_index_topk(c->qi_codes, c->qi_scales, c->ki_codes, c->ki_scales, c->B,
                                   c->Nq, c->q_pos0, E, c->m, c->H_I, c->d_I, c->k, c->topk_idx,

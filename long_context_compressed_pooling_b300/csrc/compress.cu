@@ -225,6 +225,157 @@ __global__ void __launch_bounds__(256) compress_large_kernel(const uint16_t* __r
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+// The Lightning Indexer's own compressed keys (Lighthouse 八.7 lists them beside the CSA / HCA
+// entries; 9fzt.com item 4 runs the indexer's QK path in FP4): per-token index-key rows are
+// pooled with the same block pooling, rounded to bf16, and converted to MX FP4 (OCP
+// Microscaling Formats v1.0, section 6.3: block scale X = 2^(floor(log2 max|v|) - 2), elements
+// v / X rounded to nearest-even on the E2M1 grid and clamped to 6; an all-zero block takes the
+// smallest scale byte 0). One warp per row: lane l holds elements [EPL l, EPL l + EPL) of a
+// d = 32 EPL row, so a 32-element block spans 32 / EPL lanes.
+// ---------------------------------------------------------------------------------------------
+
+// E2M1 code (3 magnitude bits) of |y|: the nearest grid value, ties to the even code. The grid
+// midpoints are 0.25 0.75 1.25 1.75 2.5 3.5 5; at a midpoint the even neighbour wins, so the
+// comparison is strict where the lower neighbour is even and inclusive where the upper one is.
+CSA_DEV uint32_t e2m1_magnitude_code(float a) {
+  return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+         (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
+}
+
+// Converts this lane's EPL bf16 values (bit patterns) of a row to E2M1 codes (low nibbles,
+// element order) and returns the block's UE8M0 scale byte (valid in every lane of the block).
+template <int EPL>
+CSA_DEV uint32_t mx_encode(const uint32_t (&bits)[EPL], uint32_t (&code)[EPL]) {
+  constexpr int LPB = 32 / EPL;  // lanes per 32-element block
+  uint32_t amax = 0;  // |v| as fp32 bits: order-preserving for non-negative values
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) amax = max(amax, (bits[e] << 16) & 0x7FFFFFFFu);
+#pragma unroll
+  for (int o = 1; o < LPB; o <<= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  // floor(log2 amax) - 2, clamped to the UE8M0 range; a zero (or bf16 subnormal) maximum gives
+  // the smallest scale
+  const int ef = (int)(amax >> 23);
+  const int xe = ef == 0 ? -127 : max(ef - 129, -127);
+  const float inv_x = __int_as_float((127 - xe) << 23);  // 2^-xe, exact
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const float v = __uint_as_float(bits[e] << 16);
+    code[e] = e2m1_magnitude_code(fabsf(v) * inv_x) | ((bits[e] >> 12) & 0x8u);
+  }
+  return (uint32_t)(xe + 127);
+}
+
+// Writes one row's codes (d / 2 bytes) and scales (d / 32 bytes).
+template <int EPL>
+CSA_DEV void mx_store(const uint32_t (&code)[EPL], uint32_t scale, uint8_t* codes_row,
+                      uint8_t* scales_row, int lane) {
+  constexpr int LPB = 32 / EPL;
+  if constexpr (EPL == 1) {
+    const uint32_t hi = __shfl_down_sync(0xffffffffu, code[0], 1);
+    if ((lane & 1) == 0) codes_row[lane >> 1] = (uint8_t)(code[0] | (hi << 4));
+  } else if constexpr (EPL == 2) {
+    codes_row[lane] = (uint8_t)(code[0] | (code[1] << 4));
+  } else {
+    *reinterpret_cast<uint16_t*>(codes_row + 2 * lane) =
+        (uint16_t)(code[0] | (code[1] << 4) | (code[2] << 8) | (code[3] << 12));
+  }
+  if (lane % LPB == 0) scales_row[lane / LPB] = (uint8_t)scale;
+}
+
+template <int EPL>
+CSA_DEV void load_row(const uint16_t* row, int lane, uint32_t (&bits)[EPL]) {
+  if constexpr (EPL == 1) {
+    bits[0] = row[lane];
+  } else if constexpr (EPL == 2) {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(row + 2 * lane);
+    bits[0] = u & 0xFFFFu;
+    bits[1] = u >> 16;
+  } else {
+    const uint2 u = *reinterpret_cast<const uint2*>(row + 4 * lane);
+    bits[0] = u.x & 0xFFFFu;
+    bits[1] = u.x >> 16;
+    bits[2] = u.y & 0xFFFFu;
+    bits[3] = u.y >> 16;
+  }
+}
+
+// Index keys of entries [j_begin, j_begin + n_entries) of every sequence; m <= 32 (one lane per
+// token of the block holds its logit).
+template <int EPL>
+__global__ void __launch_bounds__(256) index_keys_kernel(const uint16_t* __restrict__ xi_raw,
+                                                         const float* __restrict__ logits,
+                                                         uint8_t* __restrict__ ki_codes,
+                                                         uint8_t* __restrict__ ki_scales, int B,
+                                                         int64_t N, int m, int64_t j_begin,
+                                                         int64_t n_entries) {
+  constexpr int D = 32 * EPL;
+  pdl_wait();  // before the trigger, as in compress_kernel
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t E = N / m;
+  const int64_t total = (int64_t)B * n_entries;
+  for (int64_t w = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); w < total;
+       w += (int64_t)gridDim.x * 8) {
+    const int64_t b = w / n_entries, j = j_begin + w % n_entries;
+    const int64_t t0 = b * N + j * m;  // first token of the block
+    const float lg = lane < m ? logits[t0 + lane] : -INFINITY;
+    float acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    float mx = lg;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float ex = lane < m ? expf(lg - mx) : 0.f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float inv = 1.f / sum;
+    for (int i0 = 0; i0 < m; i0 += 4) {
+      uint32_t rb[4][EPL];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u < m) load_row<EPL>(xi_raw + (t0 + i0 + u) * D, lane, rb[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float pw = __shfl_sync(0xffffffffu, ex, (i0 + u) & 31) * inv;
+        if (i0 + u < m) {
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) acc[e] = fmaf(pw, __uint_as_float(rb[u][e] << 16), acc[e]);
+        }
+      }
+    }
+    uint32_t bits[EPL], code[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      bits[e] = f32_to_bf16_bits(acc[e]);
+      if (bits[e] == 0x8000u) bits[e] = 0u;  // a pooled zero is +0
+    }
+    const uint32_t scale = mx_encode<EPL>(bits, code);
+    const int64_t row = b * E + j;
+    mx_store<EPL>(code, scale, ki_codes + row * (D / 2), ki_scales + row * (D / 32), lane);
+  }
+}
+
+// MX FP4 conversion of bf16 rows (the index queries), one warp per row.
+template <int EPL>
+__global__ void __launch_bounds__(256) mxfp4_quantize_kernel(const uint16_t* __restrict__ x,
+                                                             int64_t rows,
+                                                             uint8_t* __restrict__ codes,
+                                                             uint8_t* __restrict__ scales) {
+  constexpr int D = 32 * EPL;
+  pdl_wait();
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows;
+       r += (int64_t)gridDim.x * 8) {
+    uint32_t bits[EPL], code[EPL];
+    load_row<EPL>(x + r * D, lane, bits);
+    const uint32_t scale = mx_encode<EPL>(bits, code);
+    mx_store<EPL>(code, scale, codes + r * (D / 2), scales + r * (D / 32), lane);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_compress(const uint16_t* k_raw, const uint16_t* v_raw, const float* logits,
@@ -280,6 +431,51 @@ cudaError_t launch_compress(const uint16_t* k_raw, const uint16_t* v_raw, const 
       return cudaErrorInvalidValue;
   }
   return e;
+}
+
+cudaError_t launch_index_keys(const uint16_t* xi_raw, const float* logits, int B, int64_t N, int d_I,
+                              int m, int64_t j_begin, int64_t n_entries, uint8_t* ki_codes,
+                              uint8_t* ki_scales, cudaStream_t stream) {
+  if (n_entries <= 0 || B <= 0) return cudaSuccess;
+  int64_t blocks = ((int64_t)B * n_entries + 7) / 8;
+  const int64_t cap = (int64_t)kNumSMs * 8;
+  if (blocks > cap) blocks = cap;
+  ProfScope prof(stream, "index_keys");
+  switch (d_I) {
+    case 32:
+      return launch_ex(index_keys_kernel<1>, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                       xi_raw, logits, ki_codes, ki_scales, B, N, m, j_begin, n_entries);
+    case 64:
+      return launch_ex(index_keys_kernel<2>, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                       xi_raw, logits, ki_codes, ki_scales, B, N, m, j_begin, n_entries);
+    case 128:
+      return launch_ex(index_keys_kernel<4>, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                       xi_raw, logits, ki_codes, ki_scales, B, N, m, j_begin, n_entries);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_mxfp4_quantize(const uint16_t* x, int64_t rows, int d, uint8_t* codes,
+                                  uint8_t* scales, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  int64_t blocks = (rows + 7) / 8;
+  const int64_t cap = (int64_t)kNumSMs * 8;
+  if (blocks > cap) blocks = cap;
+  ProfScope prof(stream, "mxfp4_quantize");
+  switch (d) {
+    case 32:
+      return launch_ex(mxfp4_quantize_kernel<1>, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                       x, rows, codes, scales);
+    case 64:
+      return launch_ex(mxfp4_quantize_kernel<2>, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                       x, rows, codes, scales);
+    case 128:
+      return launch_ex(mxfp4_quantize_kernel<4>, dim3((unsigned)blocks), dim3(256), 0, stream, 1,
+                       x, rows, codes, scales);
+    default:
+      return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace csa

@@ -44,6 +44,14 @@ constexpr int kNumSMs = 148;
 uint32_t* device_status_word();
 
 // ---- block pooling --------------------------------------------------------------------------
+// The indexer's own compressed keys: pool index-key rows [B, N, d_I] of entries
+// [j_begin, j_begin + n_entries) and convert them to MX FP4 (d_I in {32, 64, 128}, m <= 32).
+cudaError_t launch_index_keys(const uint16_t* xi_raw, const float* logits, int B, int64_t N, int d_I,
+                              int m, int64_t j_begin, int64_t n_entries, uint8_t* ki_codes,
+                              uint8_t* ki_scales, cudaStream_t stream);
+// MX FP4 conversion of bf16 rows [rows, d], d in {32, 64, 128}.
+cudaError_t launch_mxfp4_quantize(const uint16_t* x, int64_t rows, int d, uint8_t* codes,
+                                  uint8_t* scales, cudaStream_t stream);
 cudaError_t launch_compress(const uint16_t* k_raw, const uint16_t* v_raw, const float* logits,
                             int B, int64_t N, int d, int m, int64_t j_begin, int64_t n_entries,
                             uint16_t* k_cmp, uint16_t* v_cmp, cudaStream_t stream);

@@ -10,5 +10,6 @@ from .workloads import (  # noqa: F401
     LayerShape,
     Workload,
     generate_layer,
+    index_key_rows,
     get_config,
 )

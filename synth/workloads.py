@@ -130,7 +130,7 @@ def get_config(name_or_index) -> Workload:
 
 
 _TENSOR_IDS = {"q": 1, "k_raw": 2, "v_raw": 3, "logits": 4,
-               "qi_codes": 5, "qi_scales": 6, "ki_codes": 7, "ki_scales": 8}
+               "qi_codes": 5, "qi_scales": 6, "ki_codes": 7, "ki_scales": 8, "xi_raw": 9}
 
 
 def _gen(seed: int, layer_id: int, name: str, device) -> torch.Generator:
@@ -189,6 +189,15 @@ def generate_layer(shape: LayerShape, seed: int, layer_id: int = 0,
                                          generator=_gen(seed, layer_id, "ki_scales", device),
                                          device=device, dtype=torch.uint8)
     return out
+
+
+def index_key_rows(shape: LayerShape, seed: int, layer_id: int = 0,
+                   device: Optional[torch.device] = None) -> torch.Tensor:
+    """Per-token index-key rows xi_raw [B, N, d_I], N(0,1) rounded to bf16 (the input the
+    indexer's own compressed keys are pooled from)."""
+    device = torch.device(device) if device is not None else torch.device("cpu")
+    s = shape
+    return _normal_bf16((s.B, s.N, s.d_I), 1.0, _gen(seed, layer_id, "xi_raw", device), device)
 
 
 def bf16_bits(t: torch.Tensor):

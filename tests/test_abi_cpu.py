@@ -22,7 +22,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert len(syms) >= 14
     missing = [n for n, ok in syms.items() if not ok]
     assert not missing, missing
-    assert lib.csa_abi_version() == 1
+    assert lib.csa_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -88,10 +88,28 @@ def test_workspace_sizes(lib):
     assert lib.csa_index_topk_workspace_size(16, 1, 32768, 512, 1) == 0
 
 
+def test_index_key_and_quantizer_validation(lib):
+    f = lib.csa_compress_index_keys
+    x, w, c, sc = _p(ALN), _p(ALN * 2), _p(ALN * 3), _p(ALN * 4)
+    assert f(None, w, 1, 64, 64, 4, 0, 64, c, sc, None) == 1          # null pointer
+    assert f(_p(ALN + 2), w, 1, 64, 64, 4, 0, 64, c, sc, None) == 3   # misaligned rows
+    assert f(x, w, 1, 64, 64, 4, 2, 64, c, sc, None) == 2             # tok_begin % m
+    assert f(x, w, 1, 64, 64, 4, 0, 65, c, sc, None) == 2             # tok_end > N
+    assert f(x, w, 1, 64, 48, 4, 0, 64, c, sc, None) == 5             # d_I
+    assert f(x, w, 1, 128, 64, 64, 0, 128, c, sc, None) == 5          # m > 32
+    assert f(x, w, 1, 64, 64, 3, 0, 63, c, sc, None) == 5             # m not a power of two
+    q = lib.csa_quantize_mxfp4
+    assert q(None, 4, 64, c, sc, None) == 1
+    assert q(x, 4, 64, _p(ALN + 1), sc, None) == 3
+    assert q(x, -1, 64, c, sc, None) == 2
+    assert q(x, 4, 96, c, sc, None) == 5
+
+
 def test_descriptor_struct_layout():
-    # 15 pointers, 9 ints (+4 padding), 3 int64 / 8 pointers, 6 ints, 3 int64
-    assert ctypes.sizeof(N.CsaLayerDesc) == 15 * 8 + 9 * 4 + 4 + 3 * 8
+    # 15 pointers, 9 ints (+4 padding), 3 int64, 1 pointer / 8 pointers, 6 ints, 3 int64
+    assert ctypes.sizeof(N.CsaLayerDesc) == 15 * 8 + 9 * 4 + 4 + 3 * 8 + 8
     assert N.CsaLayerDesc.N.offset == 160
+    assert N.CsaLayerDesc.xi_raw.offset == 184
     assert ctypes.sizeof(N.HcaLayerDesc) == 8 * 8 + 6 * 4 + 3 * 8
     assert N.HcaLayerDesc.N.offset == 88
 
