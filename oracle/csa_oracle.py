@@ -221,7 +221,14 @@ def index_scores(qi_codes, qi_scales, ki_codes, ki_scales, d_I: int) -> np.ndarr
 def topk_select(score_bits, n_visible: int, k: int) -> Tuple[np.ndarray, int]:
     """R7: the min(k, n_visible) entries with the largest BF16 score, ties to the lower index,
     returned sorted ascending and padded with -1 to length k."""
-    vals = bf16_to_f64(np.asarray(score_bits)[:n_visible])
+    return topk_select_values(bf16_to_f64(np.asarray(score_bits)[:n_visible]), n_visible, k)
+
+
+def topk_select_values(values, n_visible: int, k: int) -> Tuple[np.ndarray, int]:
+    """R7 on real-valued scores (the FP32 scores the pages' BF16 rounding replaces, 9fzt.com
+    item 4): the min(k, n_visible) largest, ties (-0 equal to +0) to the lower index, sorted
+    ascending and padded with -1."""
+    vals = np.asarray(values, dtype=np.float64)[:n_visible] + 0.0
     order = np.lexsort((np.arange(n_visible), -vals))     # primary: -score, secondary: index
     cnt = min(k, n_visible)
     idx = np.full(k, -1, dtype=np.int64)

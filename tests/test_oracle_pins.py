@@ -483,3 +483,25 @@ def test_index_key_entries_follow_the_dominant_logit():
     np.testing.assert_allclose(pooled, O.bf16_to_f64(xi)[np.arange(4) * 4 + pick], rtol=1e-20,
                                atol=1e-20)
     np.testing.assert_array_equal(pb, xi[np.arange(4) * 4 + pick])
+
+
+def test_topk_on_real_values_bruteforce():
+    """The real-valued selector (FP32 scores) against the characterisation by brute force, with
+    signed zeros and values that differ below BF16 resolution; on BF16-representable values it
+    agrees with the BF16 selector."""
+    rng = np.random.default_rng(4)
+    for trial in range(300):
+        n = int(rng.integers(0, 9))
+        k = int(rng.integers(1, 10))
+        vals = rng.choice([0.0, -0.0, 1.0, 1.0 + 2.0 ** -20, 1.0 + 2.0 ** -21, 3.0, -2.0], size=n)
+        idx, cnt = O.topk_select_values(vals, n, k)
+        chosen = [int(i) for i in idx[:cnt]]
+        assert idx[cnt:].tolist() == [-1] * (k - cnt)
+        sols = [c for c in itertools.combinations(range(n), min(k, n))
+                if _valid_topk(vals + 0.0, set(c), k)]
+        assert sols == [tuple(chosen)]
+        b = rng.choice([0.0, 0.5, 1.0, 3.0, -1.5], size=n)
+        bits = O.f64_to_bf16_rne(b) if n else np.zeros(0, np.uint16)
+        i1, c1 = O.topk_select(bits, n, k)
+        i2, c2 = O.topk_select_values(b, n, k)
+        assert c1 == c2 and np.array_equal(i1, i2)
