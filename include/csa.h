@@ -157,6 +157,28 @@ csa_status csa_index_topk_noalloc(const uint8_t* qi_codes, const uint8_t* qi_sca
 csa_status csa_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
                     int k, int32_t* topk_idx, int32_t* topk_cnt,
                     void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * csa_index_scores -- the Lightning Indexer alone: BF16 scores [B, Nq, E] as csa_index_topk
+ * computes them and, when scores_f32 is not NULL, the exact FP32 scores [B, Nq, E] they are
+ * rounded from (9fzt.com item 4: the scores were FP32 before being reduced to BF16; every
+ * FP32 score here is exact, so the BF16 score is its round-to-nearest-even). Only visible
+ * entries (those csa_index_topk scores for each query) are written. Same inputs and limits as
+ * csa_index_topk; scores and scores_f32 16-byte aligned.
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_index_scores(const uint8_t* qi_codes, const uint8_t* qi_scales,
+                            const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
+                            int64_t q_pos0, int64_t E, int m, int H_I, int d_I, uint16_t* scores,
+                            float* scores_f32, void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * csa_topk_f32 -- the selector of csa_topk over FP32 scores [B, Nq, E]: the selection the
+ * pages' BF16 scores replace (9fzt.com item 4 reports the BF16 selector 2x faster). Same
+ * order, tie rule, outputs and padding as csa_topk (-0 counts as +0; NaN not supported).
+ * Rows of at most 16 x 32768 visible entries (CSA_ERR_UNSUPPORTED beyond).
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_topk_f32(const float* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
+                        int k, int32_t* topk_idx, int32_t* topk_cnt, void* stream);
 size_t csa_topk_workspace_size(int B, int Nq, int64_t E, int k);
 
 /* ----------------------------------------------------------------------------------------

@@ -17,6 +17,7 @@ from ._native import (  # noqa: F401
     device_status,
     exported_symbols,
     hca_attend,
+    index_scores,
     index_topk,
     layer_pair,
     load_library,
@@ -24,5 +25,6 @@ from ._native import (  # noqa: F401
     profiler_enable,
     quantize_mxfp4,
     topk,
+    topk_f32,
     workspace_sizes,
 )

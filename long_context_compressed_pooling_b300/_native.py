@@ -63,6 +63,8 @@ _SIGS = {
     "csa_index_topk": (_I, [_P, _P, _P, _P, _I, _I, _L, _L, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "csa_index_topk_workspace_size": (_Z, [_I, _I, _L, _I, _I]),
     "csa_index_topk_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _L, _L, _I, _I, _I, _I, _P, _P, _P]),
+    "csa_index_scores": (_I, [_P, _P, _P, _P, _I, _I, _L, _L, _I, _I, _I, _P, _P, _P]),
+    "csa_topk_f32": (_I, [_P, _I, _I, _L, _L, _I, _I, _P, _P, _P]),
     "csa_topk": (_I, [_P, _I, _I, _L, _L, _I, _I, _P, _P, _P, _Z, _P]),
     "csa_topk_workspace_size": (_Z, [_I, _I, _L, _I]),
     "csa_attend": (_I, [_P, _P, _P, _L, _P, _P, _I, _P, _P, _L, _I, _I, _I, _L, _I, _I, _P, _P, _P,
@@ -212,6 +214,40 @@ def index_topk(qi_codes, qi_scales, ki_codes, ki_scales, q_pos0: int, m: int, k:
         H_I, d_I, k, _ptr(topk_idx), _ptr(topk_cnt), _ptr(scores), _ptr(ws), wsb,
         _stream(dev)))
     return topk_idx, topk_cnt, scores
+
+
+def index_scores(qi_codes, qi_scales, ki_codes, ki_scales, q_pos0: int, m: int,
+                 want_f32: bool = True, scores=None, scores_f32=None):
+    """The indexer alone. Returns (BF16 scores [B,Nq,E], FP32 scores [B,Nq,E] or None); only
+    visible entries are written (the rest of freshly allocated buffers is zero)."""
+    lib = load_library()
+    B, Nq, H_I, half = qi_codes.shape
+    E = ki_codes.shape[1]
+    dev = qi_codes.device
+    if scores is None:
+        scores = torch.zeros((B, Nq, E), dtype=torch.bfloat16, device=dev)
+    if want_f32 and scores_f32 is None:
+        scores_f32 = torch.zeros((B, Nq, E), dtype=torch.float32, device=dev)
+    _check("csa_index_scores", lib.csa_index_scores(
+        _ptr(qi_codes), _ptr(qi_scales), _ptr(ki_codes), _ptr(ki_scales), B, Nq, q_pos0, E, m,
+        H_I, 2 * half, _ptr(_u16(scores)), _ptr(scores_f32), _stream(dev)))
+    return scores, scores_f32
+
+
+def topk_f32(scores, q_pos0: int, m: int, k: int, topk_idx=None, topk_cnt=None):
+    """The selector over FP32 scores [B, Nq, E]. Returns (topk_idx, topk_cnt)."""
+    lib = load_library()
+    if scores.dtype != torch.float32:
+        raise TypeError("FP32 scores are expected")
+    B, Nq, E = scores.shape
+    dev = scores.device
+    if topk_idx is None:
+        topk_idx = torch.empty((B, Nq, k), dtype=torch.int32, device=dev)
+    if topk_cnt is None:
+        topk_cnt = torch.empty((B, Nq), dtype=torch.int32, device=dev)
+    _check("csa_topk_f32", lib.csa_topk_f32(_ptr(scores), B, Nq, q_pos0, E, m, k, _ptr(topk_idx),
+                                            _ptr(topk_cnt), _stream(dev)))
+    return topk_idx, topk_cnt
 
 
 def topk(scores, q_pos0: int, m: int, k: int, topk_idx=None, topk_cnt=None):

@@ -3,6 +3,7 @@
 // memory; scratch lives in the caller's workspace.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/csa.h"
@@ -102,19 +103,29 @@ csa_status check_compress(const uint16_t* k_raw, const uint16_t* v_raw, const fl
   return CSA_OK;
 }
 
+csa_status check_index_inputs(const uint8_t* qi_codes, const uint8_t* qi_scales,
+                              const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
+                              int64_t q_pos0, int64_t E, int m, int H_I, int d_I,
+                              const uint16_t* scores) {
+  if (!qi_codes || !qi_scales || !ki_codes || !ki_scales) return CSA_ERR_INVALID_ARG;
+  if (!al16(qi_codes) || !al16(ki_codes) || !al16(ki_scales) || (scores && !al16(scores)))
+    return CSA_ERR_ALIGN;
+  if (B < 1 || Nq < 1 || q_pos0 < 0 || E < 0 || m < 1) return CSA_ERR_INVALID_ARG;
+  if (d_I != 32 && d_I != 64) return CSA_ERR_UNSUPPORTED;
+  if (H_I != 1 && H_I != 2 && H_I != 4 && H_I != 8) return CSA_ERR_UNSUPPORTED;
+  if (E > (int64_t)1 << 31 || (int64_t)B * Nq > ((int64_t)1 << 31) - 1) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
+
 csa_status check_index(const uint8_t* qi_codes, const uint8_t* qi_scales,
                        const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
                        int64_t q_pos0, int64_t E, int m, int H_I, int d_I, int k,
                        const int32_t* topk_idx, const int32_t* topk_cnt, const uint16_t* scores) {
-  if (!qi_codes || !qi_scales || !ki_codes || !ki_scales || !topk_idx || !topk_cnt)
-    return CSA_ERR_INVALID_ARG;
-  if (!al16(qi_codes) || !al16(ki_codes) || !al16(ki_scales) || !al16(topk_idx) ||
-      !al16(topk_cnt) || (scores && !al16(scores)))
-    return CSA_ERR_ALIGN;
-  if (B < 1 || Nq < 1 || q_pos0 < 0 || E < 0 || m < 1 || k < 1) return CSA_ERR_INVALID_ARG;
-  if (d_I != 32 && d_I != 64) return CSA_ERR_UNSUPPORTED;
-  if (H_I != 1 && H_I != 2 && H_I != 4 && H_I != 8) return CSA_ERR_UNSUPPORTED;
-  if (E > (int64_t)1 << 31 || (int64_t)B * Nq > ((int64_t)1 << 31) - 1) return CSA_ERR_UNSUPPORTED;
+  csa_status s = check_index_inputs(qi_codes, qi_scales, ki_codes, ki_scales, B, Nq, q_pos0, E, m,
+                                    H_I, d_I, scores);
+  if (s != CSA_OK) return s;
+  if (!topk_idx || !topk_cnt || k < 1) return CSA_ERR_INVALID_ARG;
+  if (!al16(topk_idx) || !al16(topk_cnt)) return CSA_ERR_ALIGN;
   return CSA_OK;
 }
 
@@ -157,12 +168,26 @@ csa_status check_index_keys(const uint16_t* xi_raw, const float* logits, int B, 
 }
 
 // ---- internal runners (arguments already validated) -----------------------------------------
+csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const uint8_t* ki_codes,
+                       const uint8_t* ki_scales, int B, int Nq, int64_t q_pos0, int64_t E, int m,
+                       int H_I, int d_I, uint16_t* sc, float* scores_f32, cudaStream_t st);
+
 csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
                           const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
                           int64_t q_pos0, int64_t E, int m, int H_I, int d_I, int k,
                           int32_t* topk_idx, int32_t* topk_cnt, uint16_t* scores, void* ws,
                           cudaStream_t st) {
   uint16_t* sc = scores ? scores : static_cast<uint16_t*>(ws);
+  csa_status s = run_indexer(qi_codes, qi_scales, ki_codes, ki_scales, B, Nq, q_pos0, E, m, H_I,
+                             d_I, sc, nullptr, st);
+  if (s != CSA_OK) return s;
+  return from_cuda(launch_topk(sc, B, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, st));
+}
+
+// The indexer alone: BF16 scores (and, when scores_f32 is set, the exact FP32 scores).
+csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const uint8_t* ki_codes,
+                       const uint8_t* ki_scales, int B, int Nq, int64_t q_pos0, int64_t E, int m,
+                       int H_I, int d_I, uint16_t* sc, float* scores_f32, cudaStream_t st) {
   if (E > 0) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return CSA_ERR_CUDA;
@@ -180,10 +205,10 @@ csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
       return CSA_ERR_CUDA;
     const IndexerPlan plan = plan_indexer(B, Nq, E, H_I, d_I);
     cudaError_t e = launch_indexer(&map, ki_codes, qi_codes, qi_scales, ki_scales, sc, B, Nq, q_pos0, E, m,
-                                   H_I, d_I, plan, status, st);
+                                   H_I, d_I, plan, status, st, scores_f32);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   }
-  return from_cuda(launch_topk(sc, B, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, st));
+  return CSA_OK;
 }
 
 size_t index_ws_bytes(int B, int Nq, int64_t E, int scores_given) {
@@ -289,6 +314,30 @@ csa_status csa_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
 size_t csa_topk_workspace_size(int B, int Nq, int64_t E, int k) {
   (void)B; (void)Nq; (void)E; (void)k;
   return 0;
+}
+
+csa_status csa_index_scores(const uint8_t* qi_codes, const uint8_t* qi_scales,
+                            const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
+                            int64_t q_pos0, int64_t E, int m, int H_I, int d_I, uint16_t* scores,
+                            float* scores_f32, void* stream) {
+  if (!scores) return CSA_ERR_INVALID_ARG;
+  if (scores_f32 && !al16(scores_f32)) return CSA_ERR_ALIGN;
+  csa_status s = check_index_inputs(qi_codes, qi_scales, ki_codes, ki_scales, B, Nq, q_pos0, E,
+                                    m, H_I, d_I, scores);
+  if (s != CSA_OK) return s;
+  return run_indexer(qi_codes, qi_scales, ki_codes, ki_scales, B, Nq, q_pos0, E, m, H_I, d_I,
+                     scores, scores_f32, static_cast<cudaStream_t>(stream));
+}
+
+csa_status csa_topk_f32(const float* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
+                        int k, int32_t* topk_idx, int32_t* topk_cnt, void* stream) {
+  csa_status s = check_topk(reinterpret_cast<const uint16_t*>(scores), B, Nq, q_pos0, E, m, k,
+                            topk_idx, topk_cnt);
+  if (s != CSA_OK) return s;
+  const int64_t n_max = std::min(E, (q_pos0 + Nq) / m);
+  if (n_max > 16 * 32768) return CSA_ERR_UNSUPPORTED;
+  return from_cuda(launch_topk_f32(scores, B, Nq, q_pos0, E, m, k, topk_idx, topk_cnt,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 csa_status csa_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,

@@ -65,6 +65,7 @@ struct IdxParams {
   const uint8_t* qi_scales;  // [B, Nq, H_I, NB]
   const uint8_t* ki_scales;  // [B, E, NB]
   uint16_t* scores;          // [B, Nq, E]
+  float* scores_f32;         // optional [B, Nq, E]: the exact FP32 scores before BF16 rounding
   int64_t q_pos0, E;
   int Nq, m, QN, ncols, G, nacc, n_splits, tmem_cols;
   int B, tiles_per_seq;      // decode: CTAs walk contiguous ranges of (sequence, tile)
@@ -429,7 +430,10 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
                     sc += fmaxf(dot, 0.f);
                   }
                   sc += 0.0f;  // -0 -> +0
-                  if (j < qvis[ql]) srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
+                  if (j < qvis[ql]) {
+                    srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
+                    if (p.scores_f32) p.scores_f32[(srow - p.scores) + (int64_t)ql * p.E] = sc;
+                  }
                 }
               }
             }
@@ -498,7 +502,10 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
                   sc += fmaxf(dot, 0.f);
                 }
                 sc += 0.0f;  // -0 -> +0
-                if (j < qvis[ql]) srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
+                if (j < qvis[ql]) {
+                  srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
+                  if (p.scores_f32) p.scores_f32[(srow - p.scores) + (int64_t)ql * p.E] = sc;
+                }
               }
             }
           }
@@ -596,12 +603,14 @@ IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I) {
 cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, const uint8_t* qi_codes,
                            const uint8_t* qi_scales, const uint8_t* ki_scales, uint16_t* scores,
                            int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I, int d_I,
-                           const IndexerPlan& plan, uint32_t* status, cudaStream_t stream) {
+                           const IndexerPlan& plan, uint32_t* status, cudaStream_t stream,
+                           float* scores_f32) {
   IdxParams prm;
   prm.qi_codes = qi_codes;
   prm.qi_scales = qi_scales;
   prm.ki_scales = ki_scales;
   prm.scores = scores;
+  prm.scores_f32 = scores_f32;
   prm.q_pos0 = q_pos0;
   prm.E = E;
   prm.Nq = Nq;

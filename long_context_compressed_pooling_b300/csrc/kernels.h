@@ -71,11 +71,16 @@ bool indexer_bulk_path(int H_I, int d_I, int64_t E, int Nq);
 cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, const uint8_t* qi_codes,
                            const uint8_t* qi_scales, const uint8_t* ki_scales, uint16_t* scores,
                            int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I, int d_I,
-                           const IndexerPlan& plan, uint32_t* status, cudaStream_t stream);
+                           const IndexerPlan& plan, uint32_t* status, cudaStream_t stream,
+                           float* scores_f32 = nullptr);
 
 // ---- top-k over BF16 scores ------------------------------------------------------------------
 cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
                         int k, int32_t* topk_idx, int32_t* topk_cnt, cudaStream_t stream);
+// The same selection over FP32 scores [B, Nq, E] (rows of at most 16 x 32768 keys; longer rows
+// return cudaErrorInvalidValue).
+cudaError_t launch_topk_f32(const float* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
+                            int k, int32_t* topk_idx, int32_t* topk_cnt, cudaStream_t stream);
 
 // ---- attention (CSA sparse / HCA dense) ------------------------------------------------------
 struct AttendArgs {

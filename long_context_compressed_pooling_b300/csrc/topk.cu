@@ -37,6 +37,12 @@ CSA_DEV uint32_t order_key(uint32_t bits) {
   return (bits & 0x8000u) ? (~bits & 0xFFFFu) : (bits | 0x8000u);
 }
 
+// FP32 scores: the same order-preserving map on 32-bit patterns.
+CSA_DEV uint32_t order_key32(uint32_t bits) {
+  if (bits == 0x80000000u) bits = 0u;  // -0 counts as +0
+  return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
+}
+
 // Sums the per-warp histograms whist[NW][256] into hist[256] (all threads call it).
 template <int NW>
 CSA_DEV void reduce_warp_hists(const uint32_t* whist, uint32_t* hist) {
@@ -404,12 +410,17 @@ __global__ void __launch_bounds__(NT) topk_kernel(const uint16_t* __restrict__ s
 // the cluster exchanges only its CTAs' maxima, histograms and counts through distributed shared
 // memory (three hardware cluster barriers), and one block scan of per-thread selection masks
 // orders the output because every thread's keys are contiguous and ranks follow key order.
-template <int NT, int KPT>
-__global__ void __launch_bounds__(NT) topk_reg_kernel(const uint16_t* __restrict__ scores, int Nq,
+//
+// F32: FP32 scores with 32-bit keys. The threshold search runs on the upper 16 bits of the key
+// first (the BF16-truncated score: near-max histogram, else the two-digit radix select), then
+// resolves the keys in that bucket with two more byte digits of the lower half.
+template <int NT, int KPT, bool F32>
+__global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ scores, int Nq,
                                                       int64_t q_pos0, int64_t E, int m, int k,
                                                       int32_t* __restrict__ topk_idx,
                                                       int32_t* __restrict__ topk_cnt) {
   constexpr int NW = NT / 32;
+  constexpr int CS = F32 ? 16 : 0;  // shift from a key to its coarse (16-bit) part
   __shared__ uint32_t whist[NW * 256];
   __shared__ uint32_t hist1[256], hist2[256], gsum[256];
   __shared__ uint32_t wmax[NW];
@@ -425,7 +436,8 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const uint16_t* __restrict
   const int64_t row = blockIdx.x / C;
   const int64_t t = q_pos0 + (row % Nq);
   const int n = (int)max((int64_t)0, min(E, (t + 1) / m));
-  const uint16_t* src = scores + row * E;
+  const uint16_t* src = static_cast<const uint16_t*>(scores) + row * E;
+  const uint32_t* src32 = static_cast<const uint32_t*>(scores) + row * E;
   int32_t* out = topk_idx + row * (int64_t)k;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   if (n <= k) {  // uniform over the cluster
@@ -436,8 +448,23 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const uint16_t* __restrict
   // ---- keys of this thread ---------------------------------------------------------------------
   const int seg0 = ((int)rank * NT + tid) * KPT;
   uint32_t key[KPT];
-  const bool vec = ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) && seg0 + KPT <= n;
-  if (vec) {
+  const uintptr_t sa = F32 ? reinterpret_cast<uintptr_t>(src32) : reinterpret_cast<uintptr_t>(src);
+  const bool vec = (sa & 15u) == 0 && seg0 + KPT <= n;
+  if constexpr (F32) {
+    if (vec) {
+#pragma unroll
+      for (int q = 0; q < KPT / 4; ++q) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src32 + seg0) + q);
+        key[4 * q] = order_key32(v.x);
+        key[4 * q + 1] = order_key32(v.y);
+        key[4 * q + 2] = order_key32(v.z);
+        key[4 * q + 3] = order_key32(v.w);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j) key[j] = seg0 + j < n ? order_key32(src32[seg0 + j]) : 0u;
+    }
+  } else if (vec) {
     uint4 v[KPT / 8];
 #pragma unroll
     for (int q = 0; q < KPT / 8; ++q) v[q] = __ldg(reinterpret_cast<const uint4*>(src + seg0) + q);
@@ -481,9 +508,10 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const uint16_t* __restrict
   }
   // ---- near-max histogram (one bin per BF16 step below the maximum) ----
   uint32_t* wh = whist + w * 256;
+  const uint32_t max_c = row_max >> CS;  // coarse parts of keys and maximum
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
-    const uint32_t dd = row_max - key[j];
+    const uint32_t dd = max_c - (key[j] >> CS);
     if (dd < 255u && seg0 + j < n) atomicAdd(&wh[dd], 1u);
   }
   __syncthreads();
@@ -502,16 +530,17 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const uint16_t* __restrict
   sum_hist(hist1);
   select_prefix(gsum, (uint32_t)k, &sh_bin, &sh_above);
   __syncthreads();
-  uint32_t T, need_eq;
+  uint32_t Tc, above_c;  // coarse threshold and the count of keys whose coarse part exceeds it
   if (sh_bin >= 0) {
-    T = row_max - (uint32_t)sh_bin;
-    need_eq = (uint32_t)k - sh_above;
+    Tc = max_c - (uint32_t)sh_bin;
+    above_c = sh_above;
   } else {
-    // fallback: exact two-digit radix select on the registers (hist2, then hist1 again: every
-    // CTA of the cluster has read hist1 before it arrives at the digit-1 cluster barrier)
+    // fallback: exact two-digit radix select of the coarse parts on the registers (hist2, then
+    // hist1 again: every CTA of the cluster has read hist1 before it arrives at the digit-1
+    // cluster barrier)
 #pragma unroll
     for (int j = 0; j < KPT; ++j)
-      if (seg0 + j < n) atomicAdd(&wh[key[j] >> 8], 1u);
+      if (seg0 + j < n) atomicAdd(&wh[(key[j] >> CS) >> 8], 1u);
     __syncthreads();
     sum_hist(hist2);
     select_bin(gsum, (uint32_t)k, &sh_bin, &sh_above);
@@ -519,13 +548,39 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const uint16_t* __restrict
     const uint32_t hi_byte = (uint32_t)sh_bin, above_hi = sh_above;
 #pragma unroll
     for (int j = 0; j < KPT; ++j)
-      if (seg0 + j < n && (key[j] >> 8) == hi_byte) atomicAdd(&wh[key[j] & 0xFFu], 1u);
+      if (seg0 + j < n && (key[j] >> CS >> 8) == hi_byte) atomicAdd(&wh[(key[j] >> CS) & 0xFFu], 1u);
     __syncthreads();
     sum_hist(hist1);
     select_bin(gsum, (uint32_t)k - above_hi, &sh_bin, &sh_above);
     __syncthreads();
-    T = (hi_byte << 8) | (uint32_t)sh_bin;
-    need_eq = (uint32_t)k - (above_hi + sh_above);
+    Tc = (hi_byte << 8) | (uint32_t)sh_bin;
+    above_c = above_hi + sh_above;
+  }
+  uint32_t T, need_eq;
+  if constexpr (F32) {
+    // the keys in the coarse bucket Tc: byte 1 of the key, then byte 0 (hist2, then hist1; the
+    // last histogram written above was hist1)
+    const uint32_t need1 = (uint32_t)k - above_c;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+      if (seg0 + j < n && (key[j] >> 16) == Tc) atomicAdd(&wh[(key[j] >> 8) & 0xFFu], 1u);
+    __syncthreads();
+    sum_hist(hist2);
+    select_bin(gsum, need1, &sh_bin, &sh_above);
+    __syncthreads();
+    const uint32_t pre = (Tc << 8) | (uint32_t)sh_bin, above2 = sh_above;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+      if (seg0 + j < n && (key[j] >> 8) == pre) atomicAdd(&wh[key[j] & 0xFFu], 1u);
+    __syncthreads();
+    sum_hist(hist1);
+    select_bin(gsum, need1 - above2, &sh_bin, &sh_above);
+    __syncthreads();
+    T = (pre << 8) | (uint32_t)sh_bin;
+    need_eq = need1 - above2 - sh_above;
+  } else {
+    T = Tc;
+    need_eq = (uint32_t)k - above_c;
   }
   // ---- ordered write: bit masks of the selected keys, one scan of their counts; only the set
   // bits are visited ----
@@ -589,25 +644,25 @@ struct RegShape {
 constexpr RegShape kRegShapes[] = {{256, 16}, {512, 16}, {1024, 16}, {1024, 32}};
 constexpr int kMaxRegCluster = 16;
 
-template <int NT, int KPT>
-cudaError_t launch_reg(const uint16_t* scores, int Nq, int64_t q_pos0, int64_t E, int m, int k,
+template <int NT, int KPT, bool F32>
+cudaError_t launch_reg(const void* scores, int Nq, int64_t q_pos0, int64_t E, int m, int k,
                        int32_t* topk_idx, int32_t* topk_cnt, int64_t rows, int C,
                        cudaStream_t stream) {
-  auto kern = topk_reg_kernel<NT, KPT>;
+  auto kern = topk_reg_kernel<NT, KPT, F32>;
   if (C > 8) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
-  ProfScope prof(stream, "topk");
+  ProfScope prof(stream, F32 ? "topk_f32" : "topk");
   return launch_ex(kern, dim3((unsigned)(rows * C)), dim3(NT), 0, stream, (unsigned)C, scores,
                    Nq, q_pos0, E, m, k, topk_idx, topk_cnt);
 }
 
 // Whether clusters of C CTAs of this shape can be resident (sizes above 8 are non-portable).
-template <int NT, int KPT>
+template <int NT, int KPT, bool F32>
 bool reg_cluster_fits(int C) {
   if (C <= 8) return true;
-  auto kern = topk_reg_kernel<NT, KPT>;
+  auto kern = topk_reg_kernel<NT, KPT, F32>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
       cudaSuccess) {
     (void)cudaGetLastError();
@@ -631,28 +686,30 @@ bool reg_cluster_fits(int C) {
   return nclusters > 0;
 }
 
+template <bool F32>
 bool reg_fits_query(int shape, int C) {
   switch (shape) {
-    case 0: return reg_cluster_fits<256, 16>(C);
-    case 1: return reg_cluster_fits<512, 16>(C);
-    case 2: return reg_cluster_fits<1024, 16>(C);
-    default: return reg_cluster_fits<1024, 32>(C);
+    case 0: return reg_cluster_fits<256, 16, F32>(C);
+    case 1: return reg_cluster_fits<512, 16, F32>(C);
+    case 2: return reg_cluster_fits<1024, 16, F32>(C);
+    default: return reg_cluster_fits<1024, 32, F32>(C);
   }
 }
 
-// Answers are cached per (shape, cluster size): 0 unknown, 1 fits, 2 does not.
-bool reg_fits(int shape, int C) {
-  static volatile int8_t cache[4][kMaxRegCluster + 1] = {};
+// Answers are cached per (key width, shape, cluster size): 0 unknown, 1 fits, 2 does not.
+bool reg_fits(int shape, int C, bool f32) {
+  static volatile int8_t cache[2][4][kMaxRegCluster + 1] = {};
   if (C <= 8) return true;
-  if (cache[shape][C] == 0) cache[shape][C] = reg_fits_query(shape, C) ? 1 : 2;
-  return cache[shape][C] == 1;
+  volatile int8_t& c = cache[f32 ? 1 : 0][shape][C];
+  if (c == 0) c = (f32 ? reg_fits_query<true>(shape, C) : reg_fits_query<false>(shape, C)) ? 1 : 2;
+  return c == 1;
 }
 
 // Picks the register-resident shape and cluster size for rows of up to n_max keys: one CTA of
 // 32768 keys per row when there are enough rows to fill the GPU; otherwise the smallest chunk
 // whose cluster (at most 16 CTAs) covers the row while the grid stays within two CTAs per SM.
 // Returns false when no shape covers the row (more than 16 x 32768 keys).
-bool pick_reg(int64_t rows, int64_t n_max, int* shape, int* C) {
+bool pick_reg(int64_t rows, int64_t n_max, int* shape, int* C, bool f32) {
   constexpr int nshapes = (int)(sizeof(kRegShapes) / sizeof(kRegShapes[0]));
   if (n_max <= kRegShapes[nshapes - 1].chunk() && rows >= kNumSMs) {
     *shape = nshapes - 1;
@@ -662,7 +719,7 @@ bool pick_reg(int64_t rows, int64_t n_max, int* shape, int* C) {
   int best = -1, best_c = 0;
   for (int i = 0; i < nshapes; ++i) {
     const int64_t c = (n_max + kRegShapes[i].chunk() - 1) / kRegShapes[i].chunk();
-    if (c > kMaxRegCluster || !reg_fits(i, (int)max((int64_t)1, c))) continue;
+    if (c > kMaxRegCluster || !reg_fits(i, (int)max((int64_t)1, c), f32)) continue;
     best = i;
     best_c = (int)max((int64_t)1, c);
     if (rows * best_c <= 2 * kNumSMs) break;
@@ -712,6 +769,26 @@ cudaError_t launch_topk_t(const uint16_t* scores, int Nq, int64_t q_pos0, int64_
   return cudaLaunchKernelEx(&cfg, kern, scores, Nq, q_pos0, E, m, k, cap, topk_idx, topk_cnt);
 }
 
+template <bool F32>
+cudaError_t launch_reg_shape(int shape, const void* scores, int Nq, int64_t q_pos0, int64_t E,
+                             int m, int k, int32_t* topk_idx, int32_t* topk_cnt, int64_t rows,
+                             int C, cudaStream_t stream) {
+  switch (shape) {
+    case 0:
+      return launch_reg<256, 16, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
+                                      stream);
+    case 1:
+      return launch_reg<512, 16, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
+                                      stream);
+    case 2:
+      return launch_reg<1024, 16, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
+                                       stream);
+    default:
+      return launch_reg<1024, 32, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
+                                       stream);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
@@ -721,26 +798,27 @@ cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, i
   int64_t n_max = min(E, (q_pos0 + Nq) / m);
   if (n_max < 0) n_max = 0;
   int shape = 0, C = 1;
-  if (pick_reg(rows, n_max, &shape, &C)) {
-    switch (shape) {
-      case 0:
-        return launch_reg<256, 16>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C, stream);
-      case 1:
-        return launch_reg<512, 16>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C, stream);
-      case 2:
-        return launch_reg<1024, 16>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
-                                    stream);
-      default:
-        return launch_reg<1024, 32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
-                                    stream);
-    }
-  }
+  if (pick_reg(rows, n_max, &shape, &C, false))
+    return launch_reg_shape<false>(shape, scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows,
+                                   C, stream);
   // rows longer than 16 x 32768 keys: clusters of up to 16 CTAs staging their chunks in
   // shared memory
   int Cs = 1;
   while (Cs < 16 && (n_max + Cs - 1) / Cs > kMaxChunkKeys) Cs <<= 1;
   return launch_topk_t<kClusterThreads>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows,
                                         n_max, Cs, kMaxChunkKeys, stream);
+}
+
+cudaError_t launch_topk_f32(const float* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
+                            int k, int32_t* topk_idx, int32_t* topk_cnt, cudaStream_t stream) {
+  const int64_t rows = (int64_t)B * Nq;
+  if (rows <= 0) return cudaSuccess;
+  int64_t n_max = min(E, (q_pos0 + Nq) / m);
+  if (n_max < 0) n_max = 0;
+  int shape = 0, C = 1;
+  if (!pick_reg(rows, n_max, &shape, &C, true)) return cudaErrorInvalidValue;
+  return launch_reg_shape<true>(shape, scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
+                                stream);
 }
 
 }  // namespace csa

@@ -105,6 +105,21 @@ def test_index_key_and_quantizer_validation(lib):
     assert q(x, 4, 96, c, sc, None) == 5
 
 
+def test_fp32_score_path_validation(lib):
+    f = lib.csa_topk_f32
+    s_, i_, c_ = _p(ALN), _p(ALN * 2), _p(ALN * 3)
+    assert f(None, 1, 1, 0, 100, 4, 8, i_, c_, None) == 1
+    assert f(_p(ALN + 4), 1, 1, 0, 100, 4, 8, i_, c_, None) == 3
+    assert f(s_, 1, 1, 0, 100, 4, 0, i_, c_, None) == 1              # k < 1
+    # rows above 16 x 32768 visible entries are not implemented for FP32 scores
+    assert f(s_, 1, 1, 4 * 600000 - 1, 600000, 4, 8, i_, c_, None) == 5
+    g = lib.csa_index_scores
+    a = _p(ALN)
+    assert g(a, a, a, a, 1, 1, 0, 100, 4, 4, 64, None, None, None) == 1    # no BF16 buffer
+    assert g(a, a, a, a, 1, 1, 0, 100, 4, 4, 64, a, _p(ALN + 8), None) == 3
+    assert g(a, a, a, a, 1, 1, 0, 100, 4, 4, 48, a, None, None) == 5
+
+
 def test_descriptor_struct_layout():
     # 15 pointers, 9 ints (+4 padding), 3 int64, 1 pointer / 8 pointers, 6 ints, 3 int64
     assert ctypes.sizeof(N.CsaLayerDesc) == 15 * 8 + 9 * 4 + 4 + 3 * 8 + 8
