@@ -87,7 +87,9 @@ CSA_DEV void work_sync(int n) { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memor
 
 // H_I heads, NB = d_I / 32 scale blocks per vector, SW = 2 for the bulk-copy path (each head's
 // blocks in place and swapped), else 1; CPQ = H_I * NB * SW MMA columns per query.
-template <int H_I, int NB, int SW, bool PREFILL, int EW = PREFILL ? 4 : 2>
+// F32OUT: also write the exact FP32 scores (p.scores_f32); a separate instantiation so that the
+// path without them carries no extra instruction in its issue-bound epilogue.
+template <int H_I, int NB, int SW, bool PREFILL, bool F32OUT, int EW = PREFILL ? 4 : 2>
 __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                                                            const IdxParams p) {
   constexpr int CPQ = H_I * NB * SW;
@@ -432,7 +434,8 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
                   sc += 0.0f;  // -0 -> +0
                   if (j < qvis[ql]) {
                     srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
-                    if (p.scores_f32) p.scores_f32[(srow - p.scores) + (int64_t)ql * p.E] = sc;
+                    if constexpr (F32OUT)
+                      p.scores_f32[(srow - p.scores) + (int64_t)ql * p.E] = sc;
                   }
                 }
               }
@@ -504,7 +507,8 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
                 sc += 0.0f;  // -0 -> +0
                 if (j < qvis[ql]) {
                   srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
-                  if (p.scores_f32) p.scores_f32[(srow - p.scores) + (int64_t)ql * p.E] = sc;
+                  if constexpr (F32OUT)
+                    p.scores_f32[(srow - p.scores) + (int64_t)ql * p.E] = sc;
                 }
               }
             }
@@ -534,10 +538,10 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
   }
 }
 
-template <int H_I, int NB, int SW, bool PREFILL>
-cudaError_t launch_t(const CUtensorMap* kmap, const IdxParams& prm, const IndexerPlan& plan, int B,
-                     cudaStream_t stream) {
-  auto kern = indexer_kernel<H_I, NB, SW, PREFILL>;
+template <int H_I, int NB, int SW, bool PREFILL, bool F32OUT>
+cudaError_t launch_t1(const CUtensorMap* kmap, const IdxParams& prm, const IndexerPlan& plan, int B,
+                      cudaStream_t stream) {
+  auto kern = indexer_kernel<H_I, NB, SW, PREFILL, F32OUT>;
   constexpr int EW = PREFILL ? 4 : 2;
   const size_t smem = smem_bytes((prm.Nq == 1 ? kMaxSeqPerCta : 1) * prm.ncols);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -547,6 +551,13 @@ cudaError_t launch_t(const CUtensorMap* kmap, const IdxParams& prm, const Indexe
             (unsigned)(prm.Nq == 1 ? 1 : B));
   ProfScope prof(stream, "indexer_mxf4");
   return launch_ex(kern, grid, dim3(threads_for(EW)), smem, stream, 1, *kmap, prm);
+}
+
+template <int H_I, int NB, int SW, bool PREFILL>
+cudaError_t launch_t(const CUtensorMap* kmap, const IdxParams& prm, const IndexerPlan& plan, int B,
+                     cudaStream_t stream) {
+  return prm.scores_f32 ? launch_t1<H_I, NB, SW, PREFILL, true>(kmap, prm, plan, B, stream)
+                        : launch_t1<H_I, NB, SW, PREFILL, false>(kmap, prm, plan, B, stream);
 }
 
 int next_pow2_at_least32(int x) {
