@@ -265,6 +265,66 @@ typedef struct hca_layer_desc {
 
 csa_status csa_hca_layer_pair(const csa_layer_desc* csa, const hca_layer_desc* hca,
                               void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------------------------------
+ * Paged heterogeneous KV cache with incremental decode-time compression.
+ * Lighthouse "deep deepseek v4 release" 八.7: the cache is split into a state cache (the
+ * sliding window and the tail of tokens not yet compressed) and a classical cache (the
+ * compressed entries), with cache blocks aligned to lcm(m, m') tokens. Layout here (one layer):
+ *   classical cache  pools of pages; page p holds the entries of CSA_PAGE_TOKENS = 4096
+ *                    consecutive tokens of one sequence (4096 / m entries, and for CSA their
+ *                    index keys); block_table[b * max_blocks + i] is the page of tokens
+ *                    [4096 i, 4096 (i + 1)) of sequence b. 4096 is a multiple of
+ *                    lcm(4, 128) = 128, so a block of m tokens never straddles pages.
+ *   state cache      rings of the last CSA_RING_TOKENS = 256 raw tokens per sequence: the token
+ *                    at position p sits in slot p % 256 of ring_k, ring_v, ring_logits (and, for
+ *                    CSA, ring_xi: the index-key rows the indexer's keys are pooled from).
+ * csa_paged_decode_step appends token N of every sequence (all sequences hold N tokens before
+ * the call) to the state cache; when N closes a block (N % m == m - 1) it pools the block from
+ * the ring into its page, with csa_compress's arithmetic (and, for CSA with xi rows, the index
+ * key as csa_compress_index_keys); then it decodes the new token against the cache exactly as
+ * the flat path does at t = N: CSA scores the (N + 1) / m visible entries with the indexer,
+ * selects the top-k and attends to the selected entries plus the window; HCA attends densely.
+ * Supported: d = 128, W <= 128; CSA: m a power of two <= 32, d_I = 64, H_I <= 4; HCA: m a
+ * power of two <= 128. Every pointer 16-byte aligned (ring_logits, logit_new: 4). Pages must
+ * be mapped (block_table entries in [0, n_pages)) for every block up to token N; an unmapped
+ * page is flagged in the device status word and its keys are left out. The caller owns the
+ * pools, rings and block table; the call writes the new token's ring slots, at most one entry
+ * per layer (plus its index key), out, lse, topk_idx, topk_cnt and the workspace.
+ * ---------------------------------------------------------------------------------------- */
+#define CSA_PAGE_TOKENS 4096
+#define CSA_RING_TOKENS 256
+
+typedef struct csa_paged_layer {
+  int kind;                     /* 0: CSA (indexer, top-k, sparse attention), 1: HCA (dense) */
+  int B, H, d, m, W, k, H_I, d_I;
+  int64_t N;                    /* tokens per sequence before this step */
+  uint16_t* k_pool;             /* [n_pages, 4096 / m, d] bf16 entries */
+  uint16_t* v_pool;
+  uint8_t* ki_codes_pool;       /* CSA: [n_pages, 4096 / m, d_I / 2] packed e2m1 */
+  uint8_t* ki_scales_pool;      /* CSA: [n_pages, 4096 / m, d_I / 32] UE8M0 */
+  const int32_t* block_table;   /* [B, max_blocks] */
+  int n_pages, max_blocks;
+  uint16_t* ring_k;             /* [B, 256, d] bf16 */
+  uint16_t* ring_v;
+  float* ring_logits;           /* [B, 256] */
+  uint16_t* ring_xi;            /* CSA: [B, 256, d_I] bf16, or NULL (keys written elsewhere) */
+  const uint16_t* k_new;        /* [B, d] the appended token's K row */
+  const uint16_t* v_new;        /* [B, d] */
+  const float* logit_new;       /* [B] its pooling logit */
+  const uint16_t* xi_new;       /* CSA: [B, d_I] its index-key row (with ring_xi) */
+  const uint16_t* q;            /* [B, H, d] the new token's queries */
+  const uint8_t* qi_codes;      /* CSA: [B, H_I, d_I / 2] */
+  const uint8_t* qi_scales;     /* CSA: [B, H_I, d_I / 32] */
+  uint16_t* out;                /* [B, H, d] */
+  float* lse;                   /* optional [B, H] */
+  int32_t* topk_idx;            /* CSA: [B, k] */
+  int32_t* topk_cnt;            /* CSA: [B] */
+} csa_paged_layer;
+
+size_t csa_paged_decode_workspace_size(const csa_paged_layer* layer);
+csa_status csa_paged_decode_step(const csa_paged_layer* layer, void* ws, size_t ws_bytes,
+                                 void* stream);
 size_t csa_hca_layer_pair_workspace_size(const csa_layer_desc* csa, const hca_layer_desc* hca);
 
 /* ----------------------------------------------------------------------------------------

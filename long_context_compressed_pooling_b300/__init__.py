@@ -10,7 +10,10 @@ from ._native import (  # noqa: F401
     CSA_OK,
     CsaError,
     LIB_PATH,
+    PAGE_TOKENS,
     PreparedLayerPair,
+    PreparedPagedStep,
+    RING_TOKENS,
     compress,
     compress_index_keys,
     csa_attend,
@@ -21,6 +24,7 @@ from ._native import (  # noqa: F401
     index_topk,
     layer_pair,
     load_library,
+    paged_decode_step,
     profiler_collect,
     profiler_enable,
     quantize_mxfp4,

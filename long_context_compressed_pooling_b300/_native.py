@@ -50,6 +50,21 @@ class HcaLayerDesc(ctypes.Structure):
                [(n, _L) for n in ("N", "q_pos0", "compress_begin")]
 
 
+class PagedLayerDesc(ctypes.Structure):
+    _fields_ = [(n, _I) for n in ("kind", "B", "H", "d", "m", "W", "k", "H_I", "d_I")] + \
+               [("N", _L)] + \
+               [(n, _P) for n in ("k_pool", "v_pool", "ki_codes_pool", "ki_scales_pool",
+                                  "block_table")] + \
+               [(n, _I) for n in ("n_pages", "max_blocks")] + \
+               [(n, _P) for n in ("ring_k", "ring_v", "ring_logits", "ring_xi", "k_new", "v_new",
+                                  "logit_new", "xi_new", "q", "qi_codes", "qi_scales", "out",
+                                  "lse", "topk_idx", "topk_cnt")]
+
+
+PAGE_TOKENS = 4096
+RING_TOKENS = 256
+
+
 class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("launches", _I), ("total_ms", ctypes.c_double)]
 
@@ -75,6 +90,8 @@ _SIGS = {
     "csa_hca_layer_pair": (_I, [ctypes.POINTER(CsaLayerDesc), ctypes.POINTER(HcaLayerDesc), _P, _Z, _P]),
     "csa_hca_layer_pair_workspace_size": (_Z, [ctypes.POINTER(CsaLayerDesc),
                                                ctypes.POINTER(HcaLayerDesc)]),
+    "csa_paged_decode_step": (_I, [ctypes.POINTER(PagedLayerDesc), _P, _Z, _P]),
+    "csa_paged_decode_workspace_size": (_Z, [ctypes.POINTER(PagedLayerDesc)]),
     "csa_get_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32)]),
     "csa_status_string": (ctypes.c_char_p, [_I]),
     "csa_abi_version": (_I, []),
@@ -361,6 +378,49 @@ class PreparedLayerPair:
     def __call__(self) -> None:
         _check("csa_hca_layer_pair", self.lib.csa_hca_layer_pair(
             self.cd, self.hd, self.wsp, self.wsb, _stream(self.dev)))
+
+
+def _paged_desc(L: Dict) -> PagedLayerDesc:
+    dsc = PagedLayerDesc()
+    dsc.kind = 0 if L["kind"] == "csa" else 1
+    B, H, d = L["q"].shape
+    dsc.B, dsc.H, dsc.d, dsc.m, dsc.W = B, H, d, L["m"], L["W"]
+    dsc.k = L.get("k", 0)
+    if dsc.kind == 0:
+        dsc.H_I, dsc.d_I = L["qi_codes"].shape[1], 2 * L["qi_codes"].shape[2]
+    dsc.N = L["N"]
+    for f in ("k_pool", "v_pool", "ki_codes_pool", "ki_scales_pool", "block_table", "ring_k",
+              "ring_v", "ring_logits", "ring_xi", "k_new", "v_new", "logit_new", "xi_new", "q",
+              "qi_codes", "qi_scales", "out", "lse", "topk_idx", "topk_cnt"):
+        setattr(dsc, f, _ptr(L.get(f)))
+    dsc.n_pages = L["k_pool"].shape[0]
+    dsc.max_blocks = L["block_table"].shape[1]
+    return dsc
+
+
+class PreparedPagedStep:
+    """One decode step on a paged cache layer (csa_paged_decode_step): the dict holds the pools,
+    rings, block table, the step's token inputs and outputs, and kind ('csa' / 'hca'), m, W, k,
+    N (tokens already cached). The descriptor and workspace are built once; calling enqueues the
+    step on torch's current stream."""
+
+    def __init__(self, layer: Dict, ws: Optional[torch.Tensor] = None):
+        self.lib = load_library()
+        self.layer = layer
+        self.dsc = ctypes.pointer(_paged_desc(layer))
+        self.dev = layer["q"].device
+        need = self.lib.csa_paged_decode_workspace_size(self.dsc)
+        self.ws, self.wsb = _ws(need, self.dev, ws)
+        self.wsp = _ptr(self.ws)
+
+    def __call__(self) -> None:
+        _check("csa_paged_decode_step", self.lib.csa_paged_decode_step(
+            self.dsc, self.wsp, self.wsb, _stream(self.dev)))
+
+
+def paged_decode_step(layer: Dict, ws: Optional[torch.Tensor] = None):
+    """One csa_paged_decode_step call on the layer dict (see PreparedPagedStep)."""
+    PreparedPagedStep(layer, ws)()
 
 
 def workspace_sizes(csa: Optional[Dict], hca: Optional[Dict]) -> int:

@@ -170,7 +170,8 @@ csa_status check_index_keys(const uint16_t* xi_raw, const float* logits, int B, 
 // ---- internal runners (arguments already validated) -----------------------------------------
 csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const uint8_t* ki_codes,
                        const uint8_t* ki_scales, int B, int Nq, int64_t q_pos0, int64_t E, int m,
-                       int H_I, int d_I, uint16_t* sc, float* scores_f32, cudaStream_t st);
+                       int H_I, int d_I, uint16_t* sc, float* scores_f32, cudaStream_t st,
+                       const PagedLayout* paged = nullptr);
 
 csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
                           const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
@@ -187,7 +188,8 @@ csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
 // The indexer alone: BF16 scores (and, when scores_f32 is set, the exact FP32 scores).
 csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const uint8_t* ki_codes,
                        const uint8_t* ki_scales, int B, int Nq, int64_t q_pos0, int64_t E, int m,
-                       int H_I, int d_I, uint16_t* sc, float* scores_f32, cudaStream_t st) {
+                       int H_I, int d_I, uint16_t* sc, float* scores_f32, cudaStream_t st,
+                       const PagedLayout* paged) {
   if (E > 0) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return CSA_ERR_CUDA;
@@ -195,17 +197,19 @@ csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const 
     if (!status) return CSA_ERR_CUDA;
     alignas(64) CUtensorMap map;
     const cuuint64_t row = (cuuint64_t)(d_I / 2);
-    cuuint64_t dims[3] = {row, (cuuint64_t)E, (cuuint64_t)B};
-    cuuint64_t strides[2] = {row, row * (cuuint64_t)E};
+    // paged keys: one flat run of pool rows (the copies then go through the block table)
+    const cuuint64_t rows = paged ? (cuuint64_t)paged->n_pages * (kPageTokens / m) : (cuuint64_t)E;
+    cuuint64_t dims[3] = {row, rows, paged ? (cuuint64_t)1 : (cuuint64_t)B};
+    cuuint64_t strides[2] = {row, row * rows};
     cuuint32_t box[3] = {32, 128, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(ki_codes), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return CSA_ERR_CUDA;
-    const IndexerPlan plan = plan_indexer(B, Nq, E, H_I, d_I);
+    const IndexerPlan plan = plan_indexer(B, Nq, E, H_I, d_I, paged != nullptr);
     cudaError_t e = launch_indexer(&map, ki_codes, qi_codes, qi_scales, ki_scales, sc, B, Nq, q_pos0, E, m,
-                                   H_I, d_I, plan, status, st, scores_f32);
+                                   H_I, d_I, plan, status, st, scores_f32, paged);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   }
   return CSA_OK;
@@ -240,9 +244,103 @@ size_t pair_hca_ws(const hca_layer_desc* h) {
   const int64_t E = h->N / (h->m > 0 ? h->m : 1);
   return round_up(attend_workspace_bytes(h->B * h->Nq, h->H, h->d, E + h->W), 256);
 }
+size_t paged_ws(const csa_paged_layer* L) {
+  if (!L || L->m < 1) return 0;
+  const int64_t E = (L->N + 1) / L->m;
+  const size_t a = L->kind == 0 ? index_ws_bytes(L->B, 1, E, 0) : 0;
+  const int64_t keys = (L->kind == 0 ? (int64_t)L->k : E) + L->W;
+  const size_t b = attend_workspace_bytes(L->B, L->H, L->d, keys);
+  return round_up(a > b ? a : b, 256);
+}
+
+bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+csa_status check_paged(const csa_paged_layer* L) {
+  if (!L) return CSA_ERR_INVALID_ARG;
+  const bool csa_kind = L->kind == 0;
+  if (L->kind != 0 && L->kind != 1) return CSA_ERR_INVALID_ARG;
+  if (!L->k_pool || !L->v_pool || !L->block_table || !L->ring_k || !L->ring_v ||
+      !L->ring_logits || !L->k_new || !L->v_new || !L->logit_new || !L->q || !L->out)
+    return CSA_ERR_INVALID_ARG;
+  if (csa_kind && (!L->ki_codes_pool || !L->ki_scales_pool || !L->qi_codes || !L->qi_scales ||
+                   !L->topk_idx || !L->topk_cnt || (L->ring_xi && !L->xi_new)))
+    return CSA_ERR_INVALID_ARG;
+  if (!al16(L->k_pool) || !al16(L->v_pool) || !al16(L->ring_k) || !al16(L->ring_v) ||
+      !al16(L->k_new) || !al16(L->v_new) || !al16(L->q) || !al16(L->out) ||
+      !al16(L->block_table) || (uintptr_t)L->ring_logits % 4 || (uintptr_t)L->logit_new % 4 ||
+      (L->lse && (uintptr_t)L->lse % 4))
+    return CSA_ERR_ALIGN;
+  if (csa_kind && (!al16(L->ki_codes_pool) || !al16(L->ki_scales_pool) || !al16(L->qi_codes) ||
+                   !al16(L->topk_idx) || !al16(L->topk_cnt) ||
+                   (L->ring_xi && (!al16(L->ring_xi) || !al16(L->xi_new)))))
+    return CSA_ERR_ALIGN;
+  if (L->B < 1 || L->H < 1 || L->N < 0 || L->W < 0 || L->n_pages < 1 || L->max_blocks < 1)
+    return CSA_ERR_INVALID_ARG;
+  if ((L->N + 1 + kPageTokens - 1) / kPageTokens > L->max_blocks) return CSA_ERR_SHAPE;
+  if (L->d != 128 || L->W > 128 || !pow2(L->m)) return CSA_ERR_UNSUPPORTED;
+  if (csa_kind && (L->m > 32 || L->d_I != 64 || !(L->H_I == 1 || L->H_I == 2 || L->H_I == 4) ||
+                   L->k < 1))
+    return CSA_ERR_UNSUPPORTED;
+  if (!csa_kind && L->m > 128) return CSA_ERR_UNSUPPORTED;
+  if ((int64_t)L->B * L->max_blocks > ((int64_t)1 << 31)) return CSA_ERR_UNSUPPORTED;
+  return CSA_OK;
+}
 }  // namespace
 
 extern "C" {
+
+size_t csa_paged_decode_workspace_size(const csa_paged_layer* layer) {
+  return check_paged(layer) == CSA_OK ? paged_ws(layer) : 0;
+}
+
+csa_status csa_paged_decode_step(const csa_paged_layer* L, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  csa_status s = check_paged(L);
+  if (s != CSA_OK) return s;
+  const size_t need = paged_ws(L);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !al16(ws))) return CSA_ERR_WORKSPACE;
+  uint32_t* status = status_word();
+  if (!status) return CSA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const bool csa_kind = L->kind == 0;
+  PagedLayout P;
+  P.d = L->d;
+  P.m = L->m;
+  P.d_I = csa_kind ? L->d_I : 0;
+  P.k_pool = L->k_pool;
+  P.v_pool = L->v_pool;
+  P.ki_codes_pool = csa_kind ? L->ki_codes_pool : nullptr;
+  P.ki_scales_pool = csa_kind ? L->ki_scales_pool : nullptr;
+  P.block_table = L->block_table;
+  P.n_pages = L->n_pages;
+  P.max_blocks = L->max_blocks;
+  P.ring_k = L->ring_k;
+  P.ring_v = L->ring_v;
+  P.ring_logits = L->ring_logits;
+  P.ring_xi = csa_kind ? L->ring_xi : nullptr;
+  const int64_t t = L->N;  // the appended token's position
+  if (launch_paged_append(P, L->B, L->k_new, L->v_new, L->logit_new,
+                          csa_kind ? L->xi_new : nullptr, t, status, st) != cudaSuccess)
+    return CSA_ERR_CUDA;
+  const int64_t E = (t + 1) / L->m;  // entries visible to the new token
+  AttendArgs a{L->q, L->k_pool, L->v_pool, nullptr, nullptr, L->ring_k, L->ring_v, L->out, L->lse,
+               E, t + 1, t, 0, L->m, L->W, L->B, 1, L->H, L->d};
+  a.paged = &P;
+  if (csa_kind) {
+    uint16_t* sc = static_cast<uint16_t*>(ws);
+    s = run_indexer(L->qi_codes, L->qi_scales, L->ki_codes_pool, L->ki_scales_pool, L->B, 1, t, E,
+                    L->m, L->H_I, L->d_I, sc, nullptr, st, &P);
+    if (s != CSA_OK) return s;
+    if (launch_topk(sc, L->B, 1, t, E, L->m, L->k, L->topk_idx, L->topk_cnt, st) != cudaSuccess)
+      return CSA_ERR_CUDA;
+    a.topk_idx = L->topk_idx;
+    a.topk_cnt = L->topk_cnt;
+    a.k = L->k;
+    return from_cuda(launch_attend(a, (int64_t)L->k + L->W, ws, status, st));
+  }
+  return from_cuda(launch_attend(a, E + L->W, ws, status, st));
+}
+
 
 int csa_abi_version(void) { return 2; }
 

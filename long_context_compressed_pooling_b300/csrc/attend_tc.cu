@@ -79,6 +79,11 @@ struct TcParams {
   float* ws_ml;  // [n_splits, tokens, H, 2] reference maximum and sum
   int64_t E, N, q_pos0;
   int64_t fresh_from;  // dense: entries below it may be read before the predecessor completes
+  // paged cache (block_table != null): entry j of sequence b is row (page << page_shift) +
+  // (j & page_mask) of the entry pools, page = block_table[b][j >> page_shift]; window token at
+  // position pos is row b * kRingTokens + (pos & (kRingTokens - 1)) of the raw rings
+  const int32_t* block_table;
+  int max_blocks, n_pages, page_shift;
   int k, m, W, Nq, H, n_splits, tokens;
   int sparse;
   int cluster_merge;
@@ -218,12 +223,22 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
       if (key < n_keys) {
         if (key < n_sel) {
           const int64_t j = p.sparse ? (int64_t)p.topk_idx[tok * p.k + key] : key;
-          if (j < 0 || j >= p.E)
+          if (j < 0 || j >= p.E) {
             atomicOr(p.status, kFlagBadIndex);  // flagged; the row is zero-filled and masked
-          else
+          } else if (p.block_table) {
+            const int64_t blk = j >> p.page_shift;
+            const int pg = blk < p.max_blocks ? p.block_table[b * p.max_blocks + blk] : -1;
+            if (pg < 0 || pg >= p.n_pages)
+              atomicOr(p.status, kFlagBadIndex);  // unmapped page: zero-filled and masked
+            else
+              cd = (((int64_t)pg << p.page_shift) + (j & ((1 << p.page_shift) - 1))) * kD;
+          } else {
             cd = (b * p.E + j) * kD;
+          }
         } else {
-          cd = ((b * p.N + w0 + (key - n_sel)) * kD) | kRawBit;
+          const int64_t pos = w0 + (key - n_sel);
+          cd = ((p.block_table ? b * kRingTokens + (pos & (kRingTokens - 1)) : b * p.N + pos) *
+                kD) | kRawBit;
         }
       }
       const uint32_t vbits = __ballot_sync(0xffffffffu, cd >= 0);
@@ -627,6 +642,12 @@ cudaError_t launch_attend_tc(const AttendArgs& a, int n_splits, int cluster, flo
   prm.N = a.N;
   prm.q_pos0 = a.q_pos0;
   prm.fresh_from = a.fresh_from;
+  prm.block_table = a.paged ? a.paged->block_table : nullptr;
+  prm.max_blocks = a.paged ? a.paged->max_blocks : 0;
+  prm.n_pages = a.paged ? a.paged->n_pages : 0;
+  prm.page_shift = 0;
+  if (a.paged)
+    while ((1 << prm.page_shift) < kPageTokens / a.m) ++prm.page_shift;
   prm.k = a.k;
   prm.m = a.m;
   prm.W = a.W;

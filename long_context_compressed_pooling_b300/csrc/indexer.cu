@@ -72,6 +72,10 @@ struct IdxParams {
   int64_t total_tiles;
   const uint8_t* ki_codes;   // [B, E, 32] (bulk-copy path)
   uint32_t* status;
+  // paged cache (bulk-copy path only): the keys of entry j of sequence b are row
+  // (page << page_shift) + (j & page_mask) of the key pools, page = block_table[b][j >> page_shift]
+  const int32_t* block_table;
+  int max_blocks, n_pages, page_shift;
 };
 
 // Shared memory for a launch whose B operand has `brows` rows (decode: 8 sequences x ncols;
@@ -190,10 +194,23 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
     // before the predecessor-dependent part. Every bulk copy costs ~0.3 us to issue whatever its
     // size, so a slot (8 tiles) is one code copy and one scale copy whenever the tiles form one
     // contiguous span of HBM (always, unless a ragged sequence tail intervenes).
+    // A page holds whole tiles, so a paged tile is always copied whole (its rows past the
+    // visible entries are never scored).
     auto tile_bytes = [&](int it) -> uint32_t {  // rows that exist in this tile x 32 B
+      if (p.block_table) return (uint32_t)kTileM * kRowBytes;
       return (uint32_t)min((int64_t)kTileM, p.E - (int64_t)tile_row0(it)) * kRowBytes;
     };
-    auto tile_addr = [&](int it) -> int64_t {  // entry index of the tile's first row
+    auto tile_addr = [&](int it) -> int64_t {  // entry (pool row) of the tile's first row
+      if (p.block_table) {
+        const int j = tile_row0(it);
+        const int blk = j >> p.page_shift;
+        int pg = blk < p.max_blocks ? p.block_table[(int64_t)tile_seq(it) * p.max_blocks + blk] : -1;
+        if (pg < 0 || pg >= p.n_pages) {
+          atomicOr(p.status, kFlagBadIndex);  // unmapped page: scores of page 0, flagged
+          pg = 0;
+        }
+        return ((int64_t)pg << p.page_shift) + (j & ((1 << p.page_shift) - 1));
+      }
       return (int64_t)tile_seq(it) * p.E + tile_row0(it);
     };
     auto issue_unit = [&](int u) {
@@ -573,9 +590,10 @@ bool indexer_bulk_path(int H_I, int d_I, int64_t E, int Nq) {
   return Nq == 1 && d_I == 64 && H_I <= 4 && E % 8 == 0;
 }
 
-IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I) {
+IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I, bool paged) {
   IndexerPlan pl{};
-  const int cpq = H_I * (d_I / 32) * (indexer_bulk_path(H_I, d_I, E, Nq) ? 2 : 1);
+  // paged keys are copied whole-tile from their pages: the bulk path whatever E is
+  const int cpq = H_I * (d_I / 32) * (indexer_bulk_path(H_I, d_I, paged ? 8 : E, Nq) ? 2 : 1);
   if (Nq == 1) {  // two CTAs per SM: 3 x 64 + 32 scale columns fit in 256
     pl.QN = 1;
     pl.ncols = cpq > 16 ? 32 : 16;
@@ -615,8 +633,17 @@ cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, con
                            const uint8_t* qi_scales, const uint8_t* ki_scales, uint16_t* scores,
                            int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I, int d_I,
                            const IndexerPlan& plan, uint32_t* status, cudaStream_t stream,
-                           float* scores_f32) {
+                           float* scores_f32, const PagedLayout* paged) {
   IdxParams prm;
+  prm.block_table = paged ? paged->block_table : nullptr;
+  prm.max_blocks = paged ? paged->max_blocks : 0;
+  prm.n_pages = paged ? paged->n_pages : 0;
+  prm.page_shift = 0;
+  if (paged) {
+    while ((1 << prm.page_shift) < kPageTokens / m) ++prm.page_shift;
+    if (!indexer_bulk_path(H_I, d_I, 8, Nq) || (1 << prm.page_shift) % kTileM != 0)
+      return cudaErrorInvalidValue;  // paged keys: decode bulk-copy path, whole tiles per page
+  }
   prm.qi_codes = qi_codes;
   prm.qi_scales = qi_scales;
   prm.ki_scales = ki_scales;
@@ -638,7 +665,7 @@ cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, con
   prm.ki_codes = ki_codes;
   prm.status = status;
   const int NB = d_I / 32;
-  const int SW = indexer_bulk_path(H_I, d_I, E, Nq) ? 2 : 1;
+  const int SW = indexer_bulk_path(H_I, d_I, paged ? 8 : E, Nq) ? 2 : 1;
 #define CSA_IDX_CASE(HH, NN, SS, PP)                                          \
   if (H_I == HH && NB == NN && SW == SS && prefill == PP)                     \
     return launch_t<HH, NN, SS, PP>(kmap, prm, plan, B, stream);

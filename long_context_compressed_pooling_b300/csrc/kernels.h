@@ -40,6 +40,28 @@ cudaError_t launch_ex(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem
 
 constexpr int kNumSMs = 148;
 
+// ---- paged heterogeneous KV cache (one layer; paged.cu has the layout) ------------------------
+constexpr int kPageTokens = 4096;  // tokens per classical-cache page (a multiple of lcm(4, 128))
+constexpr int kRingTokens = 256;   // raw tokens kept per sequence in the state cache
+struct PagedLayout {
+  int d, m, d_I;
+  uint16_t* k_pool;                // [n_pages, kPageTokens / m, d] entries
+  uint16_t* v_pool;
+  uint8_t* ki_codes_pool;          // CSA: [n_pages, kPageTokens / m, d_I / 2] (null for HCA)
+  uint8_t* ki_scales_pool;         // CSA: [n_pages, kPageTokens / m, d_I / 32]
+  const int32_t* block_table;      // [B, max_blocks]: page of tokens [4096 i, 4096 (i + 1))
+  int n_pages, max_blocks;
+  uint16_t* ring_k;                // [B, kRingTokens, d] raw rows at slot (position % 256)
+  uint16_t* ring_v;
+  float* ring_logits;              // [B, kRingTokens]
+  uint16_t* ring_xi;               // CSA: [B, kRingTokens, d_I] index-key rows (or null)
+};
+// Appends token t of every sequence to the state cache and compresses the block it closes.
+cudaError_t launch_paged_append(const PagedLayout& L, int B, const uint16_t* k_new,
+                                const uint16_t* v_new, const float* logit_new,
+                                const uint16_t* xi_new, int64_t t, uint32_t* status,
+                                cudaStream_t stream);
+
 // The library's device status word on the current device (defined in abi.cu).
 uint32_t* device_status_word();
 
@@ -66,13 +88,13 @@ struct IndexerPlan {
   int n_splits;  // entry-tile splits per (sequence, query group)
   int tmem_cols; // tensor-memory columns allocated per CTA
 };
-IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I);
+IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I, bool paged = false);
 bool indexer_bulk_path(int H_I, int d_I, int64_t E, int Nq);
 cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, const uint8_t* qi_codes,
                            const uint8_t* qi_scales, const uint8_t* ki_scales, uint16_t* scores,
                            int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I, int d_I,
                            const IndexerPlan& plan, uint32_t* status, cudaStream_t stream,
-                           float* scores_f32 = nullptr);
+                           float* scores_f32 = nullptr, const PagedLayout* paged = nullptr);
 
 // ---- top-k over BF16 scores ------------------------------------------------------------------
 cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
@@ -95,6 +117,8 @@ struct AttendArgs {
   float* lse;
   int64_t E, N, q_pos0;
   int k, m, W, B, Nq, H, d;
+  // Paged cache: entries through the block table, window rows from the ring (d = 128 only).
+  const PagedLayout* paged = nullptr;
   // Dense attention only: entries [0, fresh_from) are inputs of this launch, and every kernel
   // before the one that precedes it on the stream has completed, so they may be read before
   // waiting for that predecessor; entries from fresh_from on may be its output. 0: wait first.

@@ -120,6 +120,35 @@ def test_fp32_score_path_validation(lib):
     assert g(a, a, a, a, 1, 1, 0, 100, 4, 4, 48, a, None, None) == 5
 
 
+def _paged(**kw):
+    d = N.PagedLayerDesc()
+    d.kind, d.B, d.H, d.d, d.m, d.W, d.k, d.H_I, d.d_I = 0, 2, 64, 128, 4, 128, 64, 4, 64
+    d.N, d.n_pages, d.max_blocks = 5000, 8, 2
+    for f in ("k_pool", "v_pool", "ki_codes_pool", "ki_scales_pool", "block_table", "ring_k",
+              "ring_v", "ring_logits", "k_new", "v_new", "logit_new", "q", "qi_codes",
+              "qi_scales", "out", "topk_idx", "topk_cnt"):
+        setattr(d, f, ALN)
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return ctypes.pointer(d)
+
+
+def test_paged_validation(lib):
+    f = lambda **kw: lib.csa_paged_decode_step(_paged(**kw), None, 0, None)
+    assert f(kind=2) == 1
+    assert f(q=None) == 1
+    assert f(ring_xi=ALN) == 1                 # index-key rows in the ring but no new row
+    assert f(k_pool=ALN + 8) == 3
+    assert f(N=3 * 4096) == 2                  # the appended token beyond the block table
+    assert f(W=200) == 5
+    assert f(m=64) == 5                        # CSA pages must hold whole indexer tiles
+    assert f(d_I=32) == 5
+    assert f(kind=1, m=256) == 5
+    assert f() == 4                            # valid descriptor, no workspace
+    assert lib.csa_paged_decode_workspace_size(_paged()) > 0
+    assert lib.csa_paged_decode_workspace_size(_paged(kind=2)) == 0
+
+
 def test_descriptor_struct_layout():
     # 15 pointers, 9 ints (+4 padding), 3 int64, 1 pointer / 8 pointers, 6 ints, 3 int64
     assert ctypes.sizeof(N.CsaLayerDesc) == 15 * 8 + 9 * 4 + 4 + 3 * 8 + 8
@@ -127,6 +156,9 @@ def test_descriptor_struct_layout():
     assert N.CsaLayerDesc.xi_raw.offset == 184
     assert ctypes.sizeof(N.HcaLayerDesc) == 8 * 8 + 6 * 4 + 3 * 8
     assert N.HcaLayerDesc.N.offset == 88
+    # 9 ints (+4 padding), int64, 5 pointers, 2 ints, 15 pointers
+    assert ctypes.sizeof(N.PagedLayerDesc) == 9 * 4 + 4 + 8 + 5 * 8 + 2 * 4 + 15 * 8
+    assert N.PagedLayerDesc.N.offset == 40 and N.PagedLayerDesc.ring_k.offset == 96
 
 
 def test_library_is_sm103a_build():
