@@ -40,7 +40,7 @@ DEFAULT_CONFIG = "csa_decode_128k"
 KERNEL_SOURCES = {
     "indexer_mxf4": "indexer.cu", "topk": "topk.cu", "csa_attend": "attend_tc.cu",
     "hca_attend": "attend_tc.cu", "lse_merge": "attend.cu", "compress": "compress.cu",
-    "index_keys": "compress.cu",
+    "index_keys": "compress.cu", "paged_append": "paged.cu",
 }
 
 
@@ -54,6 +54,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
+    ap.add_argument("--paged", action="store_true",
+                    help="decode workloads through the paged KV cache (csa_paged_decode_step: "
+                         "append the step's token to the state cache, pool the block it closes "
+                         "into its page, decode through the block table)")
     ap.add_argument("--topk-compare", action="store_true",
                     help="also time the top-k selector on the same rows' FP32 scores against "
                          "the BF16 selector and report how many FP32 selections BF16 keeps")
@@ -278,6 +282,49 @@ def setup_layer(s, seed, layer_id, dev, index_keys=False):
     return d
 
 
+def setup_paged(s, d, seed, dev):
+    """The paged form of a decode layer set up by setup_layer: its entries (and index keys) in
+    4096-token pages mapped through a shuffled block table, the last 256 raw tokens before the
+    step in the rings; the step appends token N - 1 (closing the block the flat step pools)."""
+    import numpy as np
+    import torch
+    import long_context_compressed_pooling_b300 as csa
+    P, R = csa.PAGE_TOKENS, csa.RING_TOKENS
+    B, N, m = s.B, s.N, s.m
+    per_page = P // m
+    nb = (N + P - 1) // P
+    rng = np.random.default_rng(seed + 77)
+    table = torch.from_numpy(rng.permutation(B * nb).astype(np.int32).reshape(B, nb)).to(dev)
+
+    def pages(flat):
+        E = flat.shape[1]
+        src = flat
+        if E < nb * per_page:
+            src = torch.cat([flat, flat.new_zeros((B, nb * per_page - E) + tuple(flat.shape[2:]))], 1)
+        pool = flat.new_empty((B * nb, per_page) + tuple(flat.shape[2:]))
+        pool[table.view(-1).long()] = src.reshape((B * nb, per_page) + tuple(flat.shape[2:]))
+        return pool
+
+    t = N - 1
+
+    def ring(x):
+        r = x.new_zeros((B, R) + tuple(x.shape[2:]))
+        pos = torch.arange(max(0, t - R), t, device=dev)
+        r[:, pos % R] = x[:, pos]
+        return r
+
+    L = dict(kind=s.kind, m=m, W=s.W, k=getattr(s, "k", 0) if s.kind == "csa" else 0, N=t,
+             block_table=table, k_pool=pages(d["k_cmp"]), v_pool=pages(d["v_cmp"]),
+             ring_k=ring(d["k_raw"]), ring_v=ring(d["v_raw"]), ring_logits=ring(d["logits"]),
+             k_new=d["k_raw"][:, t].contiguous(), v_new=d["v_raw"][:, t].contiguous(),
+             logit_new=d["logits"][:, t].contiguous(), q=d["q"][:, 0], out=d["out"][:, 0])
+    if s.kind == "csa":
+        L.update(ki_codes_pool=pages(d["ki_codes"]), ki_scales_pool=pages(d["ki_scales"]),
+                 qi_codes=d["qi_codes"][:, 0], qi_scales=d["qi_scales"][:, 0],
+                 topk_idx=d["topk_idx"][:, 0], topk_cnt=d["topk_cnt"][:, 0])
+    return L
+
+
 def step_inputs(s, d):
     """(name, device view) of the tensors a serving loop would upload for this step: the queries,
     their indexer queries, and the raw rows / logits / index keys of the tokens the step appends."""
@@ -340,7 +387,14 @@ def run_native(args, rank, world):
     seed = rank_seed(wl, rank)             # every rank decodes its own sequences (weak scaling)
     states = {s.kind: setup_layer(s, seed, li, dev, args.index_keys)
               for li, s in enumerate(wl.layers)}
-    call = csa.PreparedLayerPair(states.get("csa"), states.get("hca"))
+    if args.paged:
+        if wl.mode != "decode" or args.index_keys:
+            raise SystemExit("--paged runs the decode workloads (index keys as inputs)")
+        pl = {s.kind: setup_paged(s, states[s.kind], seed, dev) for s in wl.layers}
+        call = (csa.PreparedPagedPair(pl["csa"], pl["hca"]) if len(pl) == 2
+                else csa.PreparedPagedStep(next(iter(pl.values()))))
+    else:
+        call = csa.PreparedLayerPair(states.get("csa"), states.get("hca"))
     torch.cuda.synchronize()
 
     def barrier():
@@ -395,6 +449,8 @@ def run_native(args, rank, world):
 
     units, unit = units_per_step(wl)
     work = step_work(wl, args.index_keys)
+    if args.paged and "compress" in work:
+        work["paged_append"] = work.pop("compress")  # the append pools the same block
     step_bytes = sum(v["bytes"] for v in work.values())
     step_flops = sum(v["flops"] for v in work.values())
     if units is not None:
@@ -412,7 +468,10 @@ def run_native(args, rank, world):
                       "launch": "cuda_graph" if graph is not None else "eager",
                       "parallelism": f"replicas x{world} (independent sequences per GPU)",
                       "index_keys": ("pooled in the step from bf16 index-key rows"
-                                     if args.index_keys else "inputs (FP4 codes + UE8M0)")},
+                                     if args.index_keys else "inputs (FP4 codes + UE8M0)"),
+                      "cache": ("paged: 4096-token pages through a shuffled block table, "
+                                "256-token state-cache rings"
+                                if args.paged else "flat per-layer buffers")},
            "step_alg_bytes": step_bytes, "step_alg_gbs": step_bytes / (ms_step * 1e-3) / 1e9,
            "step_alg_flops": step_flops}
     if not args.quick:
@@ -458,7 +517,7 @@ def run_native(args, rank, world):
 
     if args.topk_compare and "csa" in states:
         out["topk_compare"] = run_topk_compare(wl.layer("csa"), states["csa"], flush, K, dev)
-    if not args.no_e2e and not args.quick:
+    if not args.no_e2e and not args.quick and not args.paged:
         out["e2e"] = run_e2e(wl, states, call, flush, K, dev, world, barrier, args.index_keys)
     # (with --index-keys the CSA keys are the library's output, which the oracle never reads)
     if not args.no_cpu_baseline and not args.quick and rank == 0 and world == 1 \

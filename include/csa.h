@@ -325,6 +325,15 @@ typedef struct csa_paged_layer {
 size_t csa_paged_decode_workspace_size(const csa_paged_layer* layer);
 csa_status csa_paged_decode_step(const csa_paged_layer* layer, void* ws, size_t ws_bytes,
                                  void* stream);
+
+/* csa_paged_layer_pair -- one paged decode step of a CSA layer (kind 0) and an HCA layer
+ * (kind 1), the HCA layer on a library-owned side stream beside the CSA layer (joined before
+ * the call's later work on `stream`, as in csa_hca_layer_pair). The workspace holds the two
+ * layers' regions one after the other. */
+size_t csa_paged_layer_pair_workspace_size(const csa_paged_layer* csa,
+                                           const csa_paged_layer* hca);
+csa_status csa_paged_layer_pair(const csa_paged_layer* csa, const csa_paged_layer* hca,
+                                void* ws, size_t ws_bytes, void* stream);
 size_t csa_hca_layer_pair_workspace_size(const csa_layer_desc* csa, const hca_layer_desc* hca);
 
 /* ----------------------------------------------------------------------------------------

@@ -12,6 +12,7 @@ from ._native import (  # noqa: F401
     LIB_PATH,
     PAGE_TOKENS,
     PreparedLayerPair,
+    PreparedPagedPair,
     PreparedPagedStep,
     RING_TOKENS,
     compress,

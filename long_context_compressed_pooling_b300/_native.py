@@ -92,6 +92,10 @@ _SIGS = {
                                                ctypes.POINTER(HcaLayerDesc)]),
     "csa_paged_decode_step": (_I, [ctypes.POINTER(PagedLayerDesc), _P, _Z, _P]),
     "csa_paged_decode_workspace_size": (_Z, [ctypes.POINTER(PagedLayerDesc)]),
+    "csa_paged_layer_pair": (_I, [ctypes.POINTER(PagedLayerDesc), ctypes.POINTER(PagedLayerDesc),
+                                  _P, _Z, _P]),
+    "csa_paged_layer_pair_workspace_size": (_Z, [ctypes.POINTER(PagedLayerDesc),
+                                                 ctypes.POINTER(PagedLayerDesc)]),
     "csa_get_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32)]),
     "csa_status_string": (ctypes.c_char_p, [_I]),
     "csa_abi_version": (_I, []),
@@ -416,6 +420,25 @@ class PreparedPagedStep:
     def __call__(self) -> None:
         _check("csa_paged_decode_step", self.lib.csa_paged_decode_step(
             self.dsc, self.wsp, self.wsb, _stream(self.dev)))
+
+
+class PreparedPagedPair:
+    """One paged decode step of a CSA and an HCA layer (csa_paged_layer_pair: the HCA layer on
+    the library's side stream); dicts as for PreparedPagedStep."""
+
+    def __init__(self, csa_layer: Dict, hca_layer: Dict, ws: Optional[torch.Tensor] = None):
+        self.lib = load_library()
+        self.layers = (csa_layer, hca_layer)
+        self.c = ctypes.pointer(_paged_desc(csa_layer))
+        self.h = ctypes.pointer(_paged_desc(hca_layer))
+        self.dev = csa_layer["q"].device
+        need = self.lib.csa_paged_layer_pair_workspace_size(self.c, self.h)
+        self.ws, self.wsb = _ws(need, self.dev, ws)
+        self.wsp = _ptr(self.ws)
+
+    def __call__(self) -> None:
+        _check("csa_paged_layer_pair", self.lib.csa_paged_layer_pair(
+            self.c, self.h, self.wsp, self.wsb, _stream(self.dev)))
 
 
 def paged_decode_step(layer: Dict, ws: Optional[torch.Tensor] = None):

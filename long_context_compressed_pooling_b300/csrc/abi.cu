@@ -293,15 +293,52 @@ size_t csa_paged_decode_workspace_size(const csa_paged_layer* layer) {
   return check_paged(layer) == CSA_OK ? paged_ws(layer) : 0;
 }
 
+static csa_status paged_step(const csa_paged_layer* L, void* ws, cudaStream_t st);
+
 csa_status csa_paged_decode_step(const csa_paged_layer* L, void* ws, size_t ws_bytes,
                                  void* stream) {
   csa_status s = check_paged(L);
   if (s != CSA_OK) return s;
   const size_t need = paged_ws(L);
   if (need > 0 && (ws == nullptr || ws_bytes < need || !al16(ws))) return CSA_ERR_WORKSPACE;
+  return paged_step(L, ws, static_cast<cudaStream_t>(stream));
+}
+
+size_t csa_paged_layer_pair_workspace_size(const csa_paged_layer* csa,
+                                           const csa_paged_layer* hca) {
+  return round_up(csa_paged_decode_workspace_size(csa), 256) +
+         csa_paged_decode_workspace_size(hca);
+}
+
+csa_status csa_paged_layer_pair(const csa_paged_layer* csa, const csa_paged_layer* hca, void* ws,
+                                size_t ws_bytes, void* stream) {
+  if (!csa || !hca || csa->kind != 0 || hca->kind != 1) return CSA_ERR_INVALID_ARG;
+  csa_status s = check_paged(csa);
+  if (s != CSA_OK) return s;
+  if ((s = check_paged(hca)) != CSA_OK) return s;
+  const size_t need = csa_paged_layer_pair_workspace_size(csa, hca);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !al16(ws))) return CSA_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the HCA layer on the library's side stream beside the CSA layer, as in csa_hca_layer_pair
+  SideStreams* ss = side_streams(st);
+  if (ss && (cudaEventRecord(ss->ev[0], st) != cudaSuccess ||
+             cudaStreamWaitEvent(ss->s[0], ss->ev[0], 0) != cudaSuccess))
+    return CSA_ERR_CUDA;
+  uint8_t* ws_c = static_cast<uint8_t*>(ws);
+  uint8_t* ws_h = ws_c + round_up(paged_ws(csa), 256);
+  if ((s = paged_step(csa, ws_c, st)) != CSA_OK) return s;
+  if ((s = paged_step(hca, ws_h, ss ? ss->s[0] : st)) != CSA_OK) return s;
+  if (ss && (cudaEventRecord(ss->ev[2], ss->s[0]) != cudaSuccess ||
+             cudaStreamWaitEvent(st, ss->ev[2], 0) != cudaSuccess))
+    return CSA_ERR_CUDA;
+  return CSA_OK;
+}
+
+// One validated paged decode step on stream st.
+static csa_status paged_step(const csa_paged_layer* L, void* ws, cudaStream_t st) {
+  csa_status s = CSA_OK;
   uint32_t* status = status_word();
   if (!status) return CSA_ERR_CUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   const bool csa_kind = L->kind == 0;
   PagedLayout P;
   P.d = L->d;

@@ -14,10 +14,11 @@
 //                    pending tail (m - 1 <= 127 tokens) always fit.
 //
 // One CTA per sequence: it writes token t into ring slot t % 256, and when t closes a block
-// (t % m == m - 1) pools the block's m ring rows with the softmax of their logits into entry
-// t / m of its page, with the same arithmetic as the flat compressor (fp32 sums, bf16 entries);
-// a CSA layer also pools the index-key rows and converts the key to MX FP4 as
-// csa_compress_index_keys does.
+// (t % m == m - 1) pools the block's m rows (the ring's, and token t's straight from the
+// inputs) with the softmax of their logits into entry t / m of its page: fp32 sums over 16
+// token groups of 64 channel pairs, each thread keeping eight rows in flight, bf16 entries. A
+// CSA layer also pools the index-key rows and converts the key to MX FP4 with the arithmetic
+// of csa_compress_index_keys.
 #include "common.cuh"
 #include "kernels.h"
 #include "prof.h"
@@ -25,7 +26,10 @@
 namespace csa {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 1024;
+constexpr int kGroups = 16;                // token groups: group g pools the tokens i = g mod 16
+constexpr int kPairs = kThreads / kGroups; // 64 channel pairs: one 32-bit word of a d = 128 row
+constexpr int kBatch = 8;                  // rows in flight per thread
 
 struct AppendParams {
   PagedLayout L;
@@ -43,30 +47,34 @@ CSA_DEV uint32_t e2m1_code(float a) {
          (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) + (uint32_t)(a > 5.0f);
 }
 
+// d = 128 (the paged path's head dim): a row is 64 32-bit words of two bf16 channels.
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) {
   __shared__ float w_s[kRingTokens];
   __shared__ float red[2];
+  __shared__ float4 part[kGroups][kPairs];  // (k lo, k hi, v lo, v hi) partial sums per group
   pdl_wait();  // the ring and pages may still be read by the previous step's kernels
   pdl_trigger();
   const PagedLayout& L = p.L;
   const int b = blockIdx.x, tid = threadIdx.x;
-  const int d = L.d, m = L.m;
+  const int m = L.m;
   const int64_t t = p.t;
-  const int slot = (int)(t % kRingTokens);
+  const int slot = (int)(t & (kRingTokens - 1));
   const int64_t rb = (int64_t)b * kRingTokens;
+  const uint32_t* rk = reinterpret_cast<const uint32_t*>(L.ring_k);
+  const uint32_t* rv = reinterpret_cast<const uint32_t*>(L.ring_v);
+  const uint32_t* kn = reinterpret_cast<const uint32_t*>(p.k_new) + (int64_t)b * kPairs;
+  const uint32_t* vn = reinterpret_cast<const uint32_t*>(p.v_new) + (int64_t)b * kPairs;
   // ---- the new token into the state cache ----
-  for (int c = tid; c < d; c += kThreads) {
-    L.ring_k[(rb + slot) * d + c] = p.k_new[(int64_t)b * d + c];
-    L.ring_v[(rb + slot) * d + c] = p.v_new[(int64_t)b * d + c];
+  if (tid < kPairs) {
+    reinterpret_cast<uint32_t*>(L.ring_k)[(rb + slot) * kPairs + tid] = kn[tid];
+    reinterpret_cast<uint32_t*>(L.ring_v)[(rb + slot) * kPairs + tid] = vn[tid];
   }
   if (tid == 0) L.ring_logits[rb + slot] = p.logit_new[b];
-  if (L.ring_xi && p.xi_new)
-    for (int c = tid; c < L.d_I; c += kThreads)
-      L.ring_xi[(rb + slot) * L.d_I + c] = p.xi_new[(int64_t)b * L.d_I + c];
+  if (L.ring_xi && p.xi_new && tid < L.d_I)
+    L.ring_xi[(rb + slot) * L.d_I + tid] = p.xi_new[(int64_t)b * L.d_I + tid];
   if ((t % m) != m - 1) return;  // no block closes (uniform over the CTA)
-  __syncthreads();               // the ring rows of the block, the new one included
 
-  // ---- pool block j = t / m ----
+  // ---- pool block j = t / m: rows t - m + 1 .. t - 1 from the ring, row t from the inputs ----
   const int64_t j = t / m;
   const int64_t t0 = t - (m - 1);
   const int64_t blk = (j * m) / kPageTokens;
@@ -77,48 +85,101 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) 
   }
   const int per_page = kPageTokens / m;
   const int64_t dst = (int64_t)page * per_page + (j % per_page);  // entry row in the pool
-  // softmax weights of the block's logits (m <= 128)
+  const int g = tid / kPairs, c = tid % kPairs;
+  auto row_k = [&](int i) -> uint32_t {
+    return i == m - 1 ? kn[c] : rk[(rb + ((t0 + i) & (kRingTokens - 1))) * kPairs + c];
+  };
+  auto row_v = [&](int i) -> uint32_t {
+    return i == m - 1 ? vn[c] : rv[(rb + ((t0 + i) & (kRingTokens - 1))) * kPairs + c];
+  };
+  // the first batch of this thread's rows is requested before the weights are reduced
+  uint32_t kb[kBatch], vb[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    const int i = g + kGroups * u;
+    if (i < m) {
+      kb[u] = row_k(i);
+      vb[u] = row_v(i);
+    }
+  }
+  // softmax weights of the block's logits (m <= 128), warp 0
+  for (int i = tid; i < m; i += kThreads)
+    w_s[i] = i == m - 1 ? p.logit_new[b] : L.ring_logits[rb + ((t0 + i) & (kRingTokens - 1))];
+  __syncthreads();
   if (tid < 32) {
     float mx = -INFINITY;
-    for (int i = tid; i < m; i += 32) {
-      const float lg = L.ring_logits[rb + (t0 + i) % kRingTokens];
-      w_s[i] = lg;
-      mx = fmaxf(mx, lg);
-    }
+    for (int i = tid; i < m; i += 32) mx = fmaxf(mx, w_s[i]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float ex[kRingTokens / 32];
     float sum = 0.f;
-    for (int i = tid; i < m; i += 32) {
-      const float e = expf(w_s[i] - mx);
-      w_s[i] = e;
-      sum += e;
+#pragma unroll
+    for (int u = 0; u < kRingTokens / 32; ++u) {
+      const int i = tid + 32 * u;
+      ex[u] = i < m ? expf(w_s[i] - mx) : 0.f;
+      sum += ex[u];
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kRingTokens / 32; ++u)
+      if (tid + 32 * u < m) w_s[tid + 32 * u] = ex[u];
     if (tid == 0) red[0] = 1.f / sum;
   }
   __syncthreads();
   const float inv = red[0];
-  for (int c = tid; c < d; c += kThreads) {
-    float ak = 0.f, av = 0.f;
-    for (int i = 0; i < m; ++i) {
-      const int64_t r = (rb + (t0 + i) % kRingTokens) * d + c;
-      const float pw = w_s[i] * inv;
-      ak = fmaf(pw, bf16_bits_to_f32(L.ring_k[r]), ak);
-      av = fmaf(pw, bf16_bits_to_f32(L.ring_v[r]), av);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  for (int base = 0; base < m; base += kGroups * kBatch) {
+    if (base > 0) {
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = base + g + kGroups * u;
+        if (i < m) {
+          kb[u] = row_k(i);
+          vb[u] = row_v(i);
+        }
+      }
     }
-    L.k_pool[dst * d + c] = f32_to_bf16_bits(ak);
-    L.v_pool[dst * d + c] = f32_to_bf16_bits(av);
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = base + g + kGroups * u;
+      if (i < m) {
+        const float pw = w_s[i] * inv;
+        a0 = fmaf(pw, __uint_as_float(kb[u] << 16), a0);
+        a1 = fmaf(pw, __uint_as_float(kb[u] & 0xFFFF0000u), a1);
+        a2 = fmaf(pw, __uint_as_float(vb[u] << 16), a2);
+        a3 = fmaf(pw, __uint_as_float(vb[u] & 0xFFFF0000u), a3);
+      }
+    }
   }
-  if (!L.ring_xi || !L.ki_codes_pool) return;
-  // ---- the indexer's key of the entry: pooled, bf16, MX FP4 (one element per thread) ----
+  part[g][c] = make_float4(a0, a1, a2, a3);
+  __syncthreads();
+  if (g == 0) {
+    float4 s4 = part[0][c];
+#pragma unroll
+    for (int q = 1; q < kGroups; ++q) {
+      const float4 o = part[q][c];
+      s4.x += o.x;
+      s4.y += o.y;
+      s4.z += o.z;
+      s4.w += o.w;
+    }
+    reinterpret_cast<uint32_t*>(L.k_pool)[dst * kPairs + c] = pack_bf16x2(s4.x, s4.y);
+    reinterpret_cast<uint32_t*>(L.v_pool)[dst * kPairs + c] = pack_bf16x2(s4.z, s4.w);
+  }
+  if (!L.ring_xi || !L.ki_codes_pool || !p.xi_new) return;
+  // ---- the indexer's key of the entry: pooled, bf16, MX FP4 (one element per thread), with
+  // the arithmetic of csa_compress_index_keys (weights e_i / sum in token order) ----
   const int dI = L.d_I;  // 32, 64 or 128 <= kThreads
   uint32_t bits = 0;
   if (tid < dI) {
     float ax = 0.f;
-    for (int i = 0; i < m; ++i)
-      ax = fmaf(w_s[i] * inv,
-                bf16_bits_to_f32(L.ring_xi[(rb + (t0 + i) % kRingTokens) * dI + tid]), ax);
+    for (int i = 0; i < m; ++i) {
+      const uint16_t x = i == m - 1 ? p.xi_new[(int64_t)b * dI + tid]
+                                    : L.ring_xi[(rb + ((t0 + i) & (kRingTokens - 1))) * dI + tid];
+      ax = fmaf(w_s[i] * inv, bf16_bits_to_f32(x), ax);
+    }
     bits = f32_to_bf16_bits(ax);
     if (bits == 0x8000u) bits = 0u;  // a pooled zero is +0
   }
@@ -145,6 +206,7 @@ cudaError_t launch_paged_append(const PagedLayout& L, int B, const uint16_t* k_n
                                 const uint16_t* xi_new, int64_t t, uint32_t* status,
                                 cudaStream_t stream) {
   if (B <= 0) return cudaSuccess;
+  if (L.d != 2 * kPairs || L.m > kRingTokens / 2) return cudaErrorInvalidValue;
   AppendParams prm{L, k_new, v_new, logit_new, xi_new, t, status};
   ProfScope prof(stream, "paged_append");
   return launch_ex(append_kernel, dim3((unsigned)B), dim3(kThreads), 0, stream, 1, prm);

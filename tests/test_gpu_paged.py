@@ -200,3 +200,32 @@ def test_unmapped_page_is_flagged_not_faulted():
     torch.cuda.synchronize()
     assert csa.device_status(reset=True) != 0
     assert torch.isfinite(L["out"].float()).all()
+
+
+def test_paged_layer_pair_matches_oracle():
+    """csa_paged_layer_pair: a CSA and an HCA layer (independent inputs) stepped together, the
+    HCA layer on the side stream; both outputs against the oracle at every step."""
+    B, N0, T = 2, P - 2, 4
+    sc, xc, _, Lc = _setup("csa", B, N0, T, 4, 128, 64, seed=21, xi_rows=False)
+    sh, xh, _, Lh = _setup("hca", B, N0, T, 128, 128, 0, seed=22, xi_rows=False)
+    for i in range(T):
+        t = N0 + i
+        for s, x, L in ((sc, xc, Lc), (sh, xh, Lh)):
+            L.update(N=t, k_new=x["k_raw"][:, t].contiguous(), v_new=x["v_raw"][:, t].contiguous(),
+                     logit_new=x["logits"][:, t].contiguous(), q=x["q"][:, i].contiguous())
+        Lc.update(qi_codes=xc["qi_codes"][:, i].contiguous(),
+                  qi_scales=xc["qi_scales"][:, i].contiguous())
+        csa.PreparedPagedPair(Lc, Lh)()
+        torch.cuda.synchronize()
+        assert csa.device_status(reset=True) == 0
+        for b in range(B):
+            rc = O.csa_layer_seq(bits(xc["q"][b]), bits(xc["k_raw"][b]), bits(xc["v_raw"][b]),
+                                 npy(xc["logits"][b]), npy(xc["qi_codes"][b]),
+                                 npy(xc["qi_scales"][b]), npy(xc["ki_codes"][b]),
+                                 npy(xc["ki_scales"][b]), m=4, W=128, k=64, d_I=64, q_pos0=N0,
+                                 query_rows=[i])
+            np.testing.assert_array_equal(npy(Lc["topk_idx"][b]), rc["idx"][0])
+            assert_attention_close(f64(Lc["out"][b]), rc["out"][0], f"CSA step {i} b={b}")
+            rh = O.hca_layer_seq(bits(xh["q"][b]), bits(xh["k_raw"][b]), bits(xh["v_raw"][b]),
+                                 npy(xh["logits"][b]), m=128, W=128, q_pos0=N0, query_rows=[i])
+            assert_attention_close(f64(Lh["out"][b]), rh["out"][0], f"HCA step {i} b={b}")
