@@ -132,9 +132,14 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
   int64_t tb, te;
   int b_first;
   if (decode) {
-    tb = p.total_tiles * split / p.n_splits;
-    te = p.total_tiles * (split + 1) / p.n_splits;
-    b_first = (int)(tb / p.tiles_per_seq);
+    // total * split / n in 32-bit arithmetic (64-bit division is emulated): total = a n + r,
+    // so total * split / n = a split + r split / n with r split < n^2 (the launch keeps
+    // total_tiles < 2^31 and n_splits < 2^15)
+    const uint32_t T = (uint32_t)p.total_tiles, n = (uint32_t)p.n_splits;
+    const uint32_t a = T / n, r = T % n, sp = (uint32_t)split;
+    tb = (int64_t)(a * sp + r * sp / n);
+    te = (int64_t)(a * (sp + 1) + r * (sp + 1) / n);
+    b_first = (int)((uint32_t)tb / (uint32_t)p.tiles_per_seq);
   } else {
     const int64_t t_last = p.q_pos0 + i0 + nq - 1;
     const int64_t nv_max = min(p.E, (t_last + 1) / p.m);
@@ -145,7 +150,8 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
   }
   if (tb >= te) return;  // uniform over the CTA
   const int ntiles = (int)(te - tb);
-  const int n_seq = decode ? (int)((te - 1) / p.tiles_per_seq) - b_first + 1 : 1;
+  const int n_seq =
+      decode ? (int)((uint32_t)(te - 1) / (uint32_t)p.tiles_per_seq) - b_first + 1 : 1;
   if (n_seq > kMaxSeqPerCta) {  // the launch plan never produces this; refuse rather than overflow
     if (threadIdx.x == 0) atomicOr(p.status, kFlagBadIndex);
     return;
@@ -260,10 +266,14 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
         }
       }
     };
-    int issued = 0;
-    for (int u = 0; u < nunits; ++u) {
+    // the first kSlots units go to free slots: one lane each, issued together
+    const int first = min(kSlots, nunits);
+    if (lane < first) issue_unit(lane);
+    __syncwarp();
+    int issued = first;
+    for (int u = first; u < nunits; ++u) {
       const int slot = u % kSlots, use = u / kSlots;
-      if (use > 0 && !mbar_wait_warp(&empty[slot], (uint32_t)(use - 1) & 1u, p.status)) {
+      if (!mbar_wait_warp(&empty[slot], (uint32_t)(use - 1) & 1u, p.status)) {
         if (lane == 0) *aborted = 1;
         break;
       }
@@ -662,6 +672,8 @@ cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, con
   prm.B = B;
   prm.tiles_per_seq = (int)((E + kTileM - 1) / kTileM);
   prm.total_tiles = (int64_t)B * prm.tiles_per_seq;
+  if (prm.total_tiles >= ((int64_t)1 << 31) || plan.n_splits >= (1 << 15))
+    return cudaErrorInvalidValue;  // the decode range arithmetic is 32-bit
   prm.ki_codes = ki_codes;
   prm.status = status;
   const int NB = d_I / 32;
