@@ -10,24 +10,28 @@
 // heads, which form the M = 64 side of both contractions:
 //   S[64 heads, 128 keys]  = Q[64, 128 d] . K_chunk^T        (A = Q, B = K rows; both K-major)
 //   O[64 heads, 128 d]    += P[64, 128 keys] . V_chunk        (A = P, B = V rows read MN-major)
-// S and O live in tensor memory (S double-buffered: 2 x 128 columns; O: 128 columns). With M = 64
-// the accumulator rows 16w..16w+15 sit in lanes 32w..32w+15, so softmax warp w reads its 16 rows
-// with the 16x256b load, which hands every thread two rows in the m16n8 fragment layout.
+// S and O live in tensor memory (S double-buffered: 2 x 128 columns; two O accumulators of 128
+// columns, one per key half). With M = 64 the accumulator rows 16q..16q+15 sit in lanes
+// 32q..32q+15, so a softmax warp reads its 16 rows with the 16x256b load, which hands every
+// thread two rows in the m16n8 fragment layout.
 //
-// Warp roles (224 threads, one CTA per SM):
-//   warps 0-3  softmax: read S, mask, online softmax, write P (bf16) to shared memory, rescale O
-//              in tensor memory when the running maximum has risen by more than 2^8 (the
-//              reference maximum of a row only moves then, so P stays below 2^8 and the
-//              normalisation at the end uses the same reference), final normalisation and store;
-//   warps 4-7  loaders: gather the key rows of each 128-key chunk (selected entries or window
-//              tokens) with 16-byte cp.async into 128-byte-swizzled K and V tiles, two 256-byte
-//              rows per warp instruction, and write a validity byte per key (missing keys and
-//              out-of-range indices are zero-filled and masked); each loader thread arrives on
-//              the stage's barrier twice: at once (releasing the mask bytes) and when its
-//              copies land (cp.async.mbarrier.arrive);
-//   warp 6     tensor-memory allocation and the MMAs (one elected lane of the converged warp),
-//              issued as soon as they are ready: QK^T of chunk c+1 overlaps the softmax of
-//              chunk c, and PV of chunk c never waits for the loads of chunk c+1.
+// Warp roles (544 threads, one CTA per SM):
+//   warps 0-7  softmax: warp w reads rows 16(w % 4) .. +15 of key half w / 4 of S, masks, runs an
+//              online softmax with its own running maximum per key half, writes P (bf16) to
+//              shared memory, and rescales its O accumulator in tensor memory only when the
+//              running maximum has risen by more than 2^8 (the reference maximum of a row only
+//              moves then, so P stays below 2^8 and the normalisation at the end uses the same
+//              reference); at the end the two key halves are combined, normalised and stored;
+//   warps 8-15 loaders: gather the key rows of each 128-key chunk (selected entries or window
+//              tokens; through the block table and the ring for a paged cache) with 16-byte
+//              cp.async into 128-byte-swizzled K and V tiles, two 256-byte rows per warp
+//              instruction, and write a validity bit per key (missing keys, out-of-range indices
+//              and unmapped pages are zero-filled and masked); each loader thread arrives on the
+//              stage's barrier twice: at once (releasing the mask bits) and when its copies land
+//              (cp.async.mbarrier.arrive);
+//   warp 16    tensor-memory allocation and the MMAs (one elected lane of the converged warp),
+//              issued as soon as they are ready: PV of the oldest chunk whose P is written, and
+//              QK^T of the next chunk, which overlaps the softmax of the current one.
 // Three K/V stages (64 KB each) and one P buffer; every mbarrier wait is bounded.
 //
 // Decode splits a token's key chunks over several CTAs: the splits of a token form a cluster and
