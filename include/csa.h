@@ -24,9 +24,9 @@
  *     form one softmax (no de-duplication); logits are q.k with no extra scale.
  *   - Errors: arguments are validated before anything is launched and a CSA_ERR_* code is
  *     returned without side effects. A failed launch returns CSA_ERR_CUDA. Kernels never trap:
- *     an out-of-range top-k index or an expired bounded wait is recorded in a device status
- *     word that csa_get_device_status() reads. Shapes the kernels do not implement return
- *     CSA_ERR_UNSUPPORTED (there is no fallback path).
+ *     an out-of-range top-k index, an unmapped page or an expired bounded wait is recorded
+ *     in a device status word that csa_get_device_status() reads. Shapes the kernels do not
+ *     implement return CSA_ERR_UNSUPPORTED (there is no fallback path).
  */
 #ifndef CSA_B300_H
 #define CSA_B300_H
@@ -50,7 +50,8 @@ typedef enum csa_status {
 } csa_status;
 
 /* Device status bits (csa_get_device_status() returns CSA_ERR_DEVICE when any is set). */
-#define CSA_DEVFLAG_BAD_INDEX 0x1u  /* a top-k index outside [0, E) or a count above k/visible */
+#define CSA_DEVFLAG_BAD_INDEX 0x1u  /* a top-k index outside [0, E), a count above k/visible,
+                                       or a paged cache's block-table entry naming no page */
 #define CSA_DEVFLAG_TIMEOUT   0x2u  /* a bounded mbarrier wait expired; the kernel returned */
 
 /* ----------------------------------------------------------------------------------------
