@@ -36,6 +36,10 @@ the design notes of the repository):
      (block scale 2^(floor(log2 amax) - 2), elements rounded to nearest-even on the e2m1 grid,
      saturating at 6).
 
+Parity unpinned (readings with nothing on the pages to check them against; the arithmetic that
+implements them is pinned by the tests): the R6 score formula itself (which nonlinearity, unit
+head weights) and R14's use of the layer's pooling logits for the index keys.
+
 Everything is plain numpy in float64; bf16 tensors arrive as uint16 bit arrays.
 """
 from __future__ import annotations
