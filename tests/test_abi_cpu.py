@@ -147,6 +147,17 @@ def test_paged_validation(lib):
     assert f() == 4                            # valid descriptor, no workspace
     assert lib.csa_paged_decode_workspace_size(_paged()) > 0
     assert lib.csa_paged_decode_workspace_size(_paged(kind=2)) == 0
+    # the pair takes a CSA layer then an HCA layer
+    g = lib.csa_paged_layer_pair
+    hca = _paged(kind=1, m=128, k=0)
+    assert g(_paged(), _paged(), None, 0, None) == 1
+    assert g(hca, _paged(), None, 0, None) == 1
+    assert g(_paged(), None, None, 0, None) == 1
+    assert g(_paged(), _paged(kind=1, m=256), None, 0, None) == 5
+    assert g(_paged(), hca, None, 0, None) == 4
+    both = lib.csa_paged_layer_pair_workspace_size(_paged(), hca)
+    assert both >= lib.csa_paged_decode_workspace_size(_paged()) + \
+        lib.csa_paged_decode_workspace_size(hca)
 
 
 def test_descriptor_struct_layout():
