@@ -3,8 +3,9 @@
 Thin Python binding over the C ABI of include/csa.h (libcsa_b300.so, built in-tree by
 `python -m long_context_compressed_pooling_b300.build`). It only marshals torch tensors into
 pointers and sizes, allocates workspaces with torch, and passes torch's current CUDA stream;
-every step of the computation runs in the library's CUDA kernels. Importing the package fails
-loudly when the library is missing: there is no CPU or fallback path.
+every step of the computation runs in the library's CUDA kernels. The library is loaded on the
+first call; that call raises when it is missing, and every call refuses host tensors: there is
+no CPU or fallback path.
 """
 from ._native import (  # noqa: F401
     CSA_OK,

@@ -5,6 +5,7 @@ import ctypes
 import os
 
 import pytest
+import torch
 
 from long_context_compressed_pooling_b300 import build as B
 import long_context_compressed_pooling_b300 as csa
@@ -176,3 +177,24 @@ def test_library_is_sm103a_build():
     # the build targets sm_103a only
     assert "arch=compute_103a,code=sm_103a" in " ".join(B.ARCH)
     assert os.path.exists(N.LIB_PATH)
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    """No fallback: without the library the first call raises instead of computing anything."""
+    monkeypatch.setattr(N, "_lib", None)
+    monkeypatch.setattr(N, "LIB_PATH", str(tmp_path / "libcsa_b300.so"))
+    with pytest.raises(RuntimeError, match="is missing"):
+        N.load_library()
+    with pytest.raises(RuntimeError, match="is missing"):
+        csa.topk(torch.zeros((1, 1, 8), dtype=torch.bfloat16), 7, 1, 2)
+
+
+def test_host_tensors_are_refused(lib):
+    """Host tensors never reach a computation: the binding rejects them before any call."""
+    s = torch.zeros((1, 1, 8), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA device"):
+        csa.topk(s, 7, 1, 2)
+    with pytest.raises(ValueError, match="CUDA device"):
+        csa.topk_f32(s.float(), 7, 1, 2)
+    with pytest.raises(ValueError, match="CUDA device"):
+        csa.quantize_mxfp4(torch.zeros((4, 64), dtype=torch.bfloat16))
