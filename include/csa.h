@@ -346,6 +346,24 @@ size_t csa_hca_layer_pair_workspace_size(const csa_layer_desc* csa, const hca_la
 csa_status csa_get_device_status(void* stream, int reset, uint32_t* flags_out);
 
 /* ----------------------------------------------------------------------------------------
+ * csa_test_set_faults -- failure injection for tests of the device-side failure detection
+ * (no counterpart on the pages). Every wait of a kernel on data another warp or copy produces
+ * is bounded; on expiry the kernel records CSA_DEVFLAG_TIMEOUT, releases what it holds and
+ * returns. wait_budget_cycles > 0 replaces the bound (about 2e9 SM cycles, one second) for
+ * every later launch of a kernel that honours it; <= 0 restores it. skip_mask names producers
+ * that skip their work on later launches, so that the waits depending on them run out:
+ *   CSA_FAULT_SKIP_KEY_COPIES  the indexer's copy warp issues no key copies (csa_index_topk,
+ *                              csa_index_scores, the CSA layer of csa_hca_layer_pair); the
+ *                              call's top-k outputs are then unspecified, but in range.
+ * Returns CSA_ERR_INVALID_ARG for unknown bits. The settings are process-wide; a test restores
+ * them with csa_test_set_faults(0, 0) and clears the status word with csa_get_device_status.
+ * After a timeout, attention launches skip their work until the status word is cleared.
+ * ---------------------------------------------------------------------------------------- */
+#define CSA_FAULT_SKIP_KEY_COPIES 0x1u
+#define CSA_FAULT_ALL             0x1u
+csa_status csa_test_set_faults(long long wait_budget_cycles, uint32_t skip_mask);
+
+/* ----------------------------------------------------------------------------------------
  * Per-kernel timing (tracing aid; no counterpart on the pages). While enabled, every kernel
  * launch of the library is bracketed by two CUDA events recorded on its launch stream.
  * csa_profiler_collect synchronises those events and returns, per kernel name, the number of

@@ -10,6 +10,7 @@ no CPU or fallback path.
 from ._native import (  # noqa: F401
     CSA_OK,
     CsaError,
+    FAULT_SKIP_KEY_COPIES,
     LIB_PATH,
     PAGE_TOKENS,
     PreparedLayerPair,
@@ -30,6 +31,7 @@ from ._native import (  # noqa: F401
     profiler_collect,
     profiler_enable,
     quantize_mxfp4,
+    test_set_faults,
     topk,
     topk_f32,
     workspace_sizes,

@@ -99,6 +99,7 @@ _SIGS = {
     "csa_get_device_status": (_I, [_P, _I, ctypes.POINTER(ctypes.c_uint32)]),
     "csa_status_string": (ctypes.c_char_p, [_I]),
     "csa_abi_version": (_I, []),
+    "csa_test_set_faults": (_I, [ctypes.c_longlong, ctypes.c_uint32]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -462,6 +463,15 @@ def device_status(reset: bool = True) -> int:
     if code not in (CSA_OK, 7):
         raise CsaError("csa_get_device_status", code)
     return int(flags.value)
+
+
+FAULT_SKIP_KEY_COPIES = 0x1
+
+
+def test_set_faults(wait_budget_cycles: int = 0, skip_mask: int = 0) -> None:
+    """Failure injection for tests (csa_test_set_faults): a shorter bound on every device-side
+    wait and producers that skip their work. (0, 0) restores the defaults."""
+    _check("csa_test_set_faults", load_library().csa_test_set_faults(wait_budget_cycles, skip_mask))
 
 
 def profiler_enable(on: bool = True) -> None:

@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/csa.h"
@@ -168,19 +169,26 @@ csa_status check_index_keys(const uint16_t* xi_raw, const float* logits, int B, 
 }
 
 // ---- internal runners (arguments already validated) -----------------------------------------
+// What the indexer may read before its grid-dependency wait (kernels.h, launch_indexer). The
+// default, for callers that do not know the kernel enqueued before them: nothing.
+struct Freshness {
+  int64_t keys_from = 0;
+  bool queries = true;
+};
+
 csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const uint8_t* ki_codes,
                        const uint8_t* ki_scales, int B, int Nq, int64_t q_pos0, int64_t E, int m,
                        int H_I, int d_I, uint16_t* sc, float* scores_f32, cudaStream_t st,
-                       const PagedLayout* paged = nullptr);
+                       const PagedLayout* paged = nullptr, Freshness fr = Freshness());
 
 csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
                           const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
                           int64_t q_pos0, int64_t E, int m, int H_I, int d_I, int k,
                           int32_t* topk_idx, int32_t* topk_cnt, uint16_t* scores, void* ws,
-                          cudaStream_t st) {
+                          cudaStream_t st, Freshness fr = Freshness()) {
   uint16_t* sc = scores ? scores : static_cast<uint16_t*>(ws);
   csa_status s = run_indexer(qi_codes, qi_scales, ki_codes, ki_scales, B, Nq, q_pos0, E, m, H_I,
-                             d_I, sc, nullptr, st);
+                             d_I, sc, nullptr, st, nullptr, fr);
   if (s != CSA_OK) return s;
   return from_cuda(launch_topk(sc, B, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, st));
 }
@@ -189,7 +197,7 @@ csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
 csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const uint8_t* ki_codes,
                        const uint8_t* ki_scales, int B, int Nq, int64_t q_pos0, int64_t E, int m,
                        int H_I, int d_I, uint16_t* sc, float* scores_f32, cudaStream_t st,
-                       const PagedLayout* paged) {
+                       const PagedLayout* paged, Freshness fr) {
   if (E > 0) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return CSA_ERR_CUDA;
@@ -209,7 +217,8 @@ csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const 
       return CSA_ERR_CUDA;
     const IndexerPlan plan = plan_indexer(B, Nq, E, H_I, d_I, paged != nullptr);
     cudaError_t e = launch_indexer(&map, ki_codes, qi_codes, qi_scales, ki_scales, sc, B, Nq, q_pos0, E, m,
-                                   H_I, d_I, plan, status, st, scores_f32, paged);
+                                   H_I, d_I, plan, status, st, scores_f32, paged, fr.keys_from,
+                                   fr.queries);
     if (e != cudaSuccess) return CSA_ERR_CUDA;
   }
   return CSA_OK;
@@ -226,9 +235,23 @@ int64_t hca_max_keys(int64_t E, int m, int64_t N, int W) {
 
 }  // namespace
 
+namespace {
+// Failure injection (csa_test_set_faults); read at every launch of a kernel that honours it.
+std::atomic<long long> g_wait_budget{0};
+std::atomic<uint32_t> g_fault_mask{0};
+}  // namespace
+
 namespace csa {
 // The library's device status word on the current device (null if it cannot be resolved).
 uint32_t* device_status_word() { return status_word(); }
+
+FaultConfig fault_config() {
+  FaultConfig f;
+  const long long b = g_wait_budget.load();
+  f.wait_budget = b > 0 ? b : kWaitBudgetCyclesHost;
+  f.skip_mask = g_fault_mask.load();
+  return f;
+}
 }  // namespace csa
 
 namespace {
@@ -365,8 +388,13 @@ static csa_status paged_step(const csa_paged_layer* L, void* ws, cudaStream_t st
   a.paged = &P;
   if (csa_kind) {
     uint16_t* sc = static_cast<uint16_t*>(ws);
+    // The append launched just above is the only kernel this one may overlap: it writes the
+    // index key of the block the token closes (entry E - 1) and nothing else the indexer reads.
+    Freshness fr;
+    fr.keys_from = (t + 1) % L->m == 0 ? E - 1 : E;
+    fr.queries = false;
     s = run_indexer(L->qi_codes, L->qi_scales, L->ki_codes_pool, L->ki_scales_pool, L->B, 1, t, E,
-                    L->m, L->H_I, L->d_I, sc, nullptr, st, &P);
+                    L->m, L->H_I, L->d_I, sc, nullptr, st, &P, fr);
     if (s != CSA_OK) return s;
     if (launch_topk(sc, L->B, 1, t, E, L->m, L->k, L->topk_idx, L->topk_cnt, st) != cudaSuccess)
       return CSA_ERR_CUDA;
@@ -379,7 +407,14 @@ static csa_status paged_step(const csa_paged_layer* L, void* ws, cudaStream_t st
 }
 
 
-int csa_abi_version(void) { return 2; }
+int csa_abi_version(void) { return 3; }
+
+csa_status csa_test_set_faults(long long wait_budget_cycles, uint32_t skip_mask) {
+  if (skip_mask & ~CSA_FAULT_ALL) return CSA_ERR_INVALID_ARG;
+  g_wait_budget.store(wait_budget_cycles > 0 ? wait_budget_cycles : 0);
+  g_fault_mask.store(skip_mask);
+  return CSA_OK;
+}
 
 const char* csa_status_string(csa_status s) {
   switch (s) {
@@ -594,9 +629,17 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
                           const_cast<uint8_t*>(c->ki_codes), const_cast<uint8_t*>(c->ki_scales),
                           st) != cudaSuccess)
       return CSA_ERR_CUDA;
+    // When this call launched the pooling above, the indexer's predecessor is known: the pooling
+    // of the index keys from j0 on (xi_raw), else the entry pooling, which writes nothing the
+    // indexer reads. Without it the predecessor is unknown and the indexer waits first.
+    Freshness fr;
+    if (E > j0) {
+      fr.keys_from = c->xi_raw ? j0 : E;
+      fr.queries = false;
+    }
     csa_status s = run_index_topk(c->qi_codes, c->qi_scales, c->ki_codes, c->ki_scales, c->B,
                                   c->Nq, c->q_pos0, E, c->m, c->H_I, c->d_I, c->k, c->topk_idx,
-                                  c->topk_cnt, c->scores, ws_c, st);
+                                  c->topk_cnt, c->scores, ws_c, st, fr);
     if (s != CSA_OK) return s;
     AttendArgs a{c->q, c->k_cmp, c->v_cmp, c->topk_idx, c->topk_cnt, c->k_raw, c->v_raw, c->out,
                  c->lse, E, c->N, c->q_pos0, c->k, c->m, c->W, c->B, c->Nq, c->H, c->d};

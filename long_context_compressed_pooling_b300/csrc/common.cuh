@@ -104,14 +104,16 @@ CSA_DEV bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete, for at most kWaitBudgetCycles.
-// On expiry it records kFlagTimeout in the status word and returns false.
-CSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// Waits for the phase with the given parity to complete, for at most `budget` SM cycles
+// (kWaitBudgetCycles unless a test shortens it). On expiry it records kFlagTimeout in the
+// status word and returns false.
+CSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                       long long budget = kWaitBudgetCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (clock64() - t0 > kWaitBudgetCycles) {
+    if (clock64() - t0 > budget) {
       atomicOr(status, kFlagTimeout);
       return false;
     }
@@ -120,10 +122,15 @@ CSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
 
 // Warp-wide bounded wait: every lane waits (each lane's wait is bounded) and the warp takes lane
 // 0's verdict, so the result is uniform across the warp.
-CSA_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status) {
-  const int ok = mbar_wait(bar, parity, status) ? 1 : 0;
+CSA_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status,
+                            long long budget = kWaitBudgetCycles) {
+  const int ok = mbar_wait(bar, parity, status, budget) ? 1 : 0;
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
+
+// Failure-injection switches a test can set on the host (csa_test_set_faults): a shorter wait
+// budget, and producers that skip their work so that the waits depending on them run out.
+constexpr uint32_t kFaultSkipKeyCopies = 0x1u;  // the indexer's copy warp issues no copies
 
 // One lane of a converged warp (elect.sync). Single-thread operations (TMA / bulk copy issue,
 // tcgen05.mma, tcgen05.commit) are issued this way from a warp that runs its loop converged: a

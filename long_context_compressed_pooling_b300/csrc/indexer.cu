@@ -76,6 +76,13 @@ struct IdxParams {
   // (page << page_shift) + (j & page_mask) of the key pools, page = block_table[b][j >> page_shift]
   const int32_t* block_table;
   int max_blocks, n_pages, page_shift;
+  // Inputs a predecessor kernel on the stream may still be writing (it lets this kernel start
+  // early): key tiles holding an entry at or above keys_fresh_from are copied only after the
+  // grid-dependency wait, and with q_fresh set the query operands are read only after it.
+  int64_t keys_fresh_from;
+  int q_fresh;
+  long long wait_budget;  // bounded-wait budget (SM cycles)
+  uint32_t fault_mask;    // kFault* switches set by a failure-injection test (0 otherwise)
 };
 
 // Shared memory for a launch whose B operand has `brows` rows (decode: 8 sequences x ncols;
@@ -196,10 +203,12 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
 
   if (warp == 0) {
     // ---------------- copy warp: fills the ring slot by slot, never joins the set-up ----------
-    // The index keys are inputs of this call (not a predecessor's output), so copying starts
-    // before the predecessor-dependent part. Every bulk copy costs ~0.3 us to issue whatever its
-    // size, so a slot (8 tiles) is one code copy and one scale copy whenever the tiles form one
-    // contiguous span of HBM (always, unless a ragged sequence tail intervenes).
+    // Key tiles below keys_fresh_from cannot be written by the kernel this one overlaps, so they
+    // are copied at once; the first slot holding a tile at or above it is issued only after the
+    // grid-dependency wait (the predecessor, e.g. the pooling of the step's new index keys, has
+    // then completed and its writes are visible). Every bulk copy costs ~0.3 us to issue
+    // whatever its size, so a slot (8 tiles) is one code copy and one scale copy whenever the
+    // tiles form one contiguous span of HBM (always, unless a ragged sequence tail intervenes).
     // A page holds whole tiles, so a paged tile is always copied whole (its rows past the
     // visible entries are never scored).
     auto tile_bytes = [&](int it) -> uint32_t {  // rows that exist in this tile x 32 B
@@ -266,16 +275,36 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
         }
       }
     };
+    // first slot that holds a tile the predecessor may still be writing (nunits: none)
+    int fresh_unit = nunits;
+    for (int it = 0; it < ntiles; ++it)
+      if ((int64_t)tile_row0(it) + kTileM > p.keys_fresh_from) {
+        fresh_unit = it / kSlotTiles;
+        break;
+      }
+    bool waited = false;
     // the first kSlots units go to free slots: one lane each, issued together
     const int first = min(kSlots, nunits);
+    if (fresh_unit < first) {
+      pdl_wait();
+      waited = true;
+    }
+    if (p.fault_mask & kFaultSkipKeyCopies) {  // failure injection: no tile ever arrives
+      if (!waited) pdl_wait();
+      return;
+    }
     if (lane < first) issue_unit(lane);
     __syncwarp();
     int issued = first;
     for (int u = first; u < nunits; ++u) {
       const int slot = u % kSlots, use = u / kSlots;
-      if (!mbar_wait_warp(&empty[slot], (uint32_t)(use - 1) & 1u, p.status)) {
+      if (!mbar_wait_warp(&empty[slot], (uint32_t)(use - 1) & 1u, p.status, p.wait_budget)) {
         if (lane == 0) *aborted = 1;
         break;
+      }
+      if (!waited && u >= fresh_unit) {
+        pdl_wait();
+        waited = true;
       }
       if (elect_one()) issue_unit(u);
       __syncwarp();
@@ -283,12 +312,13 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
     }
     // stay until this CTA's own copies have landed (the MMA warp normally sees them first)
     for (int u = max(0, issued - kSlots); u < issued; ++u)
-      mbar_wait_warp(&full[u % kSlots], (uint32_t)(u / kSlots) & 1u, p.status);
+      mbar_wait_warp(&full[u % kSlots], (uint32_t)(u / kSlots) & 1u, p.status, p.wait_budget);
     return;
   }
 
   // ---- set-up of the work warps: B operand, query scales, visibility, TMEM, scale factors ----
   // Sequence sl of this CTA owns B rows [sl * ncols, (sl + 1) * ncols).
+  if (p.q_fresh) pdl_wait();  // the queries may be the predecessor's output
   const int wt = threadIdx.x - 32;
   for (int idx = wt; idx < n_seq * p.ncols * 2; idx += kWork) {
     const int rr = idx >> 1, c = idx & 1;
@@ -359,8 +389,8 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
       const int slot = u % kSlots;
       const int a = g % p.nacc;
       const uint32_t aph = (uint32_t)(g / p.nacc) & 1u;
-      if (!mbar_wait_warp(&tempty[a], aph ^ 1u, p.status) ||
-          !mbar_wait_warp(&full[slot], (uint32_t)(u / kSlots) & 1u, p.status)) {
+      if (!mbar_wait_warp(&tempty[a], aph ^ 1u, p.status, p.wait_budget) ||
+          !mbar_wait_warp(&full[slot], (uint32_t)(u / kSlots) & 1u, p.status, p.wait_budget)) {
         if (lane == 0) *aborted = 1;
         break;
       }
@@ -385,7 +415,7 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
     }
     if (elect_one()) umma_commit(drain);  // arrives once every MMA above has finished
     __syncwarp();
-    mbar_wait_warp(drain, 0, p.status);
+    mbar_wait_warp(drain, 0, p.status, p.wait_budget);
   } else {
     // ---------------- epilogue: 8 warps, two per tensor-memory lane quarter ----------------
     const int quarter = warp & 3;
@@ -401,9 +431,9 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
       const int slot = unit % kSlots;
       // The slot's scale tile is read below: acquire the copy that filled it (its phase is
       // complete, and it cannot be refilled before this warp releases it).
-      if (!mbar_wait_warp(&tfull[a], aph, p.status) ||
+      if (!mbar_wait_warp(&tfull[a], aph, p.status, p.wait_budget) ||
           (scales_in_smem && !mbar_wait_warp(&full[slot], (uint32_t)(unit / kSlots) & 1u,
-                                             p.status))) {
+                                             p.status, p.wait_budget))) {
         if (lane == 0) *aborted = 1;
         break;
       }
@@ -559,7 +589,7 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
   // signalled `done` (and the MMA warp has drained its MMAs above); the other warps just exit.
   __syncwarp();
   if (warp == 1) {
-    mbar_wait_warp(done, 0, p.status);  // bounded; a timeout is already recorded
+    mbar_wait_warp(done, 0, p.status, p.wait_budget);  // bounded; a timeout is already recorded
     tc_fence_after();
     tmem_dealloc(tmem, (uint32_t)p.tmem_cols);
   }
@@ -643,8 +673,14 @@ cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, con
                            const uint8_t* qi_scales, const uint8_t* ki_scales, uint16_t* scores,
                            int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I, int d_I,
                            const IndexerPlan& plan, uint32_t* status, cudaStream_t stream,
-                           float* scores_f32, const PagedLayout* paged) {
+                           float* scores_f32, const PagedLayout* paged, int64_t keys_fresh_from,
+                           bool q_fresh) {
   IdxParams prm;
+  prm.keys_fresh_from = keys_fresh_from;
+  prm.q_fresh = q_fresh ? 1 : 0;
+  const FaultConfig fc = fault_config();
+  prm.wait_budget = fc.wait_budget;
+  prm.fault_mask = fc.skip_mask;
   prm.block_table = paged ? paged->block_table : nullptr;
   prm.max_blocks = paged ? paged->max_blocks : 0;
   prm.n_pages = paged ? paged->n_pages : 0;

@@ -65,6 +65,15 @@ cudaError_t launch_paged_append(const PagedLayout& L, int B, const uint16_t* k_n
 // The library's device status word on the current device (defined in abi.cu).
 uint32_t* device_status_word();
 
+// Failure injection for tests (csa_test_set_faults): the bounded-wait budget in SM cycles the
+// kernels use, and a mask of producers (kFault* in common.cuh) that skip their work.
+constexpr long long kWaitBudgetCyclesHost = 2000000000LL;  // equals kWaitBudgetCycles
+struct FaultConfig {
+  long long wait_budget;
+  uint32_t skip_mask;
+};
+FaultConfig fault_config();
+
 // ---- block pooling --------------------------------------------------------------------------
 // The indexer's own compressed keys: pool index-key rows [B, N, d_I] of entries
 // [j_begin, j_begin + n_entries) and convert them to MX FP4 (d_I in {32, 64, 128}, m <= 32).
@@ -94,7 +103,12 @@ cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, con
                            const uint8_t* qi_scales, const uint8_t* ki_scales, uint16_t* scores,
                            int B, int Nq, int64_t q_pos0, int64_t E, int m, int H_I, int d_I,
                            const IndexerPlan& plan, uint32_t* status, cudaStream_t stream,
-                           float* scores_f32 = nullptr, const PagedLayout* paged = nullptr);
+                           float* scores_f32 = nullptr, const PagedLayout* paged = nullptr,
+                           int64_t keys_fresh_from = 0, bool q_fresh = true);
+// keys_fresh_from / q_fresh: the index-key entries at or above keys_fresh_from, and (q_fresh)
+// the index queries, may be the output of the kernel launched just before on the stream; the
+// indexer reads them only after its grid-dependency wait. The defaults (everything may be
+// fresh) are right for any caller that does not know its predecessor.
 
 // ---- top-k over BF16 scores ------------------------------------------------------------------
 cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,

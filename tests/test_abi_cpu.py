@@ -23,7 +23,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert len(syms) >= 14
     missing = [n for n, ok in syms.items() if not ok]
     assert not missing, missing
-    assert lib.csa_abi_version() == 2
+    assert lib.csa_abi_version() == 3
 
 
 def test_status_strings(lib):
@@ -198,3 +198,10 @@ def test_host_tensors_are_refused(lib):
         csa.topk_f32(s.float(), 7, 1, 2)
     with pytest.raises(ValueError, match="CUDA device"):
         csa.quantize_mxfp4(torch.zeros((4, 64), dtype=torch.bfloat16))
+
+
+def test_fault_injection_switches_are_validated_and_restorable(lib):
+    # host-only: the switches are stored for later launches, nothing touches CUDA here
+    assert lib.csa_test_set_faults(1000, 0x80) == 1   # unknown producer bit
+    assert lib.csa_test_set_faults(2_000_000, 0x1) == 0
+    assert lib.csa_test_set_faults(0, 0) == 0          # defaults restored

@@ -196,3 +196,42 @@ def test_layer_pair_writes_the_chunk_index_keys():
     n_amb = _check_seq_keys(npy(kc[0]), npy(ks[0]), bits(xi[0]), npy(x["logits"][0]), m, 0, E,
                             "layer pair")
     assert n_amb <= 0.05 * E * d_I
+
+
+@pytest.mark.parametrize("B,N,Nq", [(2, 65536, 2048), (16, 131072, 1)])
+def test_layer_pair_scores_the_keys_it_just_pooled(B, N, Nq):
+    """The layer pools the index keys of its new blocks in one launch and scores them in the
+    next, which may start before the pooling has finished: the key tiles the pooling writes must
+    be read only after it completes. The new keys are poisoned (tiny scales) before every one of
+    several repeated calls; a call that scored a poisoned key would select differently from the
+    standalone indexer run afterwards on the finished keys."""
+    m, k, W, d_I = 4, 256, 128, 64
+    q0 = N - Nq
+    cb = (q0 // m) * m if Nq > 1 else N - m
+    s = LayerShape("csa", B=B, N=N, Nq=Nq, q_pos0=q0, H=64, d=128, m=m, W=W, k=k, H_I=4,
+                   d_I=d_I, q_scale=1.0 / np.sqrt(128), compress_begin=cb)
+    x = generate_layer(s, seed=23 + Nq, device=DEV)
+    xi = index_key_rows(s, seed=23 + Nq, device=DEV)
+    E = N // m
+    j0 = cb // m
+    full_c, full_s = csa.compress_index_keys(xi, x["logits"], m)
+    kc, ks = full_c.clone(), full_s.clone()
+    k_cmp = torch.empty((B, E, 128), dtype=torch.bfloat16, device=DEV)
+    v_cmp = torch.empty_like(k_cmp)
+    csa.compress(x["k_raw"], x["v_raw"], x["logits"], m, k_cmp, v_cmp, tok_end=cb)
+    out = torch.empty_like(x["q"])
+    idx = torch.empty((B, Nq, k), dtype=torch.int32, device=DEV)
+    cnt = torch.empty((B, Nq), dtype=torch.int32, device=DEV)
+    layer = dict(q=x["q"], k_raw=x["k_raw"], v_raw=x["v_raw"], logits=x["logits"],
+                 qi_codes=x["qi_codes"], qi_scales=x["qi_scales"], ki_codes=kc, ki_scales=ks,
+                 k_cmp=k_cmp, v_cmp=v_cmp, out=out, topk_idx=idx, topk_cnt=cnt, xi_raw=xi,
+                 m=m, W=W, k=k, q_pos0=q0, compress_begin=cb)
+    ref_i, ref_c, _ = csa.index_topk(x["qi_codes"], x["qi_scales"], full_c, full_s, q0, m, k)
+    step = csa.PreparedLayerPair(layer, None)
+    for rep in range(6):
+        kc[:, j0:] = 0x77
+        ks[:, j0:] = 0x01
+        step()
+        torch.cuda.synchronize()
+        assert torch.equal(kc, full_c) and torch.equal(ks, full_s), rep
+        assert torch.equal(idx, ref_i) and torch.equal(cnt, ref_c), rep

@@ -4,8 +4,10 @@ cudaMalloc's implicit synchronisation, a C caller holding only its input and out
 Its score scratch is a fixed array inside the library instead of a workspace.
 
 Called here through the C ABI and compared with the allocating csa_index_topk on two calls in a
-row with different inputs, so scratch left over by the first call cannot leak into the second.
-Top-k lists are integer results: the comparison is exact, as for every top-k test. This file is
+row with different inputs, so scratch left over by the first call cannot leak into the second;
+the second, smaller call of each pair is also checked against the fp64 oracle's scores and
+selection, so a fault shared by both entry points would still show. Top-k lists are integer
+results: the comparisons are exact, as for every top-k test. This file is
 collected last so a failure here stops a `-x` run only after every other test has run."""
 import ctypes
 
@@ -14,6 +16,7 @@ import pytest
 import torch
 
 import long_context_compressed_pooling_b300 as csa
+import oracle as O
 from long_context_compressed_pooling_b300 import _native as N
 from synth import LayerShape, generate_layer
 
@@ -48,14 +51,26 @@ def _noalloc(x, q_pos0, m, k):
     ((23, 2, 70, 500, 600, 4, 4, 64, 24), (24, 4, 1, 8191, 8192, 4, 8, 64, 300)),
 ])
 def test_noalloc_matches_allocating_entry_point_twice(first, second):
-    for seed, B, Nq, q_pos0, N_ctx, m, H_I, d_I, k in (first, second):
+    for call, (seed, B, Nq, q_pos0, N_ctx, m, H_I, d_I, k) in enumerate((first, second)):
         x = _inputs(seed, B, Nq, q_pos0, N_ctx, m, H_I, d_I)
         ref_idx, ref_cnt, _ = csa.index_topk(x["qi_codes"], x["qi_scales"], x["ki_codes"],
                                              x["ki_scales"], q_pos0, m, k)
         got_idx, got_cnt = _noalloc(x, q_pos0, m, k)
         torch.cuda.synchronize()
-        assert np.array_equal(got_cnt.cpu().numpy(), ref_cnt.cpu().numpy())
-        assert np.array_equal(got_idx.cpu().numpy(), ref_idx.cpu().numpy())
+        gi, gc = got_idx.cpu().numpy(), got_cnt.cpu().numpy()
+        assert np.array_equal(gc, ref_cnt.cpu().numpy())
+        assert np.array_equal(gi, ref_idx.cpu().numpy())
+        if call == 1:  # the oracle: exact scores rounded to BF16, then the selection rule
+            qc, qs, kc, ks = (x[n].cpu().numpy() for n in ("qi_codes", "qi_scales", "ki_codes",
+                                                           "ki_scales"))
+            E = N_ctx // m
+            for b in range(B):
+                for i in range(Nq):
+                    nv = O.visible_entries(q_pos0 + i, m, E)
+                    sc = O.f64_to_bf16_rne(O.index_scores(qc[b, i], qs[b, i], kc[b, :nv],
+                                                          ks[b, :nv], d_I))
+                    ridx, rcnt = O.topk_select(sc, nv, k)
+                    assert gc[b, i] == rcnt and np.array_equal(gi[b, i], ridx), (b, i)
     assert csa.device_status(reset=True) == 0
 
 
