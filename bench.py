@@ -48,6 +48,7 @@ ALL_CONFIGS = ("tiny_pair_prefill_2k", "csa_decode_128k", "hca_decode_1m", "csa_
 # indexer is the measured BF16 burst peak times this ratio (no FP4 peak is measured).
 FP4_OVER_BF16 = 13.5 / 2.25
 KERNEL_SOURCES = {
+    "csa_decode": "decode.cu", "indexer_topk": "decode.cu",
     "indexer_mxf4": "indexer.cu", "topk": "topk.cu", "csa_attend": "attend_tc.cu",
     "hca_attend": "attend_tc.cu", "lse_merge": "attend.cu", "compress": "compress.cu",
     "index_keys": "compress.cu", "paged_append": "paged.cu",
@@ -138,6 +139,11 @@ def layer_work(s, index_keys=False):
     return k
 
 
+# Kernels that run several steps of the path in one launch: their work is the sum of the steps'.
+FUSED = {"csa_decode": ("indexer_mxf4", "topk", "csa_attend"),
+         "indexer_topk": ("indexer_mxf4", "topk")}
+
+
 def step_work(wl, index_keys=False):
     kernels = {}
     for s in wl.layers:
@@ -145,7 +151,16 @@ def step_work(wl, index_keys=False):
             a = kernels.setdefault(n, dict(bytes=0, flops=0))
             a["bytes"] += v["bytes"]
             a["flops"] += v["flops"]
-    # unique bytes of the step: per-layer inputs read once + outputs
+    for name, parts in FUSED.items():
+        if all(p in kernels for p in parts):
+            kernels[name] = dict(bytes=sum(kernels[p]["bytes"] for p in parts),
+                                 flops=sum(kernels[p]["flops"] for p in parts))
+    # the fused decode kernel keeps the BF16 scores on chip: no score bytes
+    if "csa_decode" in kernels:
+        for s in wl.layers:
+            if s.kind == "csa":
+                nv = sum(_vis(s.q_pos0 + i, s.m, s.E) for i in range(s.Nq))
+                kernels["csa_decode"]["bytes"] -= s.B * nv * 2 * 2  # written + read back
     return kernels
 
 

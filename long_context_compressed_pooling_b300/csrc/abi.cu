@@ -181,11 +181,41 @@ csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const 
                        int H_I, int d_I, uint16_t* sc, float* scores_f32, cudaStream_t st,
                        const PagedLayout* paged = nullptr, Freshness fr = Freshness());
 
+// The fused decode kernel (decode.cu) serves one query per sequence with 64-element index keys
+// of at most 4 heads; its plan decides whether the rest of the shape fits.
+bool decode_indexer_fits(int Nq, int H_I, int d_I) { return Nq == 1 && d_I == 64 && H_I <= 4; }
+
 csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
                           const uint8_t* ki_codes, const uint8_t* ki_scales, int B, int Nq,
                           int64_t q_pos0, int64_t E, int m, int H_I, int d_I, int k,
                           int32_t* topk_idx, int32_t* topk_cnt, uint16_t* scores, void* ws,
                           cudaStream_t st, Freshness fr = Freshness()) {
+  if (decode_indexer_fits(Nq, H_I, d_I)) {
+    const int64_t nv = std::max<int64_t>(0, std::min<int64_t>(E, (q_pos0 + 1) / m));
+    const DecodePlan pl = plan_decode(B, E, nv, k, 0, false, scores != nullptr);
+    if (pl.ok) {
+      uint32_t* status = status_word();
+      if (!status) return CSA_ERR_CUDA;
+      DecodeArgs a{};
+      a.qi_codes = qi_codes;
+      a.qi_scales = qi_scales;
+      a.ki_codes = ki_codes;
+      a.ki_scales = ki_scales;
+      a.scores = scores;
+      a.topk_idx = topk_idx;
+      a.topk_cnt = topk_cnt;
+      a.E = E;
+      a.t = q_pos0;
+      a.m = m;
+      a.k = k;
+      a.H_I = H_I;
+      a.B = B;
+      a.keys_fresh_from = fr.keys_from;
+      a.wait_first = fr.queries;
+      a.attend = false;
+      return from_cuda(launch_decode(a, pl, status, st));
+    }
+  }
   uint16_t* sc = scores ? scores : static_cast<uint16_t*>(ws);
   csa_status s = run_indexer(qi_codes, qi_scales, ki_codes, ki_scales, B, Nq, q_pos0, E, m, H_I,
                              d_I, sc, nullptr, st, nullptr, fr);
@@ -618,6 +648,7 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
   }
   uint8_t* ws_c = static_cast<uint8_t*>(ws);
   uint8_t* ws_h = ws_c + pair_csa_ws(c);
+  bool fused = false;  // the CSA decode layer ran as one launch (decode.cu)
   if (c) {
     const int64_t E = c->N / c->m;
     const int64_t j0 = c->compress_begin / c->m;
@@ -632,6 +663,52 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
     // When this call launched the pooling above, the indexer's predecessor is known: the pooling
     // of the index keys from j0 on (xi_raw), else the entry pooling, which writes nothing the
     // indexer reads. Without it the predecessor is unknown and the indexer waits first.
+    Freshness fr;
+    if (E > j0) {
+      fr.keys_from = c->xi_raw ? j0 : E;
+      fr.queries = false;
+    }
+    // Decode with 64 heads of dim 128 or fewer: indexer, top-k and attention in one launch.
+    if (decode_indexer_fits(c->Nq, c->H_I, c->d_I) && c->d == 128 && c->H <= 64) {
+      const int64_t nv = std::max<int64_t>(0, std::min<int64_t>(E, (c->q_pos0 + 1) / c->m));
+      const DecodePlan pl = plan_decode(c->B, E, nv, c->k, c->W, true, c->scores != nullptr);
+      if (pl.ok) {
+        DecodeArgs a{};
+        a.qi_codes = c->qi_codes;
+        a.qi_scales = c->qi_scales;
+        a.ki_codes = c->ki_codes;
+        a.ki_scales = c->ki_scales;
+        a.scores = c->scores;
+        a.topk_idx = c->topk_idx;
+        a.topk_cnt = c->topk_cnt;
+        a.E = E;
+        a.t = c->q_pos0;
+        a.m = c->m;
+        a.k = c->k;
+        a.H_I = c->H_I;
+        a.B = c->B;
+        a.keys_fresh_from = fr.keys_from;
+        a.wait_first = fr.queries;
+        a.attend = true;
+        a.H = c->H;
+        a.W = c->W;
+        a.q = c->q;
+        a.k_cmp = c->k_cmp;
+        a.v_cmp = c->v_cmp;
+        a.k_raw = c->k_raw;
+        a.v_raw = c->v_raw;
+        a.out = c->out;
+        a.lse = c->lse;
+        a.N = c->N;
+        a.fresh_from = E > j0 ? j0 : 0;  // the entry pooling above writes [j0, E)
+        if (launch_decode(a, pl, status, st) != cudaSuccess) return CSA_ERR_CUDA;
+        fused = true;
+      }
+    }
+  }
+  if (c && !fused) {
+    const int64_t E = c->N / c->m;
+    const int64_t j0 = c->compress_begin / c->m;
     Freshness fr;
     if (E > j0) {
       fr.keys_from = c->xi_raw ? j0 : E;

@@ -165,6 +165,11 @@ CSA_DEV void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uin
       : "memory");
 }
 
+// Brings `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2, asynchronously.
+CSA_DEV void prefetch_l2(const void* gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
 CSA_DEV void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -355,6 +360,14 @@ CSA_DEV void tmem_st_16x256b_x8(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 
+// One 8-column group of the 16x256b shape: thread t gets r[0], r[1] = lane l + t/4, columns
+// 2(t%4) and +1; r[2], r[3] = lane l + 8 + t/4, the same columns.
+CSA_DEV void tmem_ld_16x256b_x1(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+}
+
 CSA_DEV void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.16x256b.x4.b32 {"
@@ -432,6 +445,30 @@ CSA_DEV float4 dsmem_ld_f32x4(const void* local_ptr, uint32_t cta) {
                : "memory");
   return v;
 }
+// Address of the same shared-memory location in CTA `cta` of this cluster.
+CSA_DEV uint32_t dsmem_map(const void* local_ptr, uint32_t cta) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local_ptr)), "r"(cta));
+  return ra;
+}
+// Stores / atomic adds into another CTA's shared memory (fire-and-forget; a later cluster
+// barrier with release / acquire makes them visible there).
+CSA_DEV void dsmem_st_u32(uint32_t remote, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+CSA_DEV void dsmem_st_u32x4(uint32_t remote, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+CSA_DEV void dsmem_st_f32x2(uint32_t remote, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(v.x), "f"(v.y)
+               : "memory");
+}
+CSA_DEV void dsmem_red_add_u32(uint32_t remote, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+
 CSA_DEV float2 dsmem_ld_f32x2(const void* local_ptr, uint32_t cta) {
   uint32_t ra;
   float2 v;

@@ -150,4 +150,48 @@ int attend_tc_chunk_keys();
 cudaError_t launch_attend_tc(const AttendArgs& a, int n_splits, int cluster, float* ws_o,
                              float* ws_ml, uint32_t* status, cudaStream_t stream);
 
+// ---- fused CSA decode step (decode.cu): indexer + top-k (+ sparse attention) in one launch ----
+constexpr int kDecodeMaxCluster = 16;   // CTAs per sequence
+constexpr int kDecodeMaxChunk = 16384;  // entries one CTA scores (BF16 scores kept on chip)
+constexpr int kDecodeMaxKeys = 256;     // attention keys one CTA gathers
+constexpr int kDecodeMaxSel = 2048;     // largest k
+constexpr int kDecodeFusedChunk = 8192; // the layer pair fuses the attention up to this chunk
+constexpr int kMaxDevicesDecode = 64;
+struct DecodePlan {
+  bool ok;
+  int C, chunk, P;  // cluster size, entries per CTA, attention keys per CTA
+};
+struct DecodeArgs {
+  const uint8_t* qi_codes;   // [B, H_I, 32] (one query per sequence, d_I = 64)
+  const uint8_t* qi_scales;  // [B, H_I, 2]
+  const uint8_t* ki_codes;   // [B, E, 32]
+  const uint8_t* ki_scales;  // [B, E, 2]
+  uint16_t* scores;          // optional [B, E] BF16 scores
+  int32_t* topk_idx;         // [B, k]
+  int32_t* topk_cnt;         // [B]
+  int64_t E, t;              // entries, position of the query token
+  int m, k, H_I, B;
+  int64_t keys_fresh_from;   // as launch_indexer
+  bool wait_first;           // true: the kernel before may write any input (queries included)
+  bool attend;               // also the sparse attention (d = 128, H <= 64)
+  int H, W;
+  const uint16_t* q;         // [B, H, 128]
+  const uint16_t* k_cmp;
+  const uint16_t* v_cmp;     // [B, E, 128]
+  const uint16_t* k_raw;
+  const uint16_t* v_raw;     // [B, N, 128]
+  uint16_t* out;             // [B, H, 128]
+  float* lse;                // optional [B, H]
+  int64_t N;
+  // entry-cache rows at or above it may still be written by the kernel before this one (they
+  // are read only after the grid-dependency wait); 0: any row may be
+  int64_t fresh_from;
+};
+// ok = false when the shape is outside the kernel's limits (E % 8 != 0, k > 2048, more than
+// 16 x 16384 visible entries, more than 16 x 256 attention keys).
+DecodePlan plan_decode(int B, int64_t E, int64_t n_vis, int k, int W, bool attend,
+                       bool want_scores);
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, uint32_t* status,
+                          cudaStream_t stream);
+
 }  // namespace csa

@@ -48,3 +48,14 @@ def test_optional_rows_add_their_kernels():
     # the chunk's 2048 blocks: 4 index-key rows of 128 B + 4 logits read, 34 B of keys written
     assert w["index_keys"]["bytes"] == 2048 * (4 * (128 + 4) + 34)
     assert "index_keys" not in bench.layer_work(s)
+
+
+def test_fused_decode_kernel_work_is_its_steps_without_the_score_round_trip():
+    # one launch scores, selects and attends: its bytes are the three steps' bytes less the
+    # BF16 scores the separate kernels write and read back (32768 x 2 B x 2 per sequence)
+    w = bench.step_work(get_config("csa_decode_128k"))
+    B = 16
+    parts = w["indexer_mxf4"]["bytes"] + w["topk"]["bytes"] + w["csa_attend"]["bytes"]
+    assert w["csa_decode"]["bytes"] == parts - B * 32768 * 4
+    assert w["csa_decode"]["flops"] == w["indexer_mxf4"]["flops"] + w["csa_attend"]["flops"]
+    assert w["indexer_topk"]["bytes"] == w["indexer_mxf4"]["bytes"] + w["topk"]["bytes"]

@@ -1,0 +1,126 @@
+"""Parity of the one-launch CSA decode step (indexer, top-k and sparse attention of one query
+token per sequence in one kernel, one thread-block cluster per sequence) with the fp64 oracle.
+
+The step runs through csa_hca_layer_pair with a CSA layer only (its decode path with 64 heads of
+dim 128 or fewer) and through csa_index_topk (the same kernel without the attention). Shapes
+cover: several entry tiles per CTA with a ragged tail, every visible entry selected (k at or
+above the visible count), a single entry, no window, fewer heads than 64, scores whose
+k-th largest lies far below the maximum (the exact radix select instead of the near-max
+histogram), selections that all fall in one CTA's share of the entries (the attention runs then
+read another CTA's list), and a block size of 1. Top-k lists are compared bit for bit,
+attention outputs within max-abs 1e-2 and relative L2 5e-3, LSE within 2e-3."""
+import numpy as np
+import pytest
+import torch
+
+import long_context_compressed_pooling_b300 as csa
+import oracle as O
+from synth import LayerShape, generate_layer
+from _helpers import assert_attention_close, assert_lse_close, bits, f64, npy
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    if torch.cuda.is_available():
+        csa.device_status(reset=True)
+    yield
+    if torch.cuda.is_available():
+        assert csa.device_status(reset=True) == 0
+
+
+def _layer(B, N, m, k, W, H, seed, skew=None):
+    s = LayerShape("csa", B=B, N=N, Nq=1, q_pos0=N - 1, H=H, d=128, m=m, W=W, k=k, H_I=4,
+                   d_I=64, q_scale=1.0 / np.sqrt(128), compress_begin=max(0, (N // m - 1) * m))
+    x = generate_layer(s, seed=seed, device=DEV)
+    E = N // m
+    if skew == "far" and E > 0:
+        # a few entries score 16x above the rest: fewer than k keys lie within 255 BF16 steps
+        # of the maximum, so the threshold comes from the exact radix select
+        x["ki_scales"][:] = 123
+        x["ki_scales"][:, : min(E, 10)] = 127
+    elif skew == "last" and E > 0:
+        # the largest scores all sit in the last eighth of the entries
+        x["ki_scales"][:] = 123
+        x["ki_scales"][:, E - E // 8:] = 127
+    kc = torch.empty((B, E, 128), dtype=torch.bfloat16, device=DEV)
+    vc = torch.empty_like(kc)
+    if s.compress_begin > 0:
+        csa.compress(x["k_raw"], x["v_raw"], x["logits"], m, kc, vc, 0, s.compress_begin)
+    layer = dict(x, m=m, W=W, k=k, q_pos0=N - 1, compress_begin=s.compress_begin, k_cmp=kc,
+                 v_cmp=vc, out=torch.empty_like(x["q"]),
+                 lse=torch.empty((B, 1, H), dtype=torch.float32, device=DEV),
+                 topk_idx=torch.full((B, 1, k), -7, dtype=torch.int32, device=DEV),
+                 topk_cnt=torch.full((B, 1), -7, dtype=torch.int32, device=DEV),
+                 scores=torch.zeros((B, 1, E), dtype=torch.bfloat16, device=DEV))
+    return s, x, layer
+
+
+CASES = [
+    # B, N, m, k, W, H, skew
+    (3, 4096, 4, 64, 128, 64, None),      # 8 tiles: one or two per CTA
+    (2, 40032, 4, 300, 128, 64, None),    # ragged last tile, runs of ~27 keys per CTA
+    (16, 32768, 4, 512, 128, 64, None),   # the benchmark's batch and k at 1/4 of the context
+    (2, 1024, 4, 512, 128, 64, None),     # every visible entry selected
+    (2, 7, 4, 16, 128, 64, None),         # one entry: the window dominates
+    (2, 8192, 4, 128, 0, 64, None),       # no window
+    (2, 8192, 4, 100, 64, 16, None),      # 16 heads
+    (2, 16384, 4, 64, 128, 64, "far"),    # exact radix select
+    (2, 65536, 4, 2048, 128, 64, "last"), # every selected entry in one CTA's share
+    (1, 2000, 1, 77, 32, 64, None),       # block size 1
+]
+
+
+@pytest.mark.parametrize("B,N,m,k,W,H,skew", CASES)
+def test_decode_step_matches_oracle(B, N, m, k, W, H, skew):
+    s, x, layer = _layer(B, N, m, k, W, H, seed=N + k + B, skew=skew)
+    csa.layer_pair(layer, None)
+    torch.cuda.synchronize()
+    assert csa.device_status(reset=True) == 0
+    E = N // m
+    nv = O.visible_entries(N - 1, m, E)
+    for b in range(B):
+        qb, kr, vr = bits(x["q"][b]), bits(x["k_raw"][b]), bits(x["v_raw"][b])
+        w = npy(x["logits"][b])
+        ref = O.csa_layer_seq(qb, kr, vr, w, npy(x["qi_codes"][b]), npy(x["qi_scales"][b]),
+                              npy(x["ki_codes"][b]), npy(x["ki_scales"][b]), m=m, W=W, k=k,
+                              d_I=64, q_pos0=N - 1)
+        assert int(npy(layer["topk_cnt"][b])[0]) == int(ref["cnt"][0]), b
+        np.testing.assert_array_equal(npy(layer["topk_idx"][b, 0]), ref["idx"][0],
+                                      err_msg=f"top-k b={b}")
+        if nv > k:  # the scores are computed (not needed when everything is selected)
+            np.testing.assert_array_equal(bits(layer["scores"][b, 0])[:nv], ref["scores"][0],
+                                          err_msg=f"scores b={b}")
+        # attention on the layer's own bf16 entries, and the whole layer on the oracle's pooling
+        o, l = O.csa_attend_one(O.bf16_to_f64(qb[0]), f64(layer["k_cmp"][b]),
+                                f64(layer["v_cmp"][b]), ref["idx"][0], int(ref["cnt"][0]),
+                                O.bf16_to_f64(kr), O.bf16_to_f64(vr), N - 1, W)
+        assert_attention_close(f64(layer["out"][b, 0]), o, f"out b={b}")
+        assert_lse_close(npy(layer["lse"][b, 0]), l, f"lse b={b}")
+        assert_attention_close(f64(layer["out"][b, 0]), ref["out"][0], f"layer b={b}")
+
+
+@pytest.mark.parametrize("B,N,k,skew", [(4, 1048576, 2048, None), (5, 160000, 300, "far")])
+def test_decode_index_topk_matches_oracle(B, N, k, skew):
+    """csa_index_topk with one query per sequence: the same kernel without the attention."""
+    m = 4
+    E = N // m
+    s = LayerShape("csa", B=B, N=N, Nq=1, q_pos0=N - 1, H=64, d=128, m=m, W=128, k=k, H_I=4,
+                   d_I=64, q_scale=1.0 / np.sqrt(128), compress_begin=N - m)
+    x = generate_layer(s, seed=3 * N + k, device=DEV, skip=("q", "k_raw", "v_raw", "logits"))
+    if skew == "far":
+        x["ki_scales"][:] = 123
+        x["ki_scales"][:, :10] = 127
+    idx, cnt, sc = csa.index_topk(x["qi_codes"], x["qi_scales"], x["ki_codes"], x["ki_scales"],
+                                  N - 1, m, k, want_scores=True)
+    torch.cuda.synchronize()
+    qc, qs, kc, ks = (npy(x[n]) for n in ("qi_codes", "qi_scales", "ki_codes", "ki_scales"))
+    scb = bits(sc)
+    for b in range(B):
+        ref = O.f64_to_bf16_rne(O.index_scores(qc[b, 0], qs[b, 0], kc[b], ks[b], 64))
+        np.testing.assert_array_equal(scb[b, 0], ref, err_msg=f"scores b={b}")
+        ridx, rcnt = O.topk_select(ref, E, k)
+        assert int(npy(cnt)[b, 0]) == rcnt
+        np.testing.assert_array_equal(npy(idx)[b, 0], ridx, err_msg=f"top-k b={b}")
