@@ -145,23 +145,33 @@ FUSED = {"csa_decode": ("indexer_mxf4", "topk", "csa_attend"),
 
 
 def step_work(wl, index_keys=False):
+    """Algorithmic bytes / FLOPs per step of each step of the path (the step's totals are their
+    sums); see kernel_work for the kernels that run several steps in one launch."""
     kernels = {}
     for s in wl.layers:
         for n, v in layer_work(s, index_keys).items():
             a = kernels.setdefault(n, dict(bytes=0, flops=0))
             a["bytes"] += v["bytes"]
             a["flops"] += v["flops"]
+    return kernels
+
+
+def kernel_work(wl, work):
+    """step_work plus the fused kernels' work: the sum of their steps', and for the fused
+    decode kernel without the BF16 scores the separate kernels write and read back (it keeps
+    them on chip)."""
+    out = dict(work)
     for name, parts in FUSED.items():
-        if all(p in kernels for p in parts):
-            kernels[name] = dict(bytes=sum(kernels[p]["bytes"] for p in parts),
-                                 flops=sum(kernels[p]["flops"] for p in parts))
-    # the fused decode kernel keeps the BF16 scores on chip: no score bytes
-    if "csa_decode" in kernels:
+        if all(p in work for p in parts):
+            out[name] = dict(bytes=sum(work[p]["bytes"] for p in parts),
+                             flops=sum(work[p]["flops"] for p in parts))
+    if "csa_decode" in out:
         for s in wl.layers:
             if s.kind == "csa":
                 nv = sum(_vis(s.q_pos0 + i, s.m, s.E) for i in range(s.Nq))
-                kernels["csa_decode"]["bytes"] -= s.B * nv * 2 * 2  # written + read back
-    return kernels
+                out["csa_decode"] = dict(out["csa_decode"],
+                                         bytes=out["csa_decode"]["bytes"] - s.B * nv * 2 * 2)
+    return out
 
 
 def rank_seed(wl, rank):
@@ -602,8 +612,9 @@ def run_workload(args, name, rank, world, dev, local):
         timed_loop(call)
         prof = csa.profiler_collect(reset=True)
         csa.profiler_enable(False)
-        kern = kernel_times(prof, work, K, ms_step)
-        out.update(rooflines(kern, work, wl.name, wl.mode))
+        kwork = kernel_work(wl, work)
+        kern = kernel_times(prof, kwork, K, ms_step)
+        out.update(rooflines(kern, kwork, wl.name, wl.mode))
         out["kernels"] = kern
         out["gpu_launches"] = int(round(sum(v["launches_per_step"] for v in kern.values()) * K))
     out["clocks"] = clk.summary()

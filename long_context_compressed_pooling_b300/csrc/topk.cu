@@ -10,7 +10,8 @@
 // One CTA or thread-block cluster per query row, holding the row in registers: CTA rank r of
 // a cluster of C owns a contiguous chunk of NT x KPT keys, every thread KPT contiguous keys of
 // it. The shape is picked per launch: rows of up to 32768 keys with enough rows to fill the GPU
-// (prefill) take one CTA of 1024 threads x 32 keys; few rows (decode) are spread over clusters
+// (prefill) take one CTA per row, the smallest shape that holds the row (128 threads x 8 keys
+// up to 1024 x 32); few rows (decode) are spread over clusters
 // of 256-1024-thread CTAs so that the grid covers the SMs (a 32768-key row: 8 CTAs of 4096
 // keys; a 262144-key row at 1M context: 16 CTAs of 16384). The cluster exchanges only the CTA
 // maxima, 256-bin histograms and selected-key counts through distributed shared memory after
@@ -480,7 +481,7 @@ struct RegShape {
   int nt, kpt;
   int chunk() const { return nt * kpt; }
 };
-constexpr RegShape kRegShapes[] = {{256, 16}, {512, 16}, {1024, 16}, {1024, 32}};
+constexpr RegShape kRegShapes[] = {{128, 8}, {256, 16}, {512, 16}, {1024, 16}, {1024, 32}};
 constexpr int kMaxRegCluster = 16;
 
 template <int NT, int KPT, bool F32>
@@ -528,16 +529,17 @@ bool reg_cluster_fits(int C) {
 template <bool F32>
 bool reg_fits_query(int shape, int C) {
   switch (shape) {
-    case 0: return reg_cluster_fits<256, 16, F32>(C);
-    case 1: return reg_cluster_fits<512, 16, F32>(C);
-    case 2: return reg_cluster_fits<1024, 16, F32>(C);
+    case 0: return reg_cluster_fits<128, 8, F32>(C);
+    case 1: return reg_cluster_fits<256, 16, F32>(C);
+    case 2: return reg_cluster_fits<512, 16, F32>(C);
+    case 3: return reg_cluster_fits<1024, 16, F32>(C);
     default: return reg_cluster_fits<1024, 32, F32>(C);
   }
 }
 
 // Answers are cached per (key width, shape, cluster size): 0 unknown, 1 fits, 2 does not.
 bool reg_fits(int shape, int C, bool f32) {
-  static volatile int8_t cache[2][4][kMaxRegCluster + 1] = {};
+  static volatile int8_t cache[2][5][kMaxRegCluster + 1] = {};
   if (C <= 8) return true;
   volatile int8_t& c = cache[f32 ? 1 : 0][shape][C];
   if (c == 0) c = (f32 ? reg_fits_query<true>(shape, C) : reg_fits_query<false>(shape, C)) ? 1 : 2;
@@ -551,7 +553,10 @@ bool reg_fits(int shape, int C, bool f32) {
 bool pick_reg(int64_t rows, int64_t n_max, int* shape, int* C, bool f32) {
   constexpr int nshapes = (int)(sizeof(kRegShapes) / sizeof(kRegShapes[0]));
   if (n_max <= kRegShapes[nshapes - 1].chunk() && rows >= kNumSMs) {
-    *shape = nshapes - 1;
+    // enough rows to fill the GPU: one CTA per row, the smallest one that holds the row
+    int i = 0;
+    while (kRegShapes[i].chunk() < n_max) ++i;
+    *shape = i;
     *C = 1;
     return true;
   }
@@ -614,12 +619,15 @@ cudaError_t launch_reg_shape(int shape, const void* scores, int Nq, int64_t q_po
                              int C, cudaStream_t stream) {
   switch (shape) {
     case 0:
+      return launch_reg<128, 8, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
+                                     stream);
+    case 1:
       return launch_reg<256, 16, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
                                       stream);
-    case 1:
+    case 2:
       return launch_reg<512, 16, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
                                       stream);
-    case 2:
+    case 3:
       return launch_reg<1024, 16, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
                                        stream);
     default:

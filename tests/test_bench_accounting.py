@@ -53,9 +53,18 @@ def test_optional_rows_add_their_kernels():
 def test_fused_decode_kernel_work_is_its_steps_without_the_score_round_trip():
     # one launch scores, selects and attends: its bytes are the three steps' bytes less the
     # BF16 scores the separate kernels write and read back (32768 x 2 B x 2 per sequence)
-    w = bench.step_work(get_config("csa_decode_128k"))
+    wl = get_config("csa_decode_128k")
+    w = bench.kernel_work(wl, bench.step_work(wl))
     B = 16
     parts = w["indexer_mxf4"]["bytes"] + w["topk"]["bytes"] + w["csa_attend"]["bytes"]
     assert w["csa_decode"]["bytes"] == parts - B * 32768 * 4
     assert w["csa_decode"]["flops"] == w["indexer_mxf4"]["flops"] + w["csa_attend"]["flops"]
     assert w["indexer_topk"]["bytes"] == w["indexer_mxf4"]["bytes"] + w["topk"]["bytes"]
+
+
+def test_step_totals_count_each_step_once():
+    wl = get_config("csa_prefill_8k_of_128k")
+    w = bench.step_work(wl)
+    assert "csa_decode" not in w and "indexer_topk" not in w
+    assert sum(v["flops"] for v in w.values()) == w["indexer_mxf4"]["flops"] + \
+        w["csa_attend"]["flops"] + w["compress"]["flops"]
