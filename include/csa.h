@@ -12,7 +12,8 @@
  * The two layer types alternate along depth (elebank "DeepSeek-V4 explained", 模型創新 1).
  *
  * Conventions shared by every call:
- *   - All tensor pointers are DEVICE pointers, row-major and contiguous, 16-byte aligned.
+ *   - All tensor pointers are DEVICE pointers, row-major and contiguous, 16-byte aligned
+ *     (per-row counts such as topk_cnt: 4-byte aligned).
  *     The caller owns every buffer; the library never allocates device memory on these paths.
  *   - bf16 values travel as uint16_t bit patterns. `stream` is a cudaStream_t passed as void*
  *     (NULL = the legacy default stream). Every call is asynchronous on `stream`.
@@ -344,6 +345,45 @@ size_t csa_hca_layer_pair_workspace_size(const csa_layer_desc* csa, const hca_la
  * CSA_ERR_CUDA; reset != 0 clears the word afterwards.
  * ---------------------------------------------------------------------------------------- */
 csa_status csa_get_device_status(void* stream, int reset, uint32_t* flags_out);
+
+/* ----------------------------------------------------------------------------------------
+ * Entry-sharded decode: the compressed entries of each sequence split over S shards (GPUs, or
+ * slices of one GPU's cache); shard s holds entries [shard_base[s], shard_base[s] + E_s). The
+ * pages' 1M-token context (9fzt.com DeepSeek-V4 summary, item 1) with the CSA selection and
+ * attention of Lighthouse 八.3. Every entry of the global top-k is among its own shard's top-k,
+ * so merging the shards' candidates gives exactly the unsharded selection (score descending,
+ * ties to the lower global index); each shard then attends to its part of the selection (one
+ * shard also to the window) and the partial outputs merge by their log-sum-exp.
+ *
+ * csa_shard_candidates -- one shard's top-k candidates of one query per sequence: csa_index_topk
+ *   over the shard's entries (ki_codes / ki_scales point at the shard's first entry, E = E_s,
+ *   q_pos0 = t - shard_base * m so that visibility is the global one), returning the local
+ *   indices (cand_idx [B, k], ascending, -1 pad), their BF16 scores (cand_scores [B, k], 0 pad)
+ *   and counts (cand_cnt [B]). Workspace: csa_shard_candidates_workspace_size (the shard's
+ *   scores). Same limits as csa_index_topk.
+ * csa_topk_merge -- the global top-k of S shards' candidates, shard-major: cand_scores and
+ *   cand_idx [S, B, k], cand_cnt [S, B] (each shard's csa_shard_candidates outputs stacked, k of
+ *   every shard equal); shard_base: HOST array of S ascending first global indices.
+ *   topk_idx [B, k] global indices ascending, -1 pad; topk_cnt [B] = min(k, candidates);
+ *   shard_idx [S, B, k] the local indices of each shard's part of the selection (ascending, -1
+ *   pad); shard_cnt [S, B]. Supported: S <= 16, k <= 2048.
+ * csa_lse_merge -- out[r] = sum_s e^(lse_s[r] - L) parts[s][r] with L = log sum_s e^(lse_s[r])
+ *   (a shard with lse = -inf has weight 0; all -inf gives out = 0, lse = -inf).
+ *   parts [S, rows, d] bf16 (each shard's normalised output, as csa_attend writes it),
+ *   parts_lse [S, rows] fp32, out [rows, d] bf16, lse optional [rows]. d a multiple of 8.
+ * ---------------------------------------------------------------------------------------- */
+csa_status csa_shard_candidates(const uint8_t* qi_codes, const uint8_t* qi_scales,
+                                const uint8_t* ki_codes, const uint8_t* ki_scales, int B,
+                                int64_t q_pos0, int64_t E, int m, int H_I, int d_I, int k,
+                                int32_t* cand_idx, uint16_t* cand_scores, int32_t* cand_cnt,
+                                void* ws, size_t ws_bytes, void* stream);
+size_t csa_shard_candidates_workspace_size(int B, int64_t E, int k);
+csa_status csa_topk_merge(const uint16_t* cand_scores, const int32_t* cand_idx,
+                          const int32_t* cand_cnt, const int64_t* shard_base, int B, int S, int k,
+                          int32_t* topk_idx, int32_t* topk_cnt, int32_t* shard_idx,
+                          int32_t* shard_cnt, void* stream);
+csa_status csa_lse_merge(const uint16_t* parts, const float* parts_lse, int S, int64_t rows, int d,
+                         uint16_t* out, float* lse, void* stream);
 
 /* ----------------------------------------------------------------------------------------
  * csa_test_set_faults -- failure injection for tests of the device-side failure detection

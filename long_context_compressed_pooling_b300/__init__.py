@@ -26,13 +26,16 @@ from ._native import (  # noqa: F401
     index_scores,
     index_topk,
     layer_pair,
+    lse_merge,
     load_library,
     paged_decode_step,
     profiler_collect,
     profiler_enable,
     quantize_mxfp4,
+    shard_candidates,
     test_set_faults,
     topk,
     topk_f32,
+    topk_merge,
     workspace_sizes,
 )

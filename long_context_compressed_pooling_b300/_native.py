@@ -100,6 +100,12 @@ _SIGS = {
     "csa_status_string": (ctypes.c_char_p, [_I]),
     "csa_abi_version": (_I, []),
     "csa_test_set_faults": (_I, [ctypes.c_longlong, ctypes.c_uint32]),
+    "csa_shard_candidates": (_I, [_P, _P, _P, _P, _I, _L, _L, _I, _I, _I, _I, _P, _P, _P, _P, _Z,
+                                  _P]),
+    "csa_shard_candidates_workspace_size": (_Z, [_I, _L, _I]),
+    "csa_topk_merge": (_I, [_P, _P, _P, ctypes.POINTER(ctypes.c_int64), _I, _I, _I, _P, _P, _P,
+                            _P, _P]),
+    "csa_lse_merge": (_I, [_P, _P, _I, _L, _I, _P, _P, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -463,6 +469,64 @@ def device_status(reset: bool = True) -> int:
     if code not in (CSA_OK, 7):
         raise CsaError("csa_get_device_status", code)
     return int(flags.value)
+
+
+def shard_candidates(qi_codes, qi_scales, ki_codes, ki_scales, q_pos0: int, m: int, k: int,
+                     ws: Optional[torch.Tensor] = None):
+    """One shard's top-k candidates of one query per sequence (csa_shard_candidates): ki_* hold
+    the shard's entries [B, E_s, ...]; q_pos0 is the query position relative to the shard's first
+    token (t - shard_base * m). Returns (local indices [B, k] int32, BF16 scores [B, k], counts
+    [B] int32)."""
+    lib = load_library()
+    B, Nq, H_I, half = qi_codes.shape
+    if Nq != 1:
+        raise ValueError("one query per sequence")
+    E = ki_codes.shape[1]
+    dev = qi_codes.device
+    idx = torch.empty((B, k), dtype=torch.int32, device=dev)
+    sc = torch.empty((B, k), dtype=torch.bfloat16, device=dev)
+    cnt = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws, wsb = _ws(lib.csa_shard_candidates_workspace_size(B, E, k), dev, ws)
+    _check("csa_shard_candidates", lib.csa_shard_candidates(
+        _ptr(qi_codes), _ptr(qi_scales), _ptr(ki_codes), _ptr(ki_scales), B, q_pos0, E, m, H_I,
+        2 * half, k, _ptr(idx), _ptr(_u16(sc)), _ptr(cnt), _ptr(ws), wsb, _stream(dev)))
+    return idx, sc, cnt
+
+
+def topk_merge(cand_scores, cand_idx, cand_cnt, shard_base):
+    """The global top-k of S shards' candidates (csa_topk_merge), shard-major: cand_scores
+    [S, B, k] bf16, cand_idx [S, B, k] int32 (local), cand_cnt [S, B] int32, shard_base: S
+    ascending first global indices (host ints). Returns (topk_idx [B, k] global, topk_cnt [B],
+    shard_idx [S, B, k] local, shard_cnt [S, B])."""
+    lib = load_library()
+    S, B, k = cand_idx.shape
+    dev = cand_idx.device
+    bases = (ctypes.c_int64 * S)(*[int(x) for x in shard_base])
+    idx = torch.empty((B, k), dtype=torch.int32, device=dev)
+    cnt = torch.empty((B,), dtype=torch.int32, device=dev)
+    sidx = torch.empty((S, B, k), dtype=torch.int32, device=dev)
+    scnt = torch.empty((S, B), dtype=torch.int32, device=dev)
+    _check("csa_topk_merge", lib.csa_topk_merge(
+        _ptr(_u16(cand_scores)), _ptr(cand_idx), _ptr(cand_cnt), bases, B, S, k, _ptr(idx),
+        _ptr(cnt), _ptr(sidx), _ptr(scnt), _stream(dev)))
+    return idx, cnt, sidx, scnt
+
+
+def lse_merge(parts, parts_lse, out=None, lse=None, want_lse: bool = False):
+    """Merge S shards' normalised outputs parts [S, ..., d] (bf16) by their log-sum-exp
+    parts_lse [S, ...] (csa_lse_merge). Returns (out [..., d] bf16, lse [...] or None)."""
+    lib = load_library()
+    S = parts.shape[0]
+    d = parts.shape[-1]
+    rows = parts[0].numel() // d
+    dev = parts.device
+    if out is None:
+        out = torch.empty(parts.shape[1:], dtype=torch.bfloat16, device=dev)
+    if want_lse and lse is None:
+        lse = torch.empty(parts_lse.shape[1:], dtype=torch.float32, device=dev)
+    _check("csa_lse_merge", lib.csa_lse_merge(_ptr(_u16(parts)), _ptr(parts_lse), S, rows, d,
+                                              _ptr(out), _ptr(lse), _stream(dev)))
+    return out, lse
 
 
 FAULT_SKIP_KEY_COPIES = 0x1

@@ -83,6 +83,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// per-row counts are read and written one int32 at a time: 4-byte alignment is enough
+bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 csa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? CSA_OK : CSA_ERR_CUDA; }
 
@@ -126,14 +128,14 @@ csa_status check_index(const uint8_t* qi_codes, const uint8_t* qi_scales,
                                     H_I, d_I, scores);
   if (s != CSA_OK) return s;
   if (!topk_idx || !topk_cnt || k < 1) return CSA_ERR_INVALID_ARG;
-  if (!al16(topk_idx) || !al16(topk_cnt)) return CSA_ERR_ALIGN;
+  if (!al16(topk_idx) || !al4(topk_cnt)) return CSA_ERR_ALIGN;
   return CSA_OK;
 }
 
 csa_status check_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
                       int k, const int32_t* topk_idx, const int32_t* topk_cnt) {
   if (!scores || !topk_idx || !topk_cnt) return CSA_ERR_INVALID_ARG;
-  if (!al16(scores) || !al16(topk_idx) || !al16(topk_cnt)) return CSA_ERR_ALIGN;
+  if (!al16(scores) || !al16(topk_idx) || !al4(topk_cnt)) return CSA_ERR_ALIGN;
   if (B < 1 || Nq < 1 || q_pos0 < 0 || E < 0 || m < 1 || k < 1) return CSA_ERR_INVALID_ARG;
   if ((int64_t)B * Nq > ((int64_t)1 << 31) - 1) return CSA_ERR_UNSUPPORTED;
   return CSA_OK;
@@ -324,7 +326,7 @@ csa_status check_paged(const csa_paged_layer* L) {
       (L->lse && (uintptr_t)L->lse % 4))
     return CSA_ERR_ALIGN;
   if (csa_kind && (!al16(L->ki_codes_pool) || !al16(L->ki_scales_pool) || !al16(L->qi_codes) ||
-                   !al16(L->topk_idx) || !al16(L->topk_cnt) ||
+                   !al16(L->topk_idx) || !al4(L->topk_cnt) ||
                    (L->ring_xi && (!al16(L->ring_xi) || !al16(L->xi_new)))))
     return CSA_ERR_ALIGN;
   if (L->B < 1 || L->H < 1 || L->N < 0 || L->W < 0 || L->n_pages < 1 || L->max_blocks < 1)
@@ -436,6 +438,66 @@ static csa_status paged_step(const csa_paged_layer* L, void* ws, cudaStream_t st
   return from_cuda(launch_attend(a, E + L->W, ws, status, st));
 }
 
+
+size_t csa_shard_candidates_workspace_size(int B, int64_t E, int k) {
+  (void)k;
+  if (B < 1 || E < 0) return 0;
+  return round_up((size_t)B * (size_t)E * 2, 256);
+}
+
+csa_status csa_shard_candidates(const uint8_t* qi_codes, const uint8_t* qi_scales,
+                                const uint8_t* ki_codes, const uint8_t* ki_scales, int B,
+                                int64_t q_pos0, int64_t E, int m, int H_I, int d_I, int k,
+                                int32_t* cand_idx, uint16_t* cand_scores, int32_t* cand_cnt,
+                                void* ws, size_t ws_bytes, void* stream) {
+  csa_status s = check_index(qi_codes, qi_scales, ki_codes, ki_scales, B, 1, q_pos0, E, m, H_I,
+                             d_I, k, cand_idx, cand_cnt, nullptr);
+  if (s != CSA_OK) return s;
+  if (!cand_scores) return CSA_ERR_INVALID_ARG;
+  if (!al16(cand_scores)) return CSA_ERR_ALIGN;
+  const size_t need = csa_shard_candidates_workspace_size(B, E, k);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !al16(ws))) return CSA_ERR_WORKSPACE;
+  uint32_t* status = status_word();
+  if (!status) return CSA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint16_t* sc = static_cast<uint16_t*>(ws);  // the shard's BF16 scores
+  s = run_index_topk(qi_codes, qi_scales, ki_codes, ki_scales, B, 1, q_pos0, E, m, H_I, d_I, k,
+                     cand_idx, cand_cnt, sc, nullptr, st);
+  if (s != CSA_OK) return s;
+  return from_cuda(launch_candidates(sc, B, E, cand_idx, cand_cnt, k, cand_scores, status, st));
+}
+
+csa_status csa_topk_merge(const uint16_t* cand_scores, const int32_t* cand_idx,
+                          const int32_t* cand_cnt, const int64_t* shard_base, int B, int S, int k,
+                          int32_t* topk_idx, int32_t* topk_cnt, int32_t* shard_idx,
+                          int32_t* shard_cnt, void* stream) {
+  if (!cand_scores || !cand_idx || !cand_cnt || !shard_base || !topk_idx || !topk_cnt ||
+      !shard_idx || !shard_cnt)
+    return CSA_ERR_INVALID_ARG;
+  if (!al16(cand_scores) || !al16(cand_idx) || !al16(topk_idx) || !al16(shard_idx))
+    return CSA_ERR_ALIGN;
+  if (B < 1 || S < 1 || k < 1) return CSA_ERR_INVALID_ARG;
+  if (S > kMaxShards || k > 2048) return CSA_ERR_UNSUPPORTED;
+  for (int i = 0; i < S; ++i)
+    if (shard_base[i] < 0 || (i > 0 && shard_base[i] < shard_base[i - 1]) ||
+        shard_base[i] + k > ((int64_t)1 << 31))
+      return CSA_ERR_SHAPE;
+  return from_cuda(launch_topk_merge(cand_scores, cand_idx, cand_cnt, shard_base, B, S, k, topk_idx,
+                                     topk_cnt, shard_idx, shard_cnt,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+csa_status csa_lse_merge(const uint16_t* parts, const float* parts_lse, int S, int64_t rows, int d,
+                         uint16_t* out, float* lse, void* stream) {
+  if (!parts || !parts_lse || !out) return CSA_ERR_INVALID_ARG;
+  if (!al16(parts) || !al16(out) || (uintptr_t)parts_lse % 4 || (lse && (uintptr_t)lse % 4))
+    return CSA_ERR_ALIGN;
+  if (S < 1 || rows < 0) return CSA_ERR_INVALID_ARG;
+  if (d % 8 != 0 || d < 8 || d > 1024) return CSA_ERR_UNSUPPORTED;
+  if (rows == 0) return CSA_OK;
+  return from_cuda(launch_lse_merge(parts, parts_lse, S, rows, d, out, lse,
+                                    static_cast<cudaStream_t>(stream)));
+}
 
 int csa_abi_version(void) { return 3; }
 
@@ -563,7 +625,7 @@ csa_status csa_attend(const uint16_t* q, const uint16_t* k_cmp, const uint16_t* 
   csa_status s = check_attend(q, k_cmp, v_cmp, E, k_raw, v_raw, N, W, B, Nq, q_pos0, H, d, out, lse);
   if (s != CSA_OK) return s;
   if (!topk_idx || !topk_cnt || k < 0) return CSA_ERR_INVALID_ARG;
-  if (!al16(topk_idx) || !al16(topk_cnt)) return CSA_ERR_ALIGN;
+  if (!al16(topk_idx) || !al4(topk_cnt)) return CSA_ERR_ALIGN;
   const size_t need = attend_workspace_bytes(B * Nq, H, d, (int64_t)k + W);
   if (need > 0 && (ws == nullptr || ws_bytes < need || !al16(ws))) return CSA_ERR_WORKSPACE;
   uint32_t* status = status_word();

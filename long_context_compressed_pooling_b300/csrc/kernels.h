@@ -150,6 +150,21 @@ int attend_tc_chunk_keys();
 cudaError_t launch_attend_tc(const AttendArgs& a, int n_splits, int cluster, float* ws_o,
                              float* ws_ml, uint32_t* status, cudaStream_t stream);
 
+// ---- entry-sharded selection and attention (shard.cu) ------------------------------------------
+constexpr int kMaxShards = 16;
+// cand_scores[b][j] = scores[b][sel[b][j]] for j < cnt[b], else 0.
+cudaError_t launch_candidates(const uint16_t* scores, int B, int64_t E, const int32_t* sel,
+                              const int32_t* cnt, int k, uint16_t* cand_scores, uint32_t* status,
+                              cudaStream_t stream);
+// The global top-k of S shards' candidates [S, B, k] (local indices; shard_base: host array of
+// S first global indices), and each shard's part of it [S, B, k] (local indices).
+cudaError_t launch_topk_merge(const uint16_t* cand_scores, const int32_t* cand_idx,
+                              const int32_t* cand_cnt, const int64_t* shard_base, int B, int S,
+                              int k, int32_t* topk_idx, int32_t* topk_cnt, int32_t* shard_idx,
+                              int32_t* shard_cnt, cudaStream_t stream);
+cudaError_t launch_lse_merge(const uint16_t* parts, const float* lse, int S, int64_t rows, int d,
+                             uint16_t* out, float* lse_out, cudaStream_t stream);
+
 // ---- fused CSA decode step (decode.cu): indexer + top-k (+ sparse attention) in one launch ----
 constexpr int kDecodeMaxCluster = 16;   // CTAs per sequence
 constexpr int kDecodeMaxChunk = 16384;  // entries one CTA scores (BF16 scores kept on chip)

@@ -205,3 +205,16 @@ def test_fault_injection_switches_are_validated_and_restorable(lib):
     assert lib.csa_test_set_faults(1000, 0x80) == 1   # unknown producer bit
     assert lib.csa_test_set_faults(2_000_000, 0x1) == 0
     assert lib.csa_test_set_faults(0, 0) == 0          # defaults restored
+
+
+def test_sharded_calls_validate_before_launching(lib):
+    a = _p(ALN)
+    bases = (ctypes.c_int64 * 3)(0, 100, 50)  # not ascending
+    assert lib.csa_topk_merge(a, a, a, bases, 2, 3, 64, a, a, a, a, None) == 2
+    ok = (ctypes.c_int64 * 17)(*range(0, 1700, 100))
+    assert lib.csa_topk_merge(a, a, a, ok, 2, 17, 64, a, a, a, a, None) == 5   # S > 16
+    assert lib.csa_topk_merge(a, a, a, ok, 2, 4, 4096, a, a, a, a, None) == 5  # k > 2048
+    assert lib.csa_topk_merge(None, a, a, ok, 2, 4, 64, a, a, a, a, None) == 1
+    assert lib.csa_lse_merge(a, a, 2, 10, 60, a, None, None) == 5              # d % 8
+    assert lib.csa_lse_merge(a, a, 0, 10, 64, a, None, None) == 1
+    assert lib.csa_shard_candidates_workspace_size(2, 1000, 64) == 4096
