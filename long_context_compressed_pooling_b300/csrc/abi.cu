@@ -714,7 +714,16 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
   if (c) {
     const int64_t E = c->N / c->m;
     const int64_t j0 = c->compress_begin / c->m;
-    if (launch_compress(c->k_raw, c->v_raw, c->logits, c->B, c->N, c->d, c->m, j0, E - j0,
+    // Decode with 64 heads of dim 128 or fewer: indexer, top-k and attention in one launch,
+    // which also pools the few blocks the step closes when no index keys are pooled with them.
+    DecodePlan pl{};
+    if (decode_indexer_fits(c->Nq, c->H_I, c->d_I) && c->d == 128 && c->H <= 64) {
+      const int64_t nv = std::max<int64_t>(0, std::min<int64_t>(E, (c->q_pos0 + 1) / c->m));
+      pl = plan_decode(c->B, E, nv, c->k, c->W, true, c->scores != nullptr);
+    }
+    const bool pool_inside = pl.ok && !c->xi_raw && E - j0 <= kDecodePoolMax;
+    if (!pool_inside &&
+        launch_compress(c->k_raw, c->v_raw, c->logits, c->B, c->N, c->d, c->m, j0, E - j0,
                         c->k_cmp, c->v_cmp, st) != cudaSuccess)
       return CSA_ERR_CUDA;
     if (c->xi_raw &&
@@ -722,50 +731,44 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
                           const_cast<uint8_t*>(c->ki_codes), const_cast<uint8_t*>(c->ki_scales),
                           st) != cudaSuccess)
       return CSA_ERR_CUDA;
-    // When this call launched the pooling above, the indexer's predecessor is known: the pooling
-    // of the index keys from j0 on (xi_raw), else the entry pooling, which writes nothing the
-    // indexer reads. Without it the predecessor is unknown and the indexer waits first.
-    Freshness fr;
-    if (E > j0) {
-      fr.keys_from = c->xi_raw ? j0 : E;
-      fr.queries = false;
-    }
-    // Decode with 64 heads of dim 128 or fewer: indexer, top-k and attention in one launch.
-    if (decode_indexer_fits(c->Nq, c->H_I, c->d_I) && c->d == 128 && c->H <= 64) {
-      const int64_t nv = std::max<int64_t>(0, std::min<int64_t>(E, (c->q_pos0 + 1) / c->m));
-      const DecodePlan pl = plan_decode(c->B, E, nv, c->k, c->W, true, c->scores != nullptr);
-      if (pl.ok) {
-        DecodeArgs a{};
-        a.qi_codes = c->qi_codes;
-        a.qi_scales = c->qi_scales;
-        a.ki_codes = c->ki_codes;
-        a.ki_scales = c->ki_scales;
-        a.scores = c->scores;
-        a.topk_idx = c->topk_idx;
-        a.topk_cnt = c->topk_cnt;
-        a.E = E;
-        a.t = c->q_pos0;
-        a.m = c->m;
-        a.k = c->k;
-        a.H_I = c->H_I;
-        a.B = c->B;
-        a.keys_fresh_from = fr.keys_from;
-        a.wait_first = fr.queries;
-        a.attend = true;
-        a.H = c->H;
-        a.W = c->W;
-        a.q = c->q;
-        a.k_cmp = c->k_cmp;
-        a.v_cmp = c->v_cmp;
-        a.k_raw = c->k_raw;
-        a.v_raw = c->v_raw;
-        a.out = c->out;
-        a.lse = c->lse;
-        a.N = c->N;
-        a.fresh_from = E > j0 ? j0 : 0;  // the entry pooling above writes [j0, E)
-        if (launch_decode(a, pl, status, st) != cudaSuccess) return CSA_ERR_CUDA;
-        fused = true;
-      }
+    if (pl.ok) {
+      DecodeArgs a{};
+      a.qi_codes = c->qi_codes;
+      a.qi_scales = c->qi_scales;
+      a.ki_codes = c->ki_codes;
+      a.ki_scales = c->ki_scales;
+      a.scores = c->scores;
+      a.topk_idx = c->topk_idx;
+      a.topk_cnt = c->topk_cnt;
+      a.E = E;
+      a.t = c->q_pos0;
+      a.m = c->m;
+      a.k = c->k;
+      a.H_I = c->H_I;
+      a.B = c->B;
+      // When this call launched the pooling, the kernel's predecessor is known: the pooling of
+      // the index keys from j0 on (xi_raw), else the entry pooling, which writes nothing the
+      // indexer reads and the entries from j0 on. Otherwise the predecessor is unknown and the
+      // kernel waits for it before reading anything.
+      a.wait_first = pool_inside || E <= j0;
+      a.keys_fresh_from = c->xi_raw ? j0 : E;
+      a.fresh_from = E > j0 ? j0 : E;
+      a.attend = true;
+      a.H = c->H;
+      a.W = c->W;
+      a.q = c->q;
+      a.k_cmp = c->k_cmp;
+      a.v_cmp = c->v_cmp;
+      a.k_raw = c->k_raw;
+      a.v_raw = c->v_raw;
+      a.out = c->out;
+      a.lse = c->lse;
+      a.N = c->N;
+      a.logits = c->logits;
+      a.pool_j0 = pool_inside ? j0 : E;
+      a.pool_j1 = E;
+      if (launch_decode(a, pl, status, st) != cudaSuccess) return CSA_ERR_CUDA;
+      fused = true;
     }
   }
   if (c && !fused) {

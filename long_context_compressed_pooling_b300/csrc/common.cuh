@@ -53,6 +53,39 @@ CSA_DEV uint32_t smem_addr(const void* p) {
 CSA_DEV float exp2_int(int e) { return __int_as_float((e + 127) << 23); }
 
 // ---------------------------------------------------------------------------------------------
+// block pooling arithmetic (compress.cu, and the fused decode step's pooling of a closed block):
+// 16-byte streaming loads of bf16 rows, fp32 weighted sums, bf16 round-to-nearest-even
+// ---------------------------------------------------------------------------------------------
+// 16 bytes read once (not kept in L1)
+CSA_DEV uint4 ldg_stream(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// acc[i] += w * row[i] for the 8 bf16 values of v
+CSA_DEV void acc8(float (&acc)[8], uint4 v, float w) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    acc[2 * q] = fmaf(w, __uint_as_float(u[q] << 16), acc[2 * q]);
+    acc[2 * q + 1] = fmaf(w, __uint_as_float(u[q] & 0xFFFF0000u), acc[2 * q + 1]);
+  }
+}
+
+// 8 sums times inv, rounded to bf16
+CSA_DEV uint4 pack8(const float (&acc)[8], float inv) {
+  uint4 o;
+  o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+  o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  return o;
+}
+
+// ---------------------------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------------------------
 CSA_DEV void mbar_init(uint64_t* bar, uint32_t count) {

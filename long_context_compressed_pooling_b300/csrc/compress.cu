@@ -15,32 +15,6 @@
 namespace csa {
 namespace {
 
-CSA_DEV uint4 ldg_stream(const uint16_t* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-CSA_DEV void acc8(float (&acc)[8], uint4 v, float w) {
-  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    acc[2 * q] = fmaf(w, __uint_as_float(u[q] << 16), acc[2 * q]);
-    acc[2 * q + 1] = fmaf(w, __uint_as_float(u[q] & 0xFFFF0000u), acc[2 * q + 1]);
-  }
-}
-
-CSA_DEV uint4 pack8(const float (&acc)[8], float inv) {
-  uint4 o;
-  o.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  o.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-  o.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-  o.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-  return o;
-}
-
 // grid-stride over (b, entry, 16-byte chunk); CH = d / 8 chunks per row.
 template <int CH>
 __global__ void __launch_bounds__(256) compress_kernel(const uint16_t* __restrict__ k_raw,

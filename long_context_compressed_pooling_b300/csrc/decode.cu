@@ -117,14 +117,18 @@ struct DecParams {
   // attention (attend != 0)
   int attend, H, W, P;       // P: keys per CTA run
   const uint16_t* q;         // [B, H, 128]
-  const uint16_t* k_cmp;
-  const uint16_t* v_cmp;     // [B, E, 128]
+  uint16_t* k_cmp;           // written only for the pooled entries
+  uint16_t* v_cmp;           // [B, E, 128]
   const uint16_t* k_raw;
   const uint16_t* v_raw;     // [B, N, 128]
   uint16_t* out;             // [B, H, 128]
   float* lse;                // optional [B, H]
   int64_t N;
   int64_t fresh_from;        // entry-cache rows at or above it may be the predecessor's output
+  // entries [pool_j0, pool_j1) of every sequence are pooled here from k_raw / v_raw / logits
+  // (the blocks the step's tokens close), with csa_compress's arithmetic
+  const float* logits;       // [B, N]
+  int64_t pool_j0, pool_j1;
   uint32_t* status;
   long long wait_budget;
   uint32_t fault_mask;
@@ -140,6 +144,35 @@ CSA_DEV void work_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }  // 
 // the MMA warp and the work warps (the loaders never join the set-up)
 CSA_DEV void setup_sync() {
   asm volatile("bar.sync 2, %0;" ::"n"(32 * (kWarps - kMmaWarp)) : "memory");
+}
+
+// Pools entries [p.pool_j0, p.pool_j1) of sequence b into k_cmp / v_cmp with the arithmetic of
+// csa_compress (the same operations in the same order, so the entries are bit-identical):
+// p_i = expf(w_i - max w) / sum, fp32 weighted sums, bf16 round-to-nearest-even. One warp; each
+// half-warp an entry, each lane 8 of its 128 channels.
+CSA_DEV void pool_entries(const DecParams& p, int64_t b, int lane) {
+  const int64_t n = p.pool_j1 - p.pool_j0;
+  const int c = lane & 15;
+  for (int64_t e = lane >> 4; e < n; e += 2) {
+    const int64_t j = p.pool_j0 + e;
+    const int64_t tok0 = b * p.N + j * p.m;
+    const float* wl = p.logits + tok0;
+    float mx = -INFINITY;
+    for (int i = 0; i < p.m; ++i) mx = fmaxf(mx, __ldg(wl + i));
+    float acc_k[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float acc_v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float sum = 0.f;
+    for (int i = 0; i < p.m; ++i) {
+      const float pw = expf(__ldg(wl + i) - mx);
+      sum += pw;
+      acc8(acc_k, ldg_stream(p.k_raw + (tok0 + i) * kD + c * 8), pw);
+      acc8(acc_v, ldg_stream(p.v_raw + (tok0 + i) * kD + c * 8), pw);
+    }
+    const float inv = 1.0f / sum;
+    const int64_t o = (b * p.E + j) * kD + c * 8;
+    *reinterpret_cast<uint4*>(p.k_cmp + o) = pack8(acc_k, inv);
+    *reinterpret_cast<uint4*>(p.v_cmp + o) = pack8(acc_v, inv);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) csa_decode_kernel(const DecParams p) {
@@ -324,6 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1) csa_decode_kernel(const DecParams
     setup_sync();
     tc_fence_after();
   }
+
+  // The blocks this step closes: pooled by one warp of the cluster's last CTA, before its
+  // epilogue work; the attention reads them only after the cluster barriers below.
+  if (p.pool_j1 > p.pool_j0 && rank == C - 1 && warp == kWarps - 1) pool_entries(p, b, lane);
 
   // ======================= phase 1: indexer scores into shared memory =======================
   if (ntiles > 0 && warp == kMmaWarp) {
@@ -991,6 +1028,9 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, uint32_t* s
   p.lse = a.lse;
   p.N = a.N;
   p.fresh_from = a.fresh_from;
+  p.logits = a.logits;
+  p.pool_j0 = a.pool_j0;
+  p.pool_j1 = a.pool_j1;
   p.status = status;
   const FaultConfig fc = fault_config();
   p.wait_budget = fc.wait_budget;

@@ -191,8 +191,8 @@ struct DecodeArgs {
   bool attend;               // also the sparse attention (d = 128, H <= 64)
   int H, W;
   const uint16_t* q;         // [B, H, 128]
-  const uint16_t* k_cmp;
-  const uint16_t* v_cmp;     // [B, E, 128]
+  uint16_t* k_cmp;           // written only for the pooled entries (below)
+  uint16_t* v_cmp;           // [B, E, 128]
   const uint16_t* k_raw;
   const uint16_t* v_raw;     // [B, N, 128]
   uint16_t* out;             // [B, H, 128]
@@ -201,7 +201,12 @@ struct DecodeArgs {
   // entry-cache rows at or above it may still be written by the kernel before this one (they
   // are read only after the grid-dependency wait); 0: any row may be
   int64_t fresh_from;
+  // entries [pool_j0, pool_j1) pooled inside the launch (at most kDecodePoolMax per sequence;
+  // pool_j1 == pool_j0: none), with csa_compress's arithmetic; k_cmp / v_cmp are written there
+  const float* logits;
+  int64_t pool_j0, pool_j1;
 };
+constexpr int kDecodePoolMax = 4;
 // ok = false when the shape is outside the kernel's limits (E % 8 != 0, k > 2048, more than
 // 16 x 16384 visible entries, more than 16 x 256 attention keys).
 DecodePlan plan_decode(int B, int64_t E, int64_t n_vis, int k, int W, bool attend,
