@@ -752,7 +752,6 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
       // kernel waits for it before reading anything.
       a.wait_first = pool_inside || E <= j0;
       a.keys_fresh_from = c->xi_raw ? j0 : E;
-      a.fresh_from = E > j0 ? j0 : E;
       a.attend = true;
       a.H = c->H;
       a.W = c->W;

@@ -124,7 +124,6 @@ struct DecParams {
   uint16_t* out;             // [B, H, 128]
   float* lse;                // optional [B, H]
   int64_t N;
-  int64_t fresh_from;        // entry-cache rows at or above it may be the predecessor's output
   // entries [pool_j0, pool_j1) of every sequence are pooled here from k_raw / v_raw / logits
   // (the blocks the step's tokens close), with csa_compress's arithmetic
   const float* logits;       // [B, N]
@@ -310,16 +309,6 @@ __global__ void __launch_bounds__(kThreads, 1) csa_decode_kernel(const DecParams
                     in ? 16u : 0u);
       }
       cp_async_commit();
-    }
-    // The window rows of this CTA's attention run are known now: bring them into L2 while the
-    // indexer runs (the run is positions [rank P, (rank + 1) P) of selected entries, then window)
-    if (p.attend) {
-      const int p0 = min(n_keys, (int)rank * p.P), p1 = min(n_keys, p0 + p.P);
-      for (int pp = max(p0, cnt) + (tid - kLoadThreads); pp < p1; pp += kThreads - kLoadThreads) {
-        const int64_t row = (b * p.N + w0 + (pp - cnt)) * kD;
-        prefetch_l2(p.k_raw + row, kD * 2);
-        prefetch_l2(p.v_raw + row, kD * 2);
-      }
     }
     // B operand of the indexer: row r = head r / 4, block r % 2, halves swapped when
     // (r / 2) % 2; every row holds one 16-byte block of the head and zeros, stored through the
@@ -524,17 +513,6 @@ __global__ void __launch_bounds__(kThreads, 1) csa_decode_kernel(const DecParams
             m_in |= bit;
             atomicAdd(&sub[kk & 63u], 1u);
           }
-        }
-      }
-    }
-    // every score in a bin above bstar is selected: its entry rows go to L2 now, ahead of the
-    // attention's gather (the entry cache rows below fresh_from are inputs of this call)
-    if (p.attend) {
-      for (uint64_t m = m_hi; m != 0; m &= m - 1) {
-        const int64_t j = lo + s0 + (__ffsll((long long)m) - 1);
-        if (j < p.fresh_from) {
-          prefetch_l2(p.k_cmp + (b * p.E + j) * kD, kD * 2);
-          prefetch_l2(p.v_cmp + (b * p.E + j) * kD, kD * 2);
         }
       }
     }
@@ -1027,7 +1005,6 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, uint32_t* s
   p.out = a.out;
   p.lse = a.lse;
   p.N = a.N;
-  p.fresh_from = a.fresh_from;
   p.logits = a.logits;
   p.pool_j0 = a.pool_j0;
   p.pool_j1 = a.pool_j1;

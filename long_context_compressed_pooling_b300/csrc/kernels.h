@@ -198,9 +198,6 @@ struct DecodeArgs {
   uint16_t* out;             // [B, H, 128]
   float* lse;                // optional [B, H]
   int64_t N;
-  // entry-cache rows at or above it may still be written by the kernel before this one (they
-  // are read only after the grid-dependency wait); 0: any row may be
-  int64_t fresh_from;
   // entries [pool_j0, pool_j1) pooled inside the launch (at most kDecodePoolMax per sequence;
   // pool_j1 == pool_j0: none), with csa_compress's arithmetic; k_cmp / v_cmp are written there
   const float* logits;
