@@ -230,6 +230,30 @@ csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const 
                        const uint8_t* ki_scales, int B, int Nq, int64_t q_pos0, int64_t E, int m,
                        int H_I, int d_I, uint16_t* sc, float* scores_f32, cudaStream_t st,
                        const PagedLayout* paged, Freshness fr) {
+  if (E > 0 && !paged && !scores_f32 && decode_indexer_fits(Nq, H_I, d_I)) {
+    // one query per sequence: the decode kernel's indexer spread over the whole GPU
+    const int64_t nv = std::max<int64_t>(0, std::min<int64_t>(E, (q_pos0 + 1) / m));
+    int split = 0, chunk = 0;
+    if (plan_decode_scores(B, E, nv, &split, &chunk)) {
+      uint32_t* status = status_word();
+      if (!status) return CSA_ERR_CUDA;
+      DecodeArgs a{};
+      a.qi_codes = qi_codes;
+      a.qi_scales = qi_scales;
+      a.ki_codes = ki_codes;
+      a.ki_scales = ki_scales;
+      a.scores = sc;
+      a.E = E;
+      a.t = q_pos0;
+      a.m = m;
+      a.k = 1;
+      a.H_I = H_I;
+      a.B = B;
+      a.keys_fresh_from = fr.keys_from;
+      a.wait_first = fr.queries;
+      return from_cuda(launch_decode_scores(a, split, chunk, status, st));
+    }
+  }
   if (E > 0) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return CSA_ERR_CUDA;

@@ -114,6 +114,7 @@ struct DecParams {
   int m, k, H_I, n_vis, chunk;
   int64_t keys_fresh_from;   // key tiles with an entry at or above it: copied after the wait
   int wait_first;            // grid-dependency wait before reading any input
+  int split;                 // > 0: scores only, `split` CTAs per sequence without a cluster
   // attention (attend != 0)
   int attend, H, W, P;       // P: keys per CTA run
   const uint16_t* q;         // [B, H, 128]
@@ -210,8 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1) csa_decode_kernel(const DecParams
   uint16_t* pin = keys + 2048;                                   // [16][hp][128] bf16
   float2* pinml = reinterpret_cast<float2*>(keys + 2048 + kMergeBf16);  // [16][hp]
 
-  const uint32_t C = cluster_nctarank();
-  const uint32_t rank = cluster_ctarank();
+  // scores only (split > 0): no cluster, CTA blockIdx.x % split of its sequence
+  const bool score_only = p.split > 0;
+  const uint32_t C = score_only ? (uint32_t)p.split : cluster_nctarank();
+  const uint32_t rank = score_only ? blockIdx.x % (uint32_t)p.split : cluster_ctarank();
   const int64_t b = blockIdx.x / C;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
   const long long budget = p.wait_budget;
@@ -253,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) csa_decode_kernel(const DecParams
   __syncthreads();  // barriers initialised, misc words and histograms cleared
   // The other CTAs add into gall / store into subs, cab and inbox once they pass the matching
   // wait below: this arrive orders the clearing before it.
-  cluster_arrive();
+  if (!score_only) cluster_arrive();
 
   bool ok = true;  // this thread's waits all succeeded (a timeout stops the phases after it)
   float qsc[8];  // query scale of (head, block), 2^(e - 127) (work warps; loaded during set-up)
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) csa_decode_kernel(const DecParams
         sc += 0.0f;  // -0 -> +0
         const uint16_t bits = f32_to_bf16_bits(sc);
         keys[jl] = bits;
-        if (!select_all) atomicAdd(&hist[bits >> 6], 1u);  // bins of 64 BF16 steps
+        if (!select_all && !score_only) atomicAdd(&hist[bits >> 6], 1u);  // 64-step bins
         if (p.scores) p.scores[b * p.E + lo + jl] = bits;
       }
       tc_fence_before();
@@ -448,6 +451,11 @@ __global__ void __launch_bounds__(kThreads, 1) csa_decode_kernel(const DecParams
   // A timeout anywhere in the cluster must not leave the other CTAs waiting at a cluster
   // barrier: every CTA still passes every barrier below, skipping the work.
   const bool aborted = misc[kMiscAbort] != 0u;
+  if (score_only) {  // the scores are written: release tensor memory and leave
+    pdl_wait();      // completion stays ordered after the predecessor's
+    if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+    return;
+  }
 
   // ======================= phase 2: top-k through the cluster =======================
   // The threshold T (the k-th largest score) in two cluster rounds, every exchange a store or
@@ -907,7 +915,7 @@ int g_max_active[kMaxDevicesDecode][kDecodeMaxCluster + 1];
 
 // Plans the fused step: the cluster size C (each sequence's entries split over C CTAs) that
 // minimises the estimated time over the waves of co-resident clusters, within the kernel's
-// limits (at most kDecodeMaxChunk entries per CTA, kDecodeMaxKeys attention keys per CTA).
+// limits (at most kDecodeFusedChunk entries per CTA, kDecodeMaxKeys attention keys per CTA).
 DecodePlan plan_decode(int B, int64_t E, int64_t n_vis, int k, int W, bool attend,
                        bool want_scores) {
   DecodePlan best{};
@@ -926,8 +934,10 @@ DecodePlan plan_decode(int B, int64_t E, int64_t n_vis, int k, int W, bool atten
   for (int C = kDecodeMaxCluster; C >= 1; --C) {
     const int64_t chunk = (tiles + C - 1) / C * kTileM;
     // Longer chunks stream more key bytes through one SM than the separate indexer spreads
-    // over the whole GPU: measured slower there (a 1M-context row: 16 CTAs of 16384 entries).
-    if (chunk > kDecodeMaxChunk || (attend && chunk > kDecodeFusedChunk)) continue;
+    // over the whole GPU: measured slower there, with and without the attention (4 rows of
+    // 262144 entries in 16-CTA clusters: 39 us for scores and selection against 27 + 17 us for
+    // the separate indexer and top-k, whose step overlaps better with a concurrent layer).
+    if (chunk > kDecodeFusedChunk) continue;
     const int64_t P = (cnt + nw + C - 1) / C;
     if (attend && P > kDecodeMaxKeys) continue;
     int act = g_max_active[dev][C];
@@ -972,9 +982,8 @@ DecodePlan plan_decode(int B, int64_t E, int64_t n_vis, int k, int W, bool atten
   return best;
 }
 
-cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, uint32_t* status,
-                          cudaStream_t stream) {
-  if (!pl.ok) return cudaErrorInvalidValue;
+namespace {
+DecParams decode_params(const DecodeArgs& a, const DecodePlan& pl, uint32_t* status) {
   DecParams p;
   p.qi_codes = a.qi_codes;
   p.qi_scales = a.qi_scales;
@@ -1012,6 +1021,15 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, uint32_t* s
   const FaultConfig fc = fault_config();
   p.wait_budget = fc.wait_budget;
   p.fault_mask = fc.skip_mask;
+  p.split = 0;
+  return p;
+}
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, uint32_t* status,
+                          cudaStream_t stream) {
+  if (!pl.ok) return cudaErrorInvalidValue;
+  const DecParams p = decode_params(a, pl, status);
   auto kern = csa_decode_kernel;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
@@ -1023,6 +1041,43 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, uint32_t* s
   ProfScope prof(stream, a.attend ? "csa_decode" : "indexer_topk");
   return launch_ex(kern, dim3((unsigned)(a.B * pl.C)), dim3(kThreads), kSmemBytes, stream,
                    (unsigned)pl.C, p);
+}
+
+// Scores only: every sequence's visible entries split evenly over `split` CTAs (one wave of one
+// CTA per SM where the batch allows), each at most kDecodeMaxChunk entries.
+bool plan_decode_scores(int B, int64_t E, int64_t n_vis, int* split, int* chunk) {
+  if (B < 1 || n_vis < 1 || E % 8 != 0) return false;
+  const int64_t tiles = (n_vis + kTileM - 1) / kTileM;
+  int64_t sp = std::max<int64_t>(1, kNumSMs / B);
+  sp = std::min<int64_t>(sp, tiles);
+  const int64_t ch = (tiles + sp - 1) / sp * kTileM;
+  if (ch > kDecodeMaxChunk) return false;
+  *split = (int)sp;
+  *chunk = (int)ch;
+  return true;
+}
+
+cudaError_t launch_decode_scores(const DecodeArgs& a, int split, int chunk, uint32_t* status,
+                                 cudaStream_t stream) {
+  if (split < 1 || chunk < 1 || chunk > kDecodeMaxChunk || a.scores == nullptr)
+    return cudaErrorInvalidValue;
+  DecodePlan pl{};
+  pl.ok = true;
+  pl.C = 1;
+  pl.chunk = chunk;
+  pl.P = 0;
+  DecodeArgs b = a;
+  b.attend = false;
+  b.pool_j0 = b.pool_j1 = 0;
+  DecParams p = decode_params(b, pl, status);
+  p.split = split;
+  auto kern = csa_decode_kernel;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  ProfScope prof(stream, "indexer_mxf4");
+  return launch_ex(kern, dim3((unsigned)(a.B * split)), dim3(kThreads), kSmemBytes, stream, 1u,
+                   p);
 }
 
 }  // namespace csa

@@ -170,7 +170,7 @@ constexpr int kDecodeMaxCluster = 16;   // CTAs per sequence
 constexpr int kDecodeMaxChunk = 16384;  // entries one CTA scores (BF16 scores kept on chip)
 constexpr int kDecodeMaxKeys = 256;     // attention keys one CTA gathers
 constexpr int kDecodeMaxSel = 2048;     // largest k
-constexpr int kDecodeFusedChunk = 8192; // the layer pair fuses the attention up to this chunk
+constexpr int kDecodeFusedChunk = 8192; // the planner takes the one-launch kernel up to this chunk
 constexpr int kMaxDevicesDecode = 64;
 struct DecodePlan {
   bool ok;
@@ -210,5 +210,12 @@ DecodePlan plan_decode(int B, int64_t E, int64_t n_vis, int k, int W, bool atten
                        bool want_scores);
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& pl, uint32_t* status,
                           cudaStream_t stream);
+// The decode kernel's indexer alone (no cluster, no selection) for rows too long for the
+// one-launch step: BF16 scores of the visible entries into a.scores, each sequence split over
+// `split` CTAs of `chunk` entries (plan_decode_scores: false when a CTA's share would exceed
+// kDecodeMaxChunk, or E % 8 != 0).
+bool plan_decode_scores(int B, int64_t E, int64_t n_vis, int* split, int* chunk);
+cudaError_t launch_decode_scores(const DecodeArgs& a, int split, int chunk, uint32_t* status,
+                                 cudaStream_t stream);
 
 }  // namespace csa

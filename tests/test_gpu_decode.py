@@ -104,7 +104,9 @@ def test_decode_step_matches_oracle(B, N, m, k, W, H, skew):
 
 @pytest.mark.parametrize("B,N,k,skew", [(4, 1048576, 2048, None), (5, 160000, 300, "far")])
 def test_decode_index_topk_matches_oracle(B, N, k, skew):
-    """csa_index_topk with one query per sequence: the same kernel without the attention."""
+    """csa_index_topk with one query per sequence: the one-launch kernel without the attention
+    where each CTA's share of a row fits it (160000 tokens), the separate indexer and top-k
+    kernels beyond (1M tokens, 4 rows); both bit-exact."""
     m = 4
     E = N // m
     s = LayerShape("csa", B=B, N=N, Nq=1, q_pos0=N - 1, H=64, d=128, m=m, W=128, k=k, H_I=4,
