@@ -10,7 +10,9 @@ window 128); --config picks another one of the five synthetic workloads.
 Prints one JSON line (rank 0) for the --config workload; with --configs all (the default) it
 also carries a "configs" object with the same measurements for each of the five workloads.
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the launch
-stream, with a 256 MB write between steps to flush the 126 MB L2 (outside the events);
+stream, with the 126 MB L2 flushed between steps outside the events: a 256 MB write, then (by
+default, --flush write+read) a read of the same 256 MB, so that the flush's own dirty lines are
+written back before the step instead of competing with its reads;
 barrier + synchronize around the timed loop; max over ranks. `--impl reference` times the fp64
 CPU oracle on a bounded sample of the same workload instead, in a process pool over the host
 cores (as does the cpu_baseline leg).
@@ -69,6 +71,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of a CUDA graph")
+    ap.add_argument("--flush", default="write+read", choices=["write+read", "write"],
+                    help="L2 flush between timed steps: a 256 MB write, then a read of it "
+                         "(default), or the write alone (its dirty lines are then written back "
+                         "during the next step)")
     ap.add_argument("--paged", action="store_true",
                     help="decode workloads through the paged KV cache (csa_paged_decode_step: "
                          "append the step's token to the state cache, pool the block it closes "
@@ -554,7 +560,7 @@ def run_workload(args, name, rank, world, dev, local):
             print(f"# CUDA graph capture unavailable, launching eagerly: {e}", file=sys.stderr)
     step = graph.replay if graph is not None else call
 
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, args.flush)
     K = args.steps
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -563,7 +569,7 @@ def run_workload(args, name, rank, world, dev, local):
         barrier()
         torch.cuda.synchronize()
         for i in range(K):
-            flush.zero_()
+            flush()
             ev0[i].record()
             fn()
             ev1[i].record()
@@ -595,7 +601,7 @@ def run_workload(args, name, rank, world, dev, local):
            "data": "synthetic (seeded; random inputs of the workload's shapes and distributions)",
            "config": {"workload": wl.name, "description": wl.description,
                       "batch_per_gpu": wl.layers[0].B, "context": wl.layers[0].N,
-                      "l2": "flushed between timed steps (256 MB write outside the events)",
+                      "l2": flush.describe(),
                       "launch": "cuda_graph" if graph is not None else "eager",
                       "parallelism": f"replicas x{world} (independent sequences per GPU)",
                       "index_keys": ("pooled in the step from bf16 index-key rows"
@@ -631,6 +637,32 @@ def run_workload(args, name, rank, world, dev, local):
     return out
 
 
+class L2Flush:
+    """Evicts the 126 MB L2 between timed steps (outside the events): a 256 MB write, so none of
+    the step's inputs stays cached, then in mode "write+read" a read of the same 256 MB, which
+    writes the write's dirty lines back to HBM before the step starts; with the write alone that
+    write-back (up to 126 MB) happens during the step, competing with its reads."""
+
+    def __init__(self, dev, mode="write+read"):
+        import torch
+        self.buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.words = self.buf.view(torch.int64)
+        self.sink = torch.empty((), dtype=torch.int64, device=dev)
+        self.mode = mode
+
+    def __call__(self):
+        import torch
+        self.buf.zero_()
+        if self.mode == "write+read":
+            torch.sum(self.words, dim=0, out=self.sink)
+
+    def describe(self):
+        if self.mode == "write+read":
+            return ("flushed between timed steps outside the events: 256 MB written, then read "
+                    "back (the flush's dirty lines reach HBM before the step)")
+        return "flushed between timed steps (256 MB write outside the events)"
+
+
 def run_topk_compare(s, d, flush, K, dev):
     """The selector on BF16 scores (the path) against the same selection on the FP32 scores the
     BF16 ones are rounded from (9fzt.com item 4 reports the BF16 selector 2x faster and 99.7 %
@@ -651,7 +683,7 @@ def run_topk_compare(s, d, flush, K, dev):
         e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
         torch.cuda.synchronize()
         for i in range(K):
-            flush.zero_()
+            flush()
             e0[i].record()
             fn()
             e1[i].record()
@@ -735,7 +767,7 @@ def run_e2e(wl, states, call, flush, K, dev, world, barrier, index_keys=False):
     barrier()
     torch.cuda.synchronize()
     for i in range(K):
-        flush.zero_()
+        flush()
         e0[i].record()
         run()
         e1[i].record()

@@ -55,6 +55,7 @@ constexpr int kLoadWarps = 8;
 constexpr int kLoadThreads = 32 * kLoadWarps;
 constexpr int kMmaWarp = 16;
 constexpr int kThreads = 544;
+constexpr int kSetupThreads = 32 * (kSoftmaxWarps + 1);  // softmax warps + MMA warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;    // O accumulators: key half 0 at [256, 384), half 1 at [384, 512)
 constexpr int kQBytes = kM * kD * 2;        // 16 KB
@@ -148,24 +149,31 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
     mbar_init(pv_done, 1);
     fence_mbar_init();
   }
-  // Q tile of heads [h_base, h_base + 64) (zero rows past H); Q is an input of this call.
-  for (int x = threadIdx.x; x < kM * 16; x += kThreads) {
-    const int r = x >> 4, c = x & 15;
-    const bool ok = h_base + r < p.H;
-    cp_async_16(Qs + sw128(r, c, kM), ok ? p.q + (tok * p.H + h_base + r) * kD + c * 8 : p.q,
-                ok ? 16u : 0u);
+  __syncthreads();  // barriers initialised: the loaders start their copies at once
+  const bool loader = warp >= kLoadWarp0 && warp < kMmaWarp;
+  uint32_t tmem = 0;
+  if (!loader) {
+    // Q tile of heads [h_base, h_base + 64) (zero rows past H; Q is an input of this call) and
+    // the tensor memory, by the softmax and MMA warps while the loaders' first copies fly
+    const int nt = warp == kMmaWarp ? kSoftmaxWarps * 32 + lane : (int)threadIdx.x;
+    for (int x = nt; x < kM * 16; x += kSetupThreads) {
+      const int r = x >> 4, c = x & 15;
+      const bool ok = h_base + r < p.H;
+      cp_async_16(Qs + sw128(r, c, kM), ok ? p.q + (tok * p.H + h_base + r) * kD + c * 8 : p.q,
+                  ok ? 16u : 0u);
+    }
+    cp_async_commit();
+    if (warp == kMmaWarp) {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(kSetupThreads) : "memory");
+    tc_fence_after();
+    tmem = *tmem_slot;
   }
-  cp_async_commit();
-  if (warp == kMmaWarp) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
-  cp_async_wait<0>();
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
   // Top-k lists come from the preceding kernels; a dense launch defers the wait until its
   // loaders reach an entry at or above fresh_from (raw window rows and Q are inputs).
   const bool early = !p.sparse && p.fresh_from > 0;
