@@ -64,7 +64,8 @@ CSA_DEV void select_bin(const uint32_t* hist, uint32_t need, int* out_bin, uint3
 }
 
 // Finds the first bin b (ascending) with prefix(b-1) < need <= prefix(b) over bins [0, 255);
-// writes b and prefix(b-1), or bin -1 when the 255 bins hold fewer than `need`. Warp 0 only.
+// writes b and prefix(b-1), or bin -1 and the total of the 255 bins when they hold fewer than
+// `need`. Warp 0 only.
 CSA_DEV void select_prefix(const uint32_t* hist, uint32_t need, int* out_bin, uint32_t* out_before) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -83,7 +84,10 @@ CSA_DEV void select_prefix(const uint32_t* hist, uint32_t need, int* out_bin, ui
       if (lane >= o) inc += v;
     }
     const uint32_t exc = inc - tot;
-    if (lane == 31 && inc < need) *out_bin = -1;
+    if (lane == 31 && inc < need) {
+      *out_bin = -1;
+      *out_before = inc;
+    }
     if (exc < need && need <= inc) {
       uint32_t run = exc;
 #pragma unroll

@@ -375,26 +375,51 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
     Tc = max_c - (uint32_t)sh_bin;
     above_c = sh_above;
   } else {
-    // fallback: exact two-digit radix select of the coarse parts on the registers (hist2, then
-    // hist1 again: every CTA of the cluster has read hist1 before it arrives at the digit-1
-    // cluster barrier)
+    bool found = false;
+    // the histogram arrays of the radix fallback's two digits, alternating with the last one
+    // used: every CTA of a cluster has read that one before it arrives at the next barrier
+    uint32_t* const hd1 = F32 ? hist2 : hist1;
+    uint32_t* const hd2 = F32 ? hist1 : hist2;
+    if constexpr (!F32) {
+      // second window: the keys 255 .. 509 BF16 steps below the maximum (where the k-th key of a
+      // long row usually lies when it is not in the first window)
+      const uint32_t in0 = sh_above;  // keys in the first window (fewer than k)
 #pragma unroll
-    for (int j = 0; j < KPT; ++j)
-      if (seg0 + j < n) atomicAdd(&wh[(key[j] >> CS) >> 8], 1u);
-    __syncthreads();
-    sum_hist(hist2);
-    select_bin(gsum, (uint32_t)k, &sh_bin, &sh_above);
-    __syncthreads();
-    const uint32_t hi_byte = (uint32_t)sh_bin, above_hi = sh_above;
+      for (int j = 0; j < KPT; ++j) {
+        const uint32_t dd = max_c - key[j];
+        if (dd - 255u < 255u && seg0 + j < n) atomicAdd(&wh[dd - 255u], 1u);
+      }
+      __syncthreads();
+      sum_hist(hist2);
+      select_prefix(gsum, (uint32_t)k - in0, &sh_bin, &sh_above);
+      __syncthreads();
+      if (sh_bin >= 0) {
+        Tc = max_c - 255u - (uint32_t)sh_bin;
+        above_c = in0 + sh_above;
+        found = true;
+      }
+    }
+    if (!found) {
+      // fallback: exact two-digit radix select of the coarse parts on the registers
 #pragma unroll
-    for (int j = 0; j < KPT; ++j)
-      if (seg0 + j < n && (key[j] >> CS >> 8) == hi_byte) atomicAdd(&wh[(key[j] >> CS) & 0xFFu], 1u);
-    __syncthreads();
-    sum_hist(hist1);
-    select_bin(gsum, (uint32_t)k - above_hi, &sh_bin, &sh_above);
-    __syncthreads();
-    Tc = (hi_byte << 8) | (uint32_t)sh_bin;
-    above_c = above_hi + sh_above;
+      for (int j = 0; j < KPT; ++j)
+        if (seg0 + j < n) atomicAdd(&wh[(key[j] >> CS) >> 8], 1u);
+      __syncthreads();
+      sum_hist(hd1);
+      select_bin(gsum, (uint32_t)k, &sh_bin, &sh_above);
+      __syncthreads();
+      const uint32_t hi_byte = (uint32_t)sh_bin, above_hi = sh_above;
+#pragma unroll
+      for (int j = 0; j < KPT; ++j)
+        if (seg0 + j < n && (key[j] >> CS >> 8) == hi_byte)
+          atomicAdd(&wh[(key[j] >> CS) & 0xFFu], 1u);
+      __syncthreads();
+      sum_hist(hd2);
+      select_bin(gsum, (uint32_t)k - above_hi, &sh_bin, &sh_above);
+      __syncthreads();
+      Tc = (hi_byte << 8) | (uint32_t)sh_bin;
+      above_c = above_hi + sh_above;
+    }
   }
   uint32_t T, need_eq;
   if constexpr (F32) {

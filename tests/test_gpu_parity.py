@@ -132,6 +132,32 @@ def test_topk_ties_and_negative_scores(E, Nq, q_pos0, m, k):
             assert cnt[b, i] == rcnt and np.array_equal(idx[b, i], ridx), (b, i)
 
 
+@pytest.mark.parametrize("kind", ["spread", "sampled_high", "few_values"])
+def test_topk_many_rows_sampled_threshold(kind):
+    """Rows of one CTA each (>= 148 rows of 16000-32768 keys): the selector's sampled threshold
+    (every thread's first key is a sample) with ordinary scores, with the largest scores placed
+    exactly on the sampled positions (the count above the sampled threshold falls short of k and
+    the general path runs), and with only five distinct values (huge tie groups)."""
+    rng = np.random.default_rng({"spread": 1, "sampled_high": 2, "few_values": 3}[kind])
+    B, Nq, E, m, k = 1, 150, 32768, 4, 2048
+    q_pos0 = E * m - Nq  # the rows see 32731 .. 32768 entries
+    if kind == "spread":
+        vals = rng.gamma(4.0, 2.0, size=(B, Nq, E)).astype(np.float32)
+    elif kind == "sampled_high":
+        vals = rng.uniform(0.0, 1.0, size=(B, Nq, E)).astype(np.float32)
+        vals[:, :, ::32] += 100.0  # the positions one thread's first key comes from
+    else:
+        vals = rng.choice(np.array([0.0, 0.5, 1.0, 2.0, 3.0], np.float32), size=(B, Nq, E))
+    sc_np = O.f64_to_bf16_rne(vals.astype(np.float64))
+    sc = torch.from_numpy(sc_np.view(np.int16)).to(DEV).view(torch.bfloat16)
+    idx, cnt = csa.topk(sc, q_pos0, m, k)
+    idx, cnt = npy(idx), npy(cnt)
+    for i in range(Nq):
+        nv = O.visible_entries(q_pos0 + i, m, E)
+        ridx, rcnt = O.topk_select(sc_np[0, i], nv, k)
+        assert cnt[0, i] == rcnt and np.array_equal(idx[0, i], ridx), i
+
+
 # ---------------------------------------------------------------------------------------------
 # attention
 # ---------------------------------------------------------------------------------------------
