@@ -554,6 +554,7 @@ cudaError_t launch_attend(const AttendArgs& a, int64_t max_keys, void* ws, uint3
   if (tokens == 0) return cudaSuccess;
   if (a.d != 128 && a.d != 64) return cudaErrorInvalidValue;
   if (a.paged && a.d != 128) return cudaErrorInvalidValue;  // paged reads: tcgen05 kernel only
+  if (a.d == 64 && a.Nq > 1) return launch_attend_pk(a, status, stream);  // prefill
   const SplitPlan sp = plan_splits(tokens, a.H, max_keys, a.d);
   float* ws_o = reinterpret_cast<float*>(ws);
   float* ws_ml = ws_o + (size_t)sp.n_splits * tokens * a.H * a.d;

@@ -140,9 +140,11 @@ struct AttendArgs {
 };
 int plan_attend_splits(int tokens, int H, int d, int64_t max_keys);
 size_t attend_workspace_bytes(int tokens, int H, int d, int64_t max_keys);
-// d = 128 runs the tcgen05 kernel (attend_tc.cu), d = 64 the mma.sync kernel (attend.cu).
+// d = 128 runs the tcgen05 kernel (attend_tc.cu); d = 64 the tcgen05 kernel with several query
+// tokens per CTA (attend_pk.cu) for prefill, the split-K mma.sync kernel (attend.cu) for decode.
 cudaError_t launch_attend(const AttendArgs& a, int64_t max_keys, void* ws, uint32_t* status,
                           cudaStream_t stream);
+cudaError_t launch_attend_pk(const AttendArgs& a, uint32_t* status, cudaStream_t stream);
 int attend_tc_chunk_keys();
 // n_splits CTAs per (token, 64-head group); cluster = 1 merges the splits through distributed
 // shared memory (returns cudaErrorNotSupported if such a cluster cannot be scheduled), else the

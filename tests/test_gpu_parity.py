@@ -171,6 +171,10 @@ ATT_CASES = [
     (16, 1, 4095, 4096, 64, 128, 4, 128, 512),  # decode batch 16: 10-CTA cluster merge
     (1, 1, 32767, 32768, 64, 128, 4, 128, 8192),  # 65 splits: two merge batches per warp
     (1, 1, 32767, 32768, 16, 64, 4, 64, 4096),    # d = 64, workspace merge
+    # d = 64 prefill: several query tokens per CTA (64 / Hp of them)
+    (2, 37, 900, 1000, 4, 64, 4, 32, 20),    # 16 tokens per CTA, last group partial, 2 sequences
+    (1, 9, 2000, 2048, 12, 64, 4, 16, 50),   # 12 heads padded to 16: 4 tokens per CTA
+    (1, 2, 4000, 4096, 128, 64, 4, 128, 40),  # two 64-head groups, one token per CTA
 ]
 
 
@@ -219,6 +223,8 @@ HCA_CASES = [
     (2, 1, 131071, 131072, 64, 128, 128, 128),  # 9 splits per token: cluster merge
     (1, 1, 262143, 262144, 64, 128, 128, 128),  # 17 splits: workspace merge
     (1, 160, 3840, 4000, 64, 128, 4, 128),   # dense prefill rows: ~9 key chunks per CTA
+    (2, 21, 4000, 4200, 4, 64, 128, 128),    # d = 64, 16 tokens per CTA, 2 sequences
+    (1, 70, 9000, 9100, 16, 64, 4, 100),     # d = 64, 4 tokens per CTA, ~19 key chunks
 ]
 
 
@@ -280,6 +286,25 @@ def test_empty_key_set_gives_zero_and_neg_inf():
     csa.compress(x["k_raw"], x["v_raw"], x["logits"], m, kc, vc)
     out, lse = csa.hca_attend(x["q"], kc, vc, m, x["k_raw"], x["v_raw"], 0, 0, want_lse=True)
     assert torch.all(out.float() == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_bad_topk_index_is_flagged_and_skipped_packed_d64():
+    # d = 64 prefill (8 tokens per CTA): a bad index of one token is flagged and left out of that
+    # token's softmax only
+    B, Nq, q_pos0, N, H, d, m, W, k = 1, 5, 251, 256, 8, 64, 4, 8, 4
+    x, kc, vc, idx, cnt, out, lse = _run_csa(B, Nq, q_pos0, N, H, d, m, W, k, seed=11)
+    bad = idx.clone()
+    bad[0, 2, 1] = N // m + 5                     # out of range
+    out2, _ = csa.csa_attend(x["q"], kc, vc, bad, cnt, x["k_raw"], x["v_raw"], W, q_pos0)
+    flags = csa.device_status(reset=True)
+    assert flags & 0x1
+    for i in range(Nq):
+        sel = npy(idx[0, i])
+        if i == 2:
+            sel = sel[np.array([0, 2, 3])]
+        o, _ = O.csa_attend_one(f64(x["q"][0, i]), f64(kc[0]), f64(vc[0]), sel, len(sel),
+                                f64(x["k_raw"][0]), f64(x["v_raw"][0]), q_pos0 + i, W)
+        assert_attention_close(f64(out2[0, i]), o, f"i={i}")
 
 
 def test_bad_topk_index_is_flagged_and_skipped():
