@@ -1,6 +1,7 @@
 // CSA sparse attention and HCA dense attention over compressed entries plus a sliding window:
-// the mma.sync kernel (head dim 64), the split planner, the workspace merge and the dispatcher
-// (head dim 128 goes to the tcgen05 kernel in attend_tc.cu).
+// the split-K mma.sync flash-decode kernel (head dim 64, one query per sequence), the split
+// planner, the workspace merge and the dispatcher (head dim 128 goes to the tcgen05 kernel in
+// attend_tc.cu, head dim 64 prefill to the packed tcgen05 kernel in attend_pk.cu).
 //
 // Lighthouse "deep deepseek v4 release" 八.3: CSA attends to the top-k selected compressed
 // entries plus a sliding-window branch of n_win raw tokens; HCA attends densely to every
