@@ -173,10 +173,37 @@ csa_status check_index_keys(const uint16_t* xi_raw, const float* logits, int B, 
 // ---- internal runners (arguments already validated) -----------------------------------------
 // What the indexer may read before its grid-dependency wait (kernels.h, launch_indexer). The
 // default, for callers that do not know the kernel enqueued before them: nothing.
+// Entries [j0, j1) of every sequence to pool (csa_compress's arithmetic) inside the scoring
+// launch of a decode-shaped indexer call, instead of in a launch of their own.
+struct PoolRange {
+  const uint16_t* k_raw;
+  const uint16_t* v_raw;
+  const float* logits;
+  uint16_t* k_cmp;
+  uint16_t* v_cmp;
+  int64_t N, j0, j1;
+};
+
 struct Freshness {
   int64_t keys_from = 0;
   bool queries = true;
+  // optional: pool these entries inside the launch when the decode kernel scores (sets *pooled)
+  const PoolRange* pool = nullptr;
+  bool* pooled = nullptr;
 };
+
+void set_pool(DecodeArgs& a, const Freshness& fr) {
+  if (!fr.pool) return;
+  a.k_raw = fr.pool->k_raw;
+  a.v_raw = fr.pool->v_raw;
+  a.logits = fr.pool->logits;
+  a.k_cmp = fr.pool->k_cmp;
+  a.v_cmp = fr.pool->v_cmp;
+  a.N = fr.pool->N;
+  a.pool_j0 = fr.pool->j0;
+  a.pool_j1 = fr.pool->j1;
+  if (fr.pooled) *fr.pooled = true;
+}
 
 csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const uint8_t* ki_codes,
                        const uint8_t* ki_scales, int B, int Nq, int64_t q_pos0, int64_t E, int m,
@@ -215,6 +242,7 @@ csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
       a.keys_fresh_from = fr.keys_from;
       a.wait_first = fr.queries;
       a.attend = false;
+      set_pool(a, fr);
       return from_cuda(launch_decode(a, pl, status, st));
     }
   }
@@ -251,6 +279,7 @@ csa_status run_indexer(const uint8_t* qi_codes, const uint8_t* qi_scales, const 
       a.B = B;
       a.keys_fresh_from = fr.keys_from;
       a.wait_first = fr.queries;
+      set_pool(a, fr);
       return from_cuda(launch_decode_scores(a, split, chunk, status, st));
     }
   }
@@ -735,6 +764,7 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
   uint8_t* ws_c = static_cast<uint8_t*>(ws);
   uint8_t* ws_h = ws_c + pair_csa_ws(c);
   bool fused = false;  // the CSA decode layer ran as one launch (decode.cu)
+  bool pool_late = false;  // the CSA layer's closed blocks are pooled with its scoring or after it
   if (c) {
     const int64_t E = c->N / c->m;
     const int64_t j0 = c->compress_begin / c->m;
@@ -746,7 +776,11 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
       pl = plan_decode(c->B, E, nv, c->k, c->W, true, c->scores != nullptr);
     }
     const bool pool_inside = pl.ok && !c->xi_raw && E - j0 <= kDecodePoolMax;
-    if (!pool_inside &&
+    // Without the one-launch step, a decode-shaped layer may still pool the closed blocks in its
+    // scoring launch (below); other shapes pool first, in a launch of their own.
+    pool_late = !pl.ok && !c->xi_raw && E > j0 && E - j0 <= kDecodePoolMax &&
+                decode_indexer_fits(c->Nq, c->H_I, c->d_I);
+    if (!pool_inside && !pool_late &&
         launch_compress(c->k_raw, c->v_raw, c->logits, c->B, c->N, c->d, c->m, j0, E - j0,
                         c->k_cmp, c->v_cmp, st) != cudaSuccess)
       return CSA_ERR_CUDA;
@@ -798,7 +832,13 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
     const int64_t E = c->N / c->m;
     const int64_t j0 = c->compress_begin / c->m;
     Freshness fr;
-    if (E > j0) {
+    PoolRange pr{c->k_raw, c->v_raw, c->logits, c->k_cmp, c->v_cmp, c->N, j0, E};
+    bool pooled = false;
+    if (pool_late) {
+      // no launch of this call precedes the scoring: it waits for its predecessor first
+      fr.pool = &pr;
+      fr.pooled = &pooled;
+    } else if (E > j0) {
       fr.keys_from = c->xi_raw ? j0 : E;
       fr.queries = false;
     }
@@ -806,6 +846,11 @@ csa_status csa_hca_layer_pair(const csa_layer_desc* c, const hca_layer_desc* h, 
                                   c->Nq, c->q_pos0, E, c->m, c->H_I, c->d_I, c->k, c->topk_idx,
                                   c->topk_cnt, c->scores, ws_c, st, fr);
     if (s != CSA_OK) return s;
+    // the selection did not pool them: pool now, before the attention reads the entries
+    if (pool_late && !pooled &&
+        launch_compress(c->k_raw, c->v_raw, c->logits, c->B, c->N, c->d, c->m, j0, E - j0,
+                        c->k_cmp, c->v_cmp, st) != cudaSuccess)
+      return CSA_ERR_CUDA;
     AttendArgs a{c->q, c->k_cmp, c->v_cmp, c->topk_idx, c->topk_cnt, c->k_raw, c->v_raw, c->out,
                  c->lse, E, c->N, c->q_pos0, c->k, c->m, c->W, c->B, c->Nq, c->H, c->d};
     if (launch_attend(a, (int64_t)c->k + c->W, ws_c, status, st) != cudaSuccess) return CSA_ERR_CUDA;

@@ -352,7 +352,10 @@ __global__ void __launch_bounds__(kThreads, 1) csa_decode_kernel(const DecParams
 
   // The blocks this step closes: pooled by one warp of the cluster's last CTA, before its
   // epilogue work; the attention reads them only after the cluster barriers below.
-  if (p.pool_j1 > p.pool_j0 && rank == C - 1 && warp == kWarps - 1) pool_entries(p, b, lane);
+  if (p.pool_j1 > p.pool_j0 && rank == C - 1 && warp == kWarps - 1) {
+    pdl_wait();  // the entries it writes may still be read by the kernel before this one
+    pool_entries(p, b, lane);
+  }
 
   // ======================= phase 1: indexer scores into shared memory =======================
   if (ntiles > 0 && warp == kMmaWarp) {
@@ -1068,7 +1071,7 @@ cudaError_t launch_decode_scores(const DecodeArgs& a, int split, int chunk, uint
   pl.P = 0;
   DecodeArgs b = a;
   b.attend = false;
-  b.pool_j0 = b.pool_j1 = 0;
+  if (b.pool_j1 < b.pool_j0) b.pool_j1 = b.pool_j0;  // none
   DecParams p = decode_params(b, pl, status);
   p.split = split;
   auto kern = csa_decode_kernel;

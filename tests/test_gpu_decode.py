@@ -126,3 +126,37 @@ def test_decode_index_topk_matches_oracle(B, N, k, skew):
         ridx, rcnt = O.topk_select(ref, E, k)
         assert int(npy(cnt)[b, 0]) == rcnt
         np.testing.assert_array_equal(npy(idx)[b, 0], ridx, err_msg=f"top-k b={b}")
+
+
+@pytest.mark.parametrize("B,N,H,k", [(3, 8192, 128, 100),     # 128 heads: selection without attention
+                                     (2, 1048576, 64, 512)])  # 1M: scores over the whole GPU
+def test_decode_layer_pools_in_the_selection_launch(B, N, H, k):
+    """A decode layer the one-launch step does not take (more than 64 heads; entry shares above
+    8192 per CTA) pools the block the token closes inside its scoring launch: the entry written
+    there is bit-identical to csa_compress's, and the layer matches the oracle."""
+    m, W = 4, 128
+    s, x, layer = _layer(B, N, m, k, W, H, seed=N + H)
+    E = N // m
+    ref_k = torch.empty((B, E, 128), dtype=torch.bfloat16, device=DEV)
+    ref_v = torch.empty_like(ref_k)
+    csa.compress(x["k_raw"], x["v_raw"], x["logits"], m, ref_k, ref_v, E * m - m, E * m)
+    layer["k_cmp"][:, E - 1] = 7.0  # poisoned: the step must write it
+    layer["v_cmp"][:, E - 1] = 7.0
+    csa.layer_pair(layer, None)
+    torch.cuda.synchronize()
+    assert csa.device_status(reset=True) == 0
+    assert torch.equal(layer["k_cmp"][:, E - 1], ref_k[:, E - 1])
+    assert torch.equal(layer["v_cmp"][:, E - 1], ref_v[:, E - 1])
+    nv = O.visible_entries(N - 1, m, E)
+    for b in range(B):
+        qb, kr, vr = bits(x["q"][b]), bits(x["k_raw"][b]), bits(x["v_raw"][b])
+        sc = O.f64_to_bf16_rne(O.index_scores(npy(x["qi_codes"][b, 0]), npy(x["qi_scales"][b, 0]),
+                                              npy(x["ki_codes"][b]), npy(x["ki_scales"][b]), 64))
+        ridx, rcnt = O.topk_select(sc, nv, k)
+        assert int(npy(layer["topk_cnt"][b])[0]) == rcnt
+        np.testing.assert_array_equal(npy(layer["topk_idx"][b, 0]), ridx, err_msg=f"b={b}")
+        o, l = O.csa_attend_one(O.bf16_to_f64(qb[0]), f64(layer["k_cmp"][b]),
+                                f64(layer["v_cmp"][b]), ridx, rcnt, O.bf16_to_f64(kr),
+                                O.bf16_to_f64(vr), N - 1, W)
+        assert_attention_close(f64(layer["out"][b, 0]), o, f"out b={b}")
+        assert_lse_close(npy(layer["lse"][b, 0]), l, f"lse b={b}")
