@@ -460,6 +460,9 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
         sk[0] = exp2_int((int)(sbits & 0xFF) - 127);
         if (NB == 2) sk[NB - 1] = exp2_int((int)((sbits >> 8) & 0xFF) - 127);
         uint16_t* srow = p.scores + ((int64_t)b_first * p.Nq + i0) * p.E + j;
+        // every query of the group sees the whole tile (the common case away from the causal
+        // edge): no per-score visibility test
+        const bool all_vis = (int64_t)tile_row0(it) + kTileM <= (int64_t)qvis[0];
 #pragma unroll
         for (int k0 = 0; k0 < kChunksPerWarp; k0 += 2) {
           uint32_t r[2][16];
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
                     sc += fmaxf(dot, 0.f);
                   }
                   sc += 0.0f;  // -0 -> +0
-                  if (j < qvis[ql]) {
+                  if (all_vis || j < qvis[ql]) {
                     srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
                     if constexpr (F32OUT)
                       p.scores_f32[(srow - p.scores) + (int64_t)ql * p.E] = sc;
