@@ -285,6 +285,18 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
     if (rank == 0 && tid == 0) topk_cnt[row] = n;
     return;
   }
+  // One CTA per row and more rows than SMs (prefill): start the row one wave ahead on its way
+  // into L2, so that its CTA does not wait on HBM for its keys.
+  if (C == 1 && tid == 0) {
+    const int64_t r2 = row + kNumSMs;
+    constexpr int kb = F32 ? 4 : 2;
+    if (r2 < (int64_t)gridDim.x && (E * kb) % 16 == 0) {
+      const int64_t n2 = max((int64_t)0, min(E, (q_pos0 + (r2 % Nq) + 1) / m));
+      const char* a2 = static_cast<const char*>(scores) + r2 * E * kb;
+      const uint32_t bytes = (uint32_t)((n2 * kb + 15) & ~(int64_t)15);
+      if (bytes > 0 && (reinterpret_cast<uintptr_t>(a2) & 15u) == 0) prefetch_l2(a2, bytes);
+    }
+  }
   // ---- keys of this thread ---------------------------------------------------------------------
   const int seg0 = ((int)rank * NT + tid) * KPT;
   uint32_t key[KPT];
