@@ -360,11 +360,14 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
   }
   // ---- near-max histogram (one bin per BF16 step below the maximum) ----
   uint32_t* wh = whist + w * 256;
+  // The near-max windows hold few keys spread over 255 bins: with the row in one CTA they go
+  // straight into one block histogram (whist's first 256 words), which needs no per-warp sum.
+  uint32_t* const nh = C == 1 ? whist : wh;
   const uint32_t max_c = row_max >> CS;  // coarse parts of keys and maximum
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
     const uint32_t dd = max_c - (key[j] >> CS);
-    if (dd < 255u && seg0 + j < n) atomicAdd(&wh[dd], 1u);
+    if (dd < 255u && seg0 + j < n) atomicAdd(&nh[dd], 1u);
   }
   __syncthreads();
   auto sum_hist = [&](uint32_t* hist) {  // per-warp histograms -> hist -> cluster sum in gsum
@@ -379,7 +382,18 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
     }
     __syncthreads();
   };
-  sum_hist(hist1);
+  auto sum_near = [&](uint32_t* hist) {  // the near-max histogram -> gsum
+    if (C == 1) {
+      for (int q = tid; q < 256; q += NT) {
+        gsum[q] = whist[q];
+        whist[q] = 0u;
+      }
+      __syncthreads();
+    } else {
+      sum_hist(hist);
+    }
+  };
+  sum_near(hist1);
   select_prefix(gsum, (uint32_t)k, &sh_bin, &sh_above);
   __syncthreads();
   uint32_t Tc, above_c;  // coarse threshold and the count of keys whose coarse part exceeds it
@@ -399,10 +413,10 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
 #pragma unroll
       for (int j = 0; j < KPT; ++j) {
         const uint32_t dd = max_c - key[j];
-        if (dd - 255u < 255u && seg0 + j < n) atomicAdd(&wh[dd - 255u], 1u);
+        if (dd - 255u < 255u && seg0 + j < n) atomicAdd(&nh[dd - 255u], 1u);
       }
       __syncthreads();
-      sum_hist(hist2);
+      sum_near(hist2);
       select_prefix(gsum, (uint32_t)k - in0, &sh_bin, &sh_above);
       __syncthreads();
       if (sh_bin >= 0) {
