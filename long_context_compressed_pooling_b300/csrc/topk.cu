@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
   constexpr int CS = F32 ? 16 : 0;  // shift from a key to its coarse (16-bit) part
   __shared__ uint32_t whist[NW * 256];
   __shared__ uint32_t hist1[256], hist2[256], gsum[256];
-  __shared__ uint32_t wmax[NW];
+  __shared__ __align__(16) uint32_t wmax[NW];
   __shared__ uint32_t wa[33], wb[33];
   __shared__ uint32_t cta_val[3];  // this CTA's maximum, keys above T, keys equal to T
   __shared__ uint32_t bcast[2];
@@ -345,7 +345,10 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
   __syncthreads();
   uint32_t row_max = 0;
 #pragma unroll
-  for (int q = 0; q < NW; ++q) row_max = max(row_max, wmax[q]);
+  for (int q = 0; q < NW; q += 4) {  // 16-byte reads of the warps' maxima
+    const uint4 v4 = *reinterpret_cast<const uint4*>(&wmax[q]);
+    row_max = max(row_max, max(max(v4.x, v4.y), max(v4.z, v4.w)));
+  }
   if (C > 1) {
     if (tid == 0) cta_val[0] = row_max;
     cluster_sync();
