@@ -445,10 +445,10 @@ def run_native(args, rank, world):
 
 def kernel_times(prof, work, K, ms_step):
     """Per-kernel device time of one step. `prof` holds the library's event profile of K steps
-    (every launch bracketed by events on its own stream: the kernel timed alone). Kernels of a
-    step overlap (programmatic dependent launch, the side stream of a layer pair), so the step is
-    shorter than the sum of its kernels timed alone; each kernel's in-step time is the step time
-    split in proportion to its time alone."""
+    (every launch bracketed by events on its own stream, the layers of a pair one after the
+    other: the kernel timed alone). Kernels of a step overlap (programmatic dependent launch, the
+    side stream of a layer pair), so the step is shorter than the sum of its kernels timed alone;
+    each kernel's in-step time is the step time split in proportion to its time alone."""
     tot_alone = sum(t for _, t in prof.values()) / max(1, K)
     kern = {}
     for name, (launches, tot) in prof.items():
@@ -613,9 +613,16 @@ def run_workload(args, name, rank, world, dev, local):
            "step_frac_of_hbm": step_gbs / hbm, "step_alg_flops": step_flops}
     if not args.quick:
         # per-kernel device time: the same K steps again, each launch bracketed by events
+        # (a layer pair's two layers run one after the other here, so that no kernel's time
+        # includes the other layer's kernels running beside it on the side stream)
+        prof_call = call
+        if not args.paged and len(states) == 2:
+            one_c = csa.PreparedLayerPair(states["csa"], None)
+            one_h = csa.PreparedLayerPair(None, states["hca"])
+            prof_call = lambda: (one_c(), one_h())
         csa.profiler_enable(True)
         csa.profiler_collect(reset=True)
-        timed_loop(call)
+        timed_loop(prof_call)
         prof = csa.profiler_collect(reset=True)
         csa.profiler_enable(False)
         kwork = kernel_work(wl, work)
