@@ -103,8 +103,12 @@ CSA_DEV void work_sync(int n) { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memor
 template <int H_I, int NB, int SW, bool PREFILL, bool F32OUT, int EW = PREFILL ? 4 : 2>
 __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_constant__ CUtensorMap kmap,
                                                            const IdxParams p) {
-  constexpr int CPQ = H_I * NB * SW;
+  // Prefill puts both blocks' UE8M0 scales of entries (A) and queries (B) into the MMA, which
+  // then accumulates the two scaled block sums of a head into one column (exact, like every
+  // partial sum here); decode keeps one column per block and applies the scales afterwards.
+  constexpr int CPQ = PREFILL ? H_I : H_I * NB * SW;
   static_assert(16 % CPQ == 0, "columns per query must divide 16");
+  static_assert(!PREFILL || SW == 1, "prefill reads its key tiles through the tensor map");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -323,9 +327,11 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
   for (int idx = wt; idx < n_seq * p.ncols * 2; idx += kWork) {
     const int rr = idx >> 1, c = idx & 1;
     const int sl = rr / p.ncols, r = rr % p.ncols;
-    const int ql = r / CPQ, h = (r / (NB * SW)) % H_I, sw = (r / NB) % SW, blk = r % NB;
+    const int ql = r / CPQ, h = PREFILL ? r % H_I : (r / (NB * SW)) % H_I,
+              sw = (r / NB) % SW, blk = PREFILL ? c : r % NB;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (ql < nq && c == (blk ^ sw)) {
+    // prefill: row (query, head) holds both blocks; decode: one block per row, zeros elsewhere
+    if (ql < nq && (PREFILL ? c < NB : c == (blk ^ sw))) {
       const uint8_t* src = p.qi_codes +
           (((int64_t)(b_first + sl) * p.Nq + i0 + ql) * H_I + h) * (NB * 16) + blk * 16;
       v = *reinterpret_cast<const uint4*>(src);
@@ -335,11 +341,22 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
   }
   for (int rr = wt; rr < n_seq * p.ncols; rr += kWork) {
     const int sl = rr / p.ncols, r = rr % p.ncols;
-    const int ql = r / CPQ, h = (r / (NB * SW)) % H_I, blk = r % NB;
-    uint32_t e = 127u;  // scale 1.0 for the zero rows of absent queries
-    if (ql < nq)
-      e = p.qi_scales[(((int64_t)(b_first + sl) * p.Nq + i0 + ql) * H_I + h) * NB + blk];
-    qbyte[rr] = e;
+    const int ql = r / CPQ;
+    const int64_t qrow = ((int64_t)(b_first + sl) * p.Nq + i0 + ql) * H_I;
+    if constexpr (PREFILL) {
+      // the row's scale-factor word: byte 0 scales block 0, byte 1 block 1 (1.0 elsewhere)
+      const int h = r % H_I;
+      uint32_t w = 0x7F7F7F7Fu;
+      if (ql < nq) {
+        w = 0x7F7F0000u | p.qi_scales[(qrow + h) * NB];
+        w |= (NB == 2 ? (uint32_t)p.qi_scales[(qrow + h) * NB + 1] : 127u) << 8;
+      }
+      qbyte[rr] = w;
+    } else {
+      const int h = (r / (NB * SW)) % H_I, blk = r % NB;
+      qbyte[rr] = ql < nq ? (uint32_t)p.qi_scales[(qrow + h) * NB + blk]
+                          : 127u;  // scale 1.0 for the zero rows of absent queries
+    }
   }
   for (int ql = wt; ql < nq; ql += kWork)
     qvis[ql] = min(p.E, (p.q_pos0 + i0 + ql + 1) / p.m);
@@ -354,7 +371,10 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t acc_cols = (uint32_t)(G * p.ncols);  // one accumulator group
-  const uint32_t sfa_col = (uint32_t)p.nacc * acc_cols, sfb_col = sfa_col + kSfCols;
+  // scale-factor regions, each on a 16-column boundary: A (prefill: one per accumulator group,
+  // rewritten for every tile), then B
+  const uint32_t sfa_col = (uint32_t)p.nacc * acc_cols;
+  const uint32_t sfb_col = sfa_col + (uint32_t)(PREFILL ? p.nacc : 1) * kSfCols;
   // Prefill (one sequence per CTA): every B column carries its query block's UE8M0 scale, so the
   // MMA yields scale x (exact partial sum of e2m1 products), still exact. Decode CTAs may hold
   // several sequences behind one scale region: their B scales stay 1.0 and the query scales are
@@ -362,15 +382,14 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
   constexpr bool q_in_mma = PREFILL;
   if (warp >= 2 && warp < 6) {
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-#pragma unroll
-    for (int c = 0; c < 2 * kSfCols; c += 8)
-      tmem_st8_fill(tmem + lane_base + sfa_col + c, 0x7F7F7F7Fu);
+    for (uint32_t c = sfa_col; c < sfb_col + kSfCols; c += 8)
+      tmem_st8_fill(tmem + lane_base + c, 0x7F7F7F7Fu);
     if (q_in_mma) {
       tmem_st_wait();
       for (int c = 0; c < (p.ncols + 31) / 32; ++c) {
         const int n = c * 32 + lane;
-        const uint32_t e = n < p.ncols ? qbyte[n] : 127u;
-        tmem_st1(tmem + lane_base + sfb_col + (uint32_t)c, e * 0x01010101u);
+        const uint32_t w = n < p.ncols ? qbyte[n] : 0x7F7F7F7Fu;
+        tmem_st1(tmem + lane_base + sfb_col + (uint32_t)c, PREFILL ? w : w * 0x01010101u);
       }
     }
     tmem_st_wait();
@@ -389,7 +408,8 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
       const int slot = u % kSlots;
       const int a = g % p.nacc;
       const uint32_t aph = (uint32_t)(g / p.nacc) & 1u;
-      if (!mbar_wait_warp(&tempty[a], aph ^ 1u, p.status, p.wait_budget) ||
+      // (prefill: the epilogue's first round of arrivals says the buffer's tile scales are in)
+      if (!mbar_wait_warp(&tempty[a], PREFILL ? aph : aph ^ 1u, p.status, p.wait_budget) ||
           !mbar_wait_warp(&full[slot], (uint32_t)(u / kSlots) & 1u, p.status, p.wait_budget)) {
         if (lane == 0) *aborted = 1;
         break;
@@ -406,7 +426,7 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
               smem_addr(btile + (tile_seq(it) - b_first) * p.ncols * kRowBytes), 16, 256,
               kSwizzle32B);
           umma_mxf4(tmem + (uint32_t)(a * acc_cols + i * p.ncols), adesc, bdesc, idesc,
-                    tmem + sfa_col, tmem + sfb_col, 0u);
+                    tmem + sfa_col + (PREFILL ? (uint32_t)a * kSfCols : 0u), tmem + sfb_col, 0u);
         }
         if (unit_done) umma_commit(&empty[slot]);  // the slot's last group frees the slot
         umma_commit(&tfull[a]);
@@ -424,6 +444,43 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
     const bool swapped = SW == 2 && ((row >> 2) & 1);  // unswizzled row read through the swizzle
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const int cchunks = p.ncols / 16;
+    // Prefill: warp 0 of each lane quarter writes the entry scales of tile `it` into the A
+    // scale region of accumulator group `a` (row i of the tile: lane i, column i / 32, byte k
+    // scaling block k), once the tile's scales are in shared memory (or from global memory).
+    auto write_sfa = [&](int it, int a) -> bool {
+      if (scales_in_smem) {
+        const int u = it / kSlotTiles;
+        if (!mbar_wait_warp(&full[u % kSlots], (uint32_t)(u / kSlots) & 1u, p.status,
+                            p.wait_budget))
+          return false;
+      }
+      const int64_t j = (int64_t)tile_row0(it) + row;
+      uint32_t sb = 0x7F7Fu;
+      if (j < p.E) {
+        if (scales_in_smem)
+          sb = *reinterpret_cast<const uint16_t*>(stiles + ring_tile(it) * kScaleTileBytes +
+                                                  row * 2);
+        else
+          sb = NB == 2 ? (uint32_t)*reinterpret_cast<const uint16_t*>(
+                             p.ki_scales + ((int64_t)b_first * p.E + j) * 2)
+                       : (uint32_t)p.ki_scales[(int64_t)b_first * p.E + j];
+        if (NB == 1) sb = (sb & 0xFFu) | 0x7F00u;
+      }
+      tmem_st1(tmem + lane_base + sfa_col + (uint32_t)(a * kSfCols + quarter), 0x7F7F0000u | sb);
+      tmem_st_wait();
+      return true;
+    };
+    if constexpr (PREFILL) {
+      // the first tile of every accumulator group; this round of arrivals tells the MMA warp
+      bool ok = true;
+      if (sub == 0)
+        for (int a = 0; a < p.nacc && a < ntiles && ok; ++a) ok = write_sfa(a, a);
+      if (!ok && lane == 0) *aborted = 1;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0)
+        for (int a = 0; a < p.nacc; ++a) mbar_arrive(&tempty[a]);
+    }
     for (int g = 0; g < ngroups; ++g) {
       const int a = g % p.nacc;
       const uint32_t aph = (uint32_t)(g / p.nacc) & 1u;
@@ -446,19 +503,6 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
         constexpr int kChunksPerWarp = (kMaxCols / 16 + EW - 1) / EW;
         const int it = g;
         const int64_t j = (int64_t)tile_row0(it) + row;
-        uint32_t sbits = 0;
-        if (j < p.E) {
-          if (scales_in_smem && NB == 2)
-            sbits = *reinterpret_cast<const uint16_t*>(stiles + ring_tile(it) * kScaleTileBytes +
-                                                       row * 2);
-          else
-            sbits = NB == 2
-                ? (uint32_t)*reinterpret_cast<const uint16_t*>(p.ki_scales + ((int64_t)b_first * p.E + j) * 2)
-                : (uint32_t)p.ki_scales[(int64_t)b_first * p.E + j];
-        }
-        float sk[NB];
-        sk[0] = exp2_int((int)(sbits & 0xFF) - 127);
-        if (NB == 2) sk[NB - 1] = exp2_int((int)((sbits >> 8) & 0xFF) - 127);
         uint16_t* srow = p.scores + ((int64_t)b_first * p.Nq + i0) * p.E + j;
         // every query of the group sees the whole tile (the common case away from the causal
         // edge): no per-score visibility test
@@ -482,15 +526,10 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
               for (int cc = 0; cc < 16; cc += CPQ) {
                 const int ql = (c * 16 + cc) / CPQ;
                 if (ql < nq) {
+                  // column (query, head) holds the head's exact scaled dot product
                   float sc = 0.f;
 #pragma unroll
-                  for (int h = 0; h < H_I; ++h) {
-                    float dot = 0.f;
-#pragma unroll
-                    for (int blk = 0; blk < NB; ++blk)
-                      dot = fmaf(__uint_as_float(r[k][cc + h * NB + blk]), sk[blk], dot);
-                    sc += fmaxf(dot, 0.f);
-                  }
+                  for (int h = 0; h < H_I; ++h) sc += fmaxf(__uint_as_float(r[k][cc + h]), 0.f);
                   sc += 0.0f;  // -0 -> +0
                   if (all_vis || j < qvis[ql]) {
                     srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
@@ -575,6 +614,11 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
           }
         }
       }
+      if (PREFILL && sub == 0 && g + p.nacc < ntiles) {
+        // this group's accumulator and scale region are free once this warp arrives: the
+        // scales of the tile that reuses them go in first
+        if (!write_sfa(g + p.nacc, a) && lane == 0) *aborted = 1;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -636,13 +680,15 @@ bool indexer_bulk_path(int H_I, int d_I, int64_t E, int Nq) {
 IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I, bool paged) {
   IndexerPlan pl{};
   // paged keys are copied whole-tile from their pages: the bulk path whatever E is
-  const int cpq = H_I * (d_I / 32) * (indexer_bulk_path(H_I, d_I, paged ? 8 : E, Nq) ? 2 : 1);
+  // prefill: one column per (query, head), both blocks scaled inside the MMA
+  const int cpq = Nq > 1 ? H_I
+                         : H_I * (d_I / 32) * (indexer_bulk_path(H_I, d_I, paged ? 8 : E, Nq) ? 2 : 1);
   if (Nq == 1) {  // two CTAs per SM: 3 x 64 + 32 scale columns fit in 256
     pl.QN = 1;
     pl.ncols = cpq > 16 ? 32 : 16;
     pl.G = kMaxG;
     pl.nacc = 3;
-  } else {         // one CTA per SM: 2 x 224 + 32 columns fit in 512
+  } else {         // one CTA per SM: 2 x 224 + 3 x 16 scale columns fit in 512
     pl.QN = kMaxCols / cpq;
     pl.ncols = pl.QN * cpq;
     pl.G = 1;
@@ -668,7 +714,8 @@ IndexerPlan plan_indexer(int B, int Nq, int64_t E, int H_I, int d_I, bool paged)
     if (splits < 1) splits = 1;
     pl.n_splits = (int)splits;
   }
-  pl.tmem_cols = next_pow2_at_least32(pl.nacc * pl.G * pl.ncols + 2 * kSfCols);
+  pl.tmem_cols = next_pow2_at_least32(pl.nacc * pl.G * pl.ncols +
+                                      (Nq > 1 ? pl.nacc + 1 : 2) * kSfCols);
   return pl;
 }
 
