@@ -118,7 +118,8 @@ def _tie_scores(rng, shape):
                                              (262144, 1, 1048575, 4, 2048),  # cluster of 16
                                              (33001, 1, 132007, 4, 400),     # odd rows, C = 9
                                              (40000, 5, 159000, 4, 300),     # C = 10, 5 rows
-                                             (5000, 3, 4094, 1, 40)])  # CTAs past the row end
+                                             (5000, 3, 4094, 1, 40),   # CTAs past the row end
+                                             (20000, 300, 79700, 4, 2048)])  # 600 one-CTA rows
 def test_topk_ties_and_negative_scores(E, Nq, q_pos0, m, k):
     rng = np.random.default_rng(E + k)
     sc_np = _tie_scores(rng, (2, Nq, E))
@@ -132,14 +133,14 @@ def test_topk_ties_and_negative_scores(E, Nq, q_pos0, m, k):
             assert cnt[b, i] == rcnt and np.array_equal(idx[b, i], ridx), (b, i)
 
 
+@pytest.mark.parametrize("Nq", [150, 300])
 @pytest.mark.parametrize("kind", ["spread", "sampled_high", "few_values"])
-def test_topk_many_rows_sampled_threshold(kind):
-    """Rows of one CTA each (>= 148 rows of 16000-32768 keys): the selector's sampled threshold
-    (every thread's first key is a sample) with ordinary scores, with the largest scores placed
-    exactly on the sampled positions (the count above the sampled threshold falls short of k and
-    the general path runs), and with only five distinct values (huge tie groups)."""
-    rng = np.random.default_rng({"spread": 1, "sampled_high": 2, "few_values": 3}[kind])
-    B, Nq, E, m, k = 1, 150, 32768, 4, 2048
+def test_topk_many_rows_one_cta_each(kind, Nq):
+    """Rows of one CTA each, 32768 keys (150 and 300 rows): ordinary scores, the largest scores
+    on every 32nd position, and only five distinct values (huge tie groups); top-k lists
+    bit-exact."""
+    rng = np.random.default_rng({"spread": 1, "sampled_high": 2, "few_values": 3}[kind] + Nq)
+    B, E, m, k = 1, 32768, 4, 2048
     q_pos0 = E * m - Nq  # the rows see 32731 .. 32768 entries
     if kind == "spread":
         vals = rng.gamma(4.0, 2.0, size=(B, Nq, E)).astype(np.float32)
