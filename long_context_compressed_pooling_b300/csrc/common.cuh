@@ -154,7 +154,7 @@ CSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
 }
 
 // Warp-wide bounded wait: every lane waits (each lane's wait is bounded) and the warp takes lane
-// 0's verdict, so the result is uniform across the warp.
+// 0's outcome, so the result is uniform across the warp.
 CSA_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status,
                             long long budget = kWaitBudgetCycles) {
   const int ok = mbar_wait(bar, parity, status, budget) ? 1 : 0;

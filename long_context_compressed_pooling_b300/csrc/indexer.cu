@@ -7,20 +7,28 @@
 // with q_I, k_I block-scaled FP4 vectors (e2m1 codes, one UE8M0 scale per 32 elements).
 //
 // Layout of the contraction. A = the entries' FP4 index keys (M = 128 entries per tile,
-// K = 64 e2m1 values = 32 bytes per row). B = the queries, one B row per (query, head, 32-element
-// block): the row holds that block's codes and zeros elsewhere, so D[j, (q,h,blk)] is the
-// UNSCALED partial dot product of one scale block. With d_I = 64 a tile is 4 KB contiguous in
-// HBM and arrives with ONE bulk copy (a tensor-map box with 32-byte rows would cost 128 small
-// TMA requests per tile); it lands unswizzled while the MMA reads it through the 32-byte swizzle,
-// which swaps the two 16-byte halves of rows whose bit 2 is set. Those rows therefore meet the
-// query blocks in swapped positions, so B carries each head twice (blocks in place, blocks
-// swapped) and every epilogue thread reads the pair that matches its row. d_I = 32 rows (16 B)
-// keep the TMA path, whose box is zero-filled to 32 bytes. The
-// MMA runs kind::mxf4 with every scale factor set to 1.0; the real UE8M0 scales are applied in
-// the epilogue as exact power-of-two multiplies. Partial sums of e2m1 products are multiples of
-// 1/4 below 2^11, so the tensor core's fp32 accumulation is exact, and the epilogue's scaled
-// sums stay exact for the scale range the workloads use (2^-4..2^0): the BF16 rounding is then
-// the only rounding, as the method specifies.
+// K = 64 e2m1 values = 32 bytes per row).
+// Decode (one query per sequence): B = one row per (query, head, 32-element block) holding that
+// block's codes and zeros elsewhere, so D[j, (q,h,blk)] is the UNSCALED partial dot product of
+// one scale block, every scale factor is 1.0 and the UE8M0 scales are applied in the epilogue as
+// exact power-of-two multiplies. With d_I = 64 a tile is 4 KB contiguous in HBM and arrives with
+// ONE bulk copy (a tensor-map box with 32-byte rows would cost 128 small TMA requests per tile);
+// it lands unswizzled while the MMA reads it through the 32-byte swizzle, which swaps the two
+// 16-byte halves of rows whose bit 2 is set. Those rows therefore meet the query blocks in
+// swapped positions, so B carries each head twice (blocks in place, blocks swapped) and every
+// epilogue thread reads the pair that matches its row.
+// Prefill (a query group per CTA, swizzled TMA tiles): B = one row per (query, head) with both
+// blocks, and the block scales of entries (A) and queries (B) are the MMA's scale factors, so
+// D[j, (q,h)] is the head's scaled dot product and the epilogue only takes ReLU, sums the heads
+// and rounds. The A scale factors change with every tile: one region per accumulator group,
+// rewritten by the epilogue before it releases the group to the next tile (row i of a tile: lane
+// i, column i / 32; byte k of the word scales block k). d_I = 32 rows (16 B) are zero-padded to
+// 32 bytes (the TMA box is zero-filled, B's second block is zero).
+// Exactness: a block's partial sum of e2m1 products is a multiple of 1/4 below 2^11, a scaled
+// block sum a multiple of 2^-10 below 2^12 for the workloads' scales (2^-4..2^0), so the fp32
+// sums, in the tensor core or in the epilogue, are exact (a GPU probe confirmed it for the
+// scaled two-block accumulation) and the BF16 rounding is the only rounding, as the method
+// specifies.
 //
 // Pipeline. A copy warp fills a 3-slot ring (8 tiles per slot: one bulk copy of codes and one
 // of scales per slot, since each copy instruction costs ~0.3 us to issue whatever its size); it
