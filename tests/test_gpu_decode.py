@@ -160,3 +160,51 @@ def test_decode_layer_pools_in_the_selection_launch(B, N, H, k):
                                 O.bf16_to_f64(vr), N - 1, W)
         assert_attention_close(f64(layer["out"][b, 0]), o, f"out b={b}")
         assert_lse_close(npy(layer["lse"][b, 0]), l, f"lse b={b}")
+
+
+@pytest.mark.parametrize("B,N,Nq,H,d", [(2, 8192, 1, 64, 128),    # decode: the one-launch step
+                                        (1, 2048, 40, 64, 128),   # prefill rows
+                                        (1, 1024, 24, 8, 64)])    # head dim 64, packed prefill
+def test_shared_kv_buffers(B, N, Nq, H, d):
+    """Shared-KV models pass one buffer as both K and V (raw and pooled): k_raw is v_raw and
+    k_cmp is v_cmp. Both layers of a pair must match the oracle run with V = K."""
+    m, k, W = 4, 64, 32
+    q0 = N - Nq
+    cb = (q0 // m) * m if Nq > 1 else N - m
+    s = LayerShape("csa", B=B, N=N, Nq=Nq, q_pos0=q0, H=H, d=d, m=m, W=W, k=k, H_I=4, d_I=64,
+                   q_scale=1.0 / np.sqrt(d), compress_begin=cb)
+    x = generate_layer(s, seed=N + Nq + d, device=DEV)
+    kv = x["k_raw"]  # one raw buffer
+    E = N // m
+    cmp = torch.empty((B, E, d), dtype=torch.bfloat16, device=DEV)  # one pooled buffer
+    if cb > 0:
+        csa.compress(kv, kv, x["logits"], m, cmp, cmp, 0, cb)
+    layer = dict(q=x["q"], k_raw=kv, v_raw=kv, logits=x["logits"], qi_codes=x["qi_codes"],
+                 qi_scales=x["qi_scales"], ki_codes=x["ki_codes"], ki_scales=x["ki_scales"],
+                 k_cmp=cmp, v_cmp=cmp, out=torch.empty_like(x["q"]),
+                 topk_idx=torch.empty((B, Nq, k), dtype=torch.int32, device=DEV),
+                 topk_cnt=torch.empty((B, Nq), dtype=torch.int32, device=DEV),
+                 m=m, W=W, k=k, q_pos0=q0, compress_begin=cb)
+    hs = LayerShape("hca", B=B, N=N, Nq=Nq, q_pos0=q0, H=H, d=d, m=128, W=W, k=0, H_I=0, d_I=0,
+                    q_scale=1.0 / np.sqrt(d), compress_begin=(q0 // 128) * 128 if Nq > 1 else N - 128)
+    hx = generate_layer(hs, seed=N + 7, device=DEV)
+    hkv, hE = hx["k_raw"], N // 128
+    hcmp = torch.empty((B, hE, d), dtype=torch.bfloat16, device=DEV)
+    if hs.compress_begin > 0:
+        csa.compress(hkv, hkv, hx["logits"], 128, hcmp, hcmp, 0, hs.compress_begin)
+    hlayer = dict(q=hx["q"], k_raw=hkv, v_raw=hkv, logits=hx["logits"], k_cmp=hcmp, v_cmp=hcmp,
+                  out=torch.empty_like(hx["q"]), m=128, W=W, q_pos0=q0,
+                  compress_begin=hs.compress_begin)
+    csa.layer_pair(layer, hlayer)
+    torch.cuda.synchronize()
+    assert csa.device_status(reset=True) == 0
+    for b in range(B):
+        qb, kr = bits(x["q"][b]), bits(kv[b])
+        ref = O.csa_layer_seq(qb, kr, kr, npy(x["logits"][b]), npy(x["qi_codes"][b]),
+                              npy(x["qi_scales"][b]), npy(x["ki_codes"][b]),
+                              npy(x["ki_scales"][b]), m=m, W=W, k=k, d_I=64, q_pos0=q0)
+        np.testing.assert_array_equal(npy(layer["topk_idx"][b]), ref["idx"], err_msg=f"b={b}")
+        assert_attention_close(f64(layer["out"][b]), ref["out"], f"csa b={b}")
+        hr = O.hca_layer_seq(bits(hx["q"][b]), bits(hkv[b]), bits(hkv[b]), npy(hx["logits"][b]),
+                             m=128, W=W, q_pos0=q0)
+        assert_attention_close(f64(hlayer["out"][b]), hr["out"], f"hca b={b}")
