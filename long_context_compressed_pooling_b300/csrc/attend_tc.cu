@@ -15,7 +15,7 @@
 // 32q..32q+15, so a softmax warp reads its 16 rows with the 16x256b load, which hands every
 // thread two rows in the m16n8 fragment layout.
 //
-// Warp roles (544 threads, one CTA per SM):
+// Warp roles (576 threads, one CTA per SM):
 //   warps 0-7  softmax: warp w reads rows 16(w % 4) .. +15 of key half w / 4 of S, masks, runs an
 //              online softmax with its own running maximum per key half, writes P (bf16) to
 //              shared memory, and rescales its O accumulator in tensor memory only when the
@@ -29,9 +29,10 @@
 //              and unmapped pages are zero-filled and masked); each loader thread arrives on the
 //              stage's barrier twice: at once (releasing the mask bits) and when its copies land
 //              (cp.async.mbarrier.arrive);
-//   warp 16    tensor-memory allocation and the MMAs (one elected lane of the converged warp),
-//              issued as soon as they are ready: PV of the oldest chunk whose P is written, and
-//              QK^T of the next chunk, which overlaps the softmax of the current one.
+//   warp 16    tensor-memory allocation and the QK^T MMAs of each chunk once its K/V rows have
+//              landed and an S buffer is free (one elected lane of the converged warp);
+//   warp 17    the PV MMAs of each chunk once its P is written: a tcgen05.mma takes ~100 cycles
+//              to issue from one thread, so the two contractions have an issuing warp each.
 // Three K/V stages (64 KB each) and one P buffer; every mbarrier wait is bounded.
 //
 // Decode splits a token's key chunks over several CTAs: the splits of a token form a cluster and
@@ -53,9 +54,10 @@ constexpr int kSoftmaxWarps = 8;   // warps 0-7: lane quarter w % 4, key half w 
 constexpr int kLoadWarp0 = 8;      // warps 8-15
 constexpr int kLoadWarps = 8;
 constexpr int kLoadThreads = 32 * kLoadWarps;
-constexpr int kMmaWarp = 16;
-constexpr int kThreads = 544;
-constexpr int kSetupThreads = 32 * (kSoftmaxWarps + 1);  // softmax warps + MMA warp
+constexpr int kMmaWarp = 16;      // QK^T issuer, tensor-memory allocation
+constexpr int kPvWarp = 17;       // PV issuer
+constexpr int kThreads = 576;
+constexpr int kSetupThreads = 32 * (kSoftmaxWarps + 2);  // softmax warps + both MMA warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 256;    // O accumulators: key half 0 at [256, 384), half 1 at [384, 512)
 constexpr int kQBytes = kM * kD * 2;        // 16 KB
@@ -155,7 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
   if (!loader) {
     // Q tile of heads [h_base, h_base + 64) (zero rows past H; Q is an input of this call) and
     // the tensor memory, by the softmax and MMA warps while the loaders' first copies fly
-    const int nt = warp == kMmaWarp ? kSoftmaxWarps * 32 + lane : (int)threadIdx.x;
+    const int nt = warp >= kMmaWarp ? (kSoftmaxWarps + warp - kMmaWarp) * 32 + lane
+                                    : (int)threadIdx.x;
     for (int x = nt; x < kM * 16; x += kSetupThreads) {
       const int r = x >> 4, c = x & 15;
       const bool ok = h_base + r < p.H;
@@ -275,76 +278,60 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
     }
     cp_async_wait<0>();  // never leave with copies in flight
   } else if (warp == kMmaWarp) {
-    // ------------------------------- MMA issuer -------------------------------
-    // Issues whichever MMA is ready (PV of the oldest chunk with its P written, QK^T of the next
-    // chunk with its K/V landed and an S buffer free), so neither waits behind the other.
+    // ------------------------------- QK^T issuer -------------------------------
+    // One tcgen05.mma takes ~100 cycles to issue from one thread, so QK^T and PV have a warp
+    // each: QK^T of the next chunk never waits behind the PV of the current one.
     const uint32_t id_qk = idesc_bf16(kM, kKC, false, false);
-    const uint32_t id_pv = idesc_bf16(kM, kD, false, true);
-    int nq = 0, np = 0;
-    long long idle0 = clock64();
-    while (np < nloc) {
-      bool did = false;
-      if (np < nq) {
-        int ready = lane == 0 ? (int)mbar_test(p_full, (uint32_t)np & 1u) : 0;
-        ready = __shfl_sync(0xffffffffu, ready, 0);
-        if (ready) {
-          tc_fence_after();
-          const int s = np % kStages;
-          if (elect_one()) {
-            const uint32_t pt = smem_addr(Ps);
-            const uint32_t vt = smem_addr(KV + s * 2 * kTileBytes + kTileBytes);
-#pragma unroll
-            for (int kk = 0; kk < kKC / 16; ++kk) {
-              const uint32_t atom = kk >> 2, kin = (kk & 3) * 32;
-              const uint64_t ad = smem_desc(pt + atom * kM * 128 + kin, 16, 1024, kSwizzle128B);
-              // V rows are keys (the K dimension) with d contiguous: MN-major B, 64-column
-              // atoms kKC * 128 bytes apart, 8-key groups 1024 bytes apart.
-              const uint64_t bd = smem_desc(vt + kk * 16 * 128, kKC * 128, 1024, kSwizzle128B);
-              // keys 0-63 accumulate into O half 0, keys 64-127 into O half 1
-              umma_bf16(tmem + kOCol + atom * kD, ad, bd, id_pv,
-                        (np > 0 || (kk & 3) > 0) ? 1u : 0u);
-            }
-            umma_commit(&kv_empty[s]);
-            umma_commit(pv_done);
-          }
-          __syncwarp();
-          ++np;
-          did = true;
-        }
-      }
-      if (nq < nloc) {
-        const int s = nq % kStages, sb = nq & 1;
-        int ready = 0;
-        if (lane == 0)
-          ready = mbar_test(&kv_full[s], (uint32_t)(nq / kStages) & 1u) &&
-                  (nq < 2 || mbar_test(&s_free[sb], (uint32_t)((nq >> 1) - 1) & 1u));
-        ready = __shfl_sync(0xffffffffu, ready, 0);
-        if (ready) {
-          fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
-          tc_fence_after();
-          if (elect_one()) {
-            const uint32_t kt = smem_addr(KV + s * 2 * kTileBytes);
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t atom = kk >> 2, kin = (kk & 3) * 32;
-              const uint64_t ad = smem_desc(smem_addr(Qs) + atom * kM * 128 + kin, 16, 1024,
-                                            kSwizzle128B);
-              const uint64_t bd = smem_desc(kt + atom * kKC * 128 + kin, 16, 1024, kSwizzle128B);
-              umma_bf16(tmem + (uint32_t)(sb * kKC), ad, bd, id_qk, kk > 0 ? 1u : 0u);
-            }
-            umma_commit(&s_full[sb]);
-          }
-          __syncwarp();
-          ++nq;
-          did = true;
-        }
-      }
-      if (did) {
-        idle0 = clock64();
-      } else if (clock64() - idle0 > kWaitBudgetCycles) {
-        if (lane == 0) atomicOr(p.status, kFlagTimeout);
+    for (int nq = 0; nq < nloc; ++nq) {
+      const int s = nq % kStages, sb = nq & 1;
+      if (!mbar_wait_warp(&kv_full[s], (uint32_t)(nq / kStages) & 1u, p.status) ||
+          (nq >= 2 && !mbar_wait_warp(&s_free[sb], (uint32_t)((nq >> 1) - 1) & 1u, p.status)))
         break;
+      fence_proxy_async_smem();  // cp.async (generic proxy) data -> tensor-core reads
+      tc_fence_after();
+      // descriptors of the first K step, built by the whole (converged) warp; a step's
+      // descriptor adds its byte offset / 16 to the start-address field
+      const uint64_t qd = smem_desc(smem_addr(Qs), 16, 1024, kSwizzle128B);
+      const uint64_t kd = smem_desc(smem_addr(KV + s * 2 * kTileBytes), 16, 1024, kSwizzle128B);
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t atom = kk >> 2, kin = (kk & 3) * 32;
+          umma_bf16(tmem + (uint32_t)(sb * kKC), qd + ((atom * kM * 128 + kin) >> 4),
+                    kd + ((atom * kKC * 128 + kin) >> 4), id_qk, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&s_full[sb]);
       }
+      __syncwarp();
+    }
+  } else if (warp == kPvWarp) {
+    // ------------------------------- PV issuer -------------------------------
+    const uint32_t id_pv = idesc_bf16(kM, kD, false, true);
+    for (int np = 0; np < nloc; ++np) {
+      const int s = np % kStages;
+      // P of the chunk is written (and its stage's V rows landed before its S existed)
+      if (!mbar_wait_warp(p_full, (uint32_t)np & 1u, p.status) ||
+          !mbar_wait_warp(&kv_full[s], (uint32_t)(np / kStages) & 1u, p.status))
+        break;
+      fence_proxy_async_smem();
+      tc_fence_after();
+      const uint64_t pd = smem_desc(smem_addr(Ps), 16, 1024, kSwizzle128B);
+      // V rows are keys (the K dimension) with d contiguous: MN-major B, 64-column atoms
+      // kKC * 128 bytes apart, 8-key groups 1024 bytes apart.
+      const uint64_t vd = smem_desc(smem_addr(KV + s * 2 * kTileBytes + kTileBytes), kKC * 128,
+                                    1024, kSwizzle128B);
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < kKC / 16; ++kk) {
+          const uint32_t atom = kk >> 2, kin = (kk & 3) * 32;
+          // keys 0-63 accumulate into O half 0, keys 64-127 into O half 1
+          umma_bf16(tmem + kOCol + atom * kD, pd + ((atom * kM * 128 + kin) >> 4),
+                    vd + ((kk * 16 * 128) >> 4), id_pv, (np > 0 || (kk & 3) > 0) ? 1u : 0u);
+        }
+        umma_commit(&kv_empty[s]);
+        umma_commit(pv_done);
+      }
+      __syncwarp();
     }
   } else {
     // ------------------------------- softmax -------------------------------
