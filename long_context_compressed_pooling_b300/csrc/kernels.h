@@ -148,7 +148,8 @@ cudaError_t launch_attend_pk(const AttendArgs& a, uint32_t* status, cudaStream_t
 int attend_tc_chunk_keys();
 // n_splits CTAs per (token, 64-head group); cluster = 1 merges the splits through distributed
 // shared memory (returns cudaErrorNotSupported if such a cluster cannot be scheduled), else the
-// splits write ws_o / ws_ml for the merge kernel.
+// splits write ws_o / ws_ml for the merge kernel. n_splits = 1 (without a cluster) launches
+// persistent CTAs, at most one per SM, each walking several (token, head group) items.
 cudaError_t launch_attend_tc(const AttendArgs& a, int n_splits, int cluster, float* ws_o,
                              float* ws_ml, uint32_t* status, cudaStream_t stream);
 

@@ -176,6 +176,10 @@ ATT_CASES = [
     (2, 37, 900, 1000, 4, 64, 4, 32, 20),    # 16 tokens per CTA, last group partial, 2 sequences
     (1, 9, 2000, 2048, 12, 64, 4, 16, 50),   # 12 heads padded to 16: 4 tokens per CTA
     (1, 2, 4000, 4096, 128, 64, 4, 128, 40),  # two 64-head groups, one token per CTA
+    # d = 128 prefill, persistent CTAs (one per SM) walking several tokens each
+    (2, 300, 1700, 2000, 64, 128, 4, 100, 300),  # 600 tokens of 4 key chunks, ragged last chunk
+    (1, 500, 100, 700, 64, 128, 4, 40, 150),    # 1-2 chunks per token, counts vary by token
+    (1, 200, 1000, 1200, 128, 128, 4, 64, 100),  # two head groups: 400 (token, group) items
 ]
 
 
@@ -215,6 +219,27 @@ def test_csa_attend_matches_oracle(B, Nq, q_pos0, N, H, d, m, W, k):
         assert_attention_close(f64(out[b]), ref["out"], f"layer b={b}")
 
 
+def test_csa_attend_tokens_without_keys_persistent():
+    """Persistent CTAs walking tokens of which some have no key (no window, t < 3 sees no
+    entry) and most have one to a few: every token's output and log-sum-exp against the oracle
+    on the GPU's bf16 entries; keyless tokens give zeros and -inf. (The whole-layer comparison
+    with the oracle's fp64 pooling does not apply here: a token with one key outputs that entry,
+    so its error is the entry's own bf16 rounding, up to ~2^-9 of values near 3.)"""
+    B, Nq, q_pos0, N, H, d, m, W, k = 1, 300, 0, 300, 64, 128, 4, 0, 64
+    x, kc, vc, idx, cnt, out, lse = _run_csa(B, Nq, q_pos0, N, H, d, m, W, k, seed=N + k)
+    qb, kr, vr = bits(x["q"]), bits(x["k_raw"]), bits(x["v_raw"])
+    kcf, vcf = f64(kc[0]), f64(vc[0])
+    for i in range(Nq):
+        o, l = O.csa_attend_one(O.bf16_to_f64(qb[0, i]), kcf, vcf, npy(idx[0, i]),
+                                int(cnt[0, i]), O.bf16_to_f64(kr[0]), O.bf16_to_f64(vr[0]),
+                                q_pos0 + i, W)
+        assert_attention_close(f64(out[0, i]), o, f"i={i}")
+        assert_lse_close(npy(lse[0, i]), l, f"i={i}")
+    for i in range(3):
+        assert int(cnt[0, i]) == 0
+        assert not f64(out[0, i]).any() and np.all(np.isneginf(npy(lse[0, i])))
+
+
 HCA_CASES = [
     # B, Nq, q_pos0, N, H, d, m, W
     (2, 3, 1021, 1024, 64, 128, 128, 16),
@@ -226,6 +251,8 @@ HCA_CASES = [
     (1, 160, 3840, 4000, 64, 128, 4, 128),   # dense prefill rows: ~9 key chunks per CTA
     (2, 21, 4000, 4200, 4, 64, 128, 128),    # d = 64, 16 tokens per CTA, 2 sequences
     (1, 70, 9000, 9100, 16, 64, 4, 100),     # d = 64, 4 tokens per CTA, ~19 key chunks
+    (1, 300, 3700, 4000, 64, 128, 4, 128),   # persistent CTAs: 2-3 tokens of 8-9 chunks each
+    (1, 400, 0, 400, 64, 128, 4, 0),         # persistent, no window: early tokens see no key
 ]
 
 
