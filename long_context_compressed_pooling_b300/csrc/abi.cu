@@ -250,7 +250,7 @@ csa_status run_index_topk(const uint8_t* qi_codes, const uint8_t* qi_scales,
   csa_status s = run_indexer(qi_codes, qi_scales, ki_codes, ki_scales, B, Nq, q_pos0, E, m, H_I,
                              d_I, sc, nullptr, st, nullptr, fr);
   if (s != CSA_OK) return s;
-  return from_cuda(launch_topk(sc, B, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, st));
+  return from_cuda(launch_topk(sc, B, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, st, true));
 }
 
 // The indexer alone: BF16 scores (and, when scores_f32 is set, the exact FP32 scores).
@@ -481,7 +481,8 @@ static csa_status paged_step(const csa_paged_layer* L, void* ws, cudaStream_t st
     s = run_indexer(L->qi_codes, L->qi_scales, L->ki_codes_pool, L->ki_scales_pool, L->B, 1, t, E,
                     L->m, L->H_I, L->d_I, sc, nullptr, st, &P, fr);
     if (s != CSA_OK) return s;
-    if (launch_topk(sc, L->B, 1, t, E, L->m, L->k, L->topk_idx, L->topk_cnt, st) != cudaSuccess)
+    if (launch_topk(sc, L->B, 1, t, E, L->m, L->k, L->topk_idx, L->topk_cnt, st, true) !=
+        cudaSuccess)
       return CSA_ERR_CUDA;
     a.topk_idx = L->topk_idx;
     a.topk_cnt = L->topk_cnt;

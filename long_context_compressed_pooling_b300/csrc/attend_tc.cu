@@ -183,8 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
   if (!loader) {
     // Q tile of the first item's heads (zero rows past H; Q is an input of this call) and the
     // tensor memory, by the softmax and MMA warps while the loaders' first copies fly
-    const int64_t tok0 = item0 / groups;
-    const int hb0 = (int)(item0 % groups) * kM;
+    const int64_t tok0 = kPersist ? item0 / groups : (int64_t)blockIdx.y;
+    const int hb0 = kPersist ? (int)(item0 % groups) * kM : (int)blockIdx.z * kM;
     const int nt = warp >= kMmaWarp ? (kSoftmaxWarps + warp - kMmaWarp) * 32 + lane
                                     : (int)threadIdx.x;
     for (int x = nt; x < kM * 16; x += kSetupThreads) {
@@ -215,8 +215,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
   const bool dead = (*reinterpret_cast<volatile uint32_t*>(p.status) & kFlagTimeout) != 0;
   auto item_at = [&](int64_t i) {
     Item I;
-    I.tok = i / groups;
-    I.h_base = (int)(i % groups) * kM;
+    if constexpr (kPersist) {
+      I.tok = i / groups;
+      I.h_base = (int)(i % groups) * kM;
+    } else {  // the CTA's one item (64-bit division is emulated: none here)
+      I.tok = blockIdx.y;
+      I.h_base = (int)blockIdx.z * kM;
+    }
     I.b = I.tok / p.Nq;
     I.t = p.q_pos0 + I.tok % p.Nq;
     if (p.sparse) {
@@ -246,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
   const uint32_t o_half = tmem + lane_base + kOCol + (uint32_t)(hf * kD);  // this half's O
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
   bool sm_ok = true;
+  int sm_nloc = 0;  // a softmax warp's chunks of its (last) item
   const int dc = hf * 64;  // a softmax warp's output columns
 
   // The two key halves of an item combined (softmax warps, after both halves' (max, sum) are in
@@ -490,6 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
     int gc = 0;
     for (int64_t ii = item0; ii < n_items; ii += item_step) {
       const Item I = item_at(ii);
+      sm_nloc = I.nloc;
       m0 = -INFINITY;
       m1 = -INFINITY;
       l0 = 0.f;
@@ -658,13 +665,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
 
   __syncthreads();
   if (early) pdl_wait();  // outputs are written only once the predecessor has completed
-  const Item I0 = item_at(item0);
-  const int64_t tok = I0.tok;
-  const int h_base = I0.h_base;
+  const int64_t tok = blockIdx.y;  // the CTA's one item
+  const int h_base = (int)blockIdx.z * kM;
   const bool smx = warp < kSoftmaxWarps;
   uint32_t o[32];
   float M0 = -INFINITY, M1 = -INFINITY, L0 = 0.f, L1 = 0.f;
-  if (smx) combine(sm_ok && I0.nloc > 0, o, M0, M1, L0, L1);
+  if (smx) combine(sm_ok && sm_nloc > 0, o, M0, M1, L0, L1);
   // Every role is done with tensor memory and the pipeline buffers.
   tc_fence_before();
   __syncthreads();

@@ -111,8 +111,11 @@ cudaError_t launch_indexer(const CUtensorMap* kmap, const uint8_t* ki_codes, con
 // fresh) are right for any caller that does not know its predecessor.
 
 // ---- top-k over BF16 scores ------------------------------------------------------------------
+// nonneg: every score is a non-negative BF16 value with zero stored as +0 (the indexer's
+// output), so the selection uses the bit patterns as keys unchanged.
 cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
-                        int k, int32_t* topk_idx, int32_t* topk_cnt, cudaStream_t stream);
+                        int k, int32_t* topk_idx, int32_t* topk_cnt, cudaStream_t stream,
+                        bool nonneg = false);
 // The same selection over FP32 scores [B, Nq, E] (rows of at most 16 x 32768 keys; longer rows
 // return cudaErrorInvalidValue).
 cudaError_t launch_topk_f32(const float* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,

@@ -254,7 +254,9 @@ __global__ void __launch_bounds__(NT) topk_kernel(const uint16_t* __restrict__ s
 // F32: FP32 scores with 32-bit keys. The threshold search runs on the upper 16 bits of the key
 // first (the BF16-truncated score: near-max histogram, else the two-digit radix select), then
 // resolves the keys in that bucket with two more byte digits of the lower half.
-template <int NT, int KPT, bool F32>
+// NN: BF16 scores known to be non-negative with zero stored as +0 (the indexer's ReLU sums):
+// their bit patterns already order like their values and serve as keys unchanged.
+template <int NT, int KPT, bool F32, bool NN = false>
 __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ scores, int Nq,
                                                       int64_t q_pos0, int64_t E, int m, int k,
                                                       int32_t* __restrict__ topk_idx,
@@ -325,13 +327,14 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
       const uint32_t u[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        key[q * 8 + 2 * h] = order_key(u[h] & 0xFFFFu);
-        key[q * 8 + 2 * h + 1] = order_key(u[h] >> 16);
+        key[q * 8 + 2 * h] = NN ? (u[h] & 0xFFFFu) : order_key(u[h] & 0xFFFFu);
+        key[q * 8 + 2 * h + 1] = NN ? (u[h] >> 16) : order_key(u[h] >> 16);
       }
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < KPT; ++j) key[j] = seg0 + j < n ? order_key(src[seg0 + j]) : 0u;
+    for (int j = 0; j < KPT; ++j)
+      key[j] = seg0 + j < n ? (NN ? (uint32_t)src[seg0 + j] : order_key(src[seg0 + j])) : 0u;
   }
   // slots past the row end hold 0 and are excluded by index, never by value
   // ---- row maximum ----
@@ -541,8 +544,8 @@ constexpr int kMaxRegCluster = 16;
 template <int NT, int KPT, bool F32>
 cudaError_t launch_reg(const void* scores, int Nq, int64_t q_pos0, int64_t E, int m, int k,
                        int32_t* topk_idx, int32_t* topk_cnt, int64_t rows, int C,
-                       cudaStream_t stream) {
-  auto kern = topk_reg_kernel<NT, KPT, F32>;
+                       cudaStream_t stream, bool nonneg = false) {
+  auto kern = nonneg && !F32 ? topk_reg_kernel<NT, KPT, F32, true> : topk_reg_kernel<NT, KPT, F32>;
   if (C > 8) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -670,30 +673,31 @@ cudaError_t launch_topk_t(const uint16_t* scores, int Nq, int64_t q_pos0, int64_
 template <bool F32>
 cudaError_t launch_reg_shape(int shape, const void* scores, int Nq, int64_t q_pos0, int64_t E,
                              int m, int k, int32_t* topk_idx, int32_t* topk_cnt, int64_t rows,
-                             int C, cudaStream_t stream) {
+                             int C, cudaStream_t stream, bool nonneg = false) {
   switch (shape) {
     case 0:
       return launch_reg<128, 8, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
-                                     stream);
+                                     stream, nonneg);
     case 1:
       return launch_reg<256, 16, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
-                                      stream);
+                                      stream, nonneg);
     case 2:
       return launch_reg<512, 16, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
-                                      stream);
+                                      stream, nonneg);
     case 3:
       return launch_reg<1024, 16, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
-                                       stream);
+                                       stream, nonneg);
     default:
       return launch_reg<1024, 32, F32>(scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows, C,
-                                       stream);
+                                       stream, nonneg);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, int64_t E, int m,
-                        int k, int32_t* topk_idx, int32_t* topk_cnt, cudaStream_t stream) {
+                        int k, int32_t* topk_idx, int32_t* topk_cnt, cudaStream_t stream,
+                        bool nonneg) {
   const int64_t rows = (int64_t)B * Nq;
   if (rows <= 0) return cudaSuccess;
   int64_t n_max = min(E, (q_pos0 + Nq) / m);
@@ -701,7 +705,7 @@ cudaError_t launch_topk(const uint16_t* scores, int B, int Nq, int64_t q_pos0, i
   int shape = 0, C = 1;
   if (pick_reg(rows, n_max, &shape, &C, false))
     return launch_reg_shape<false>(shape, scores, Nq, q_pos0, E, m, k, topk_idx, topk_cnt, rows,
-                                   C, stream);
+                                   C, stream, nonneg);
   // rows longer than 16 x 32768 keys: clusters of up to 16 CTAs staging their chunks in
   // shared memory
   int Cs = 1;
