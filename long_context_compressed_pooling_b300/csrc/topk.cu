@@ -263,6 +263,7 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
                                                       int32_t* __restrict__ topk_cnt) {
   constexpr int NW = NT / 32;
   constexpr int CS = F32 ? 16 : 0;  // shift from a key to its coarse (16-bit) part
+  static_assert(KPT <= 32, "a thread's selection is a 32-bit mask");
   __shared__ uint32_t whist[NW * 256];
   __shared__ uint32_t hist1[256], hist2[256], gsum[256];
   __shared__ __align__(16) uint32_t wmax[NW];
@@ -484,9 +485,14 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
   uint32_t gt = 0u, eq = 0u;
 #pragma unroll
   for (int j = 0; j < KPT; ++j) {
-    const bool ok = seg0 + j < n;
-    gt |= (ok && key[j] > T) ? (1u << j) : 0u;
-    eq |= (ok && key[j] == T) ? (1u << j) : 0u;
+    gt |= key[j] > T ? (1u << j) : 0u;
+    eq |= key[j] == T ? (1u << j) : 0u;
+  }
+  {  // keys past the row end are dropped by position
+    const int nv = n - seg0;
+    const uint32_t valid = nv >= 32 ? 0xFFFFFFFFu : nv <= 0 ? 0u : (1u << nv) - 1u;
+    gt &= valid;
+    eq &= valid;
   }
   uint32_t gb, eb, tg, te;
   block_scan2((uint32_t)__popc(gt), (uint32_t)__popc(eq), &gb, &eb, &tg, &te, wa, wb);
