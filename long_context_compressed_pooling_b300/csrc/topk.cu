@@ -371,10 +371,20 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
   // straight into one block histogram (whist's first 256 words), which needs no per-warp sum.
   uint32_t* const nh = C == 1 ? whist : wh;
   const uint32_t max_c = row_max >> CS;  // coarse parts of keys and maximum
+  // slots past the row end hold key 0, which lies in the window only when the maximum does
+  // (max_c < 255): otherwise no test of the position is needed
+  if (max_c >= 255u || seg0 + KPT <= n) {
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const uint32_t dd = max_c - (key[j] >> CS);
-    if (dd < 255u && seg0 + j < n) atomicAdd(&nh[dd], 1u);
+    for (int j = 0; j < KPT; ++j) {
+      const uint32_t dd = max_c - (key[j] >> CS);
+      if (dd < 255u) atomicAdd(&nh[dd], 1u);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const uint32_t dd = max_c - (key[j] >> CS);
+      if (dd < 255u && seg0 + j < n) atomicAdd(&nh[dd], 1u);
+    }
   }
   __syncthreads();
   auto sum_hist = [&](uint32_t* hist) {  // per-warp histograms -> hist -> cluster sum in gsum
@@ -400,9 +410,18 @@ __global__ void __launch_bounds__(NT) topk_reg_kernel(const void* __restrict__ s
       sum_hist(hist);
     }
   };
-  sum_near(hist1);
-  select_prefix(gsum, (uint32_t)k, &sh_bin, &sh_above);
-  __syncthreads();
+  if (C == 1) {
+    select_prefix(whist, (uint32_t)k, &sh_bin, &sh_above);  // the block histogram in place
+    __syncthreads();
+    if (F32 || sh_bin < 0) {  // the searches below count into whist again
+      for (int q = tid; q < 256; q += NT) whist[q] = 0u;
+      __syncthreads();
+    }
+  } else {
+    sum_hist(hist1);
+    select_prefix(gsum, (uint32_t)k, &sh_bin, &sh_above);
+    __syncthreads();
+  }
   uint32_t Tc, above_c;  // coarse threshold and the count of keys whose coarse part exceeds it
   if (sh_bin >= 0) {
     Tc = max_c - (uint32_t)sh_bin;
