@@ -534,11 +534,12 @@ __global__ void __launch_bounds__(threads_for(EW)) indexer_kernel(const __grid_c
               for (int cc = 0; cc < 16; cc += CPQ) {
                 const int ql = (c * 16 + cc) / CPQ;
                 if (ql < nq) {
-                  // column (query, head) holds the head's exact scaled dot product
-                  float sc = 0.f;
+                  // column (query, head) holds the head's exact scaled dot product; the ReLU
+                  // acts on the bit patterns (negative values and -0 become +0), so the sum of
+                  // the non-negative terms is never -0 (the terms are exact: any order)
+                  float sc = __int_as_float(max((int)r[k][cc], 0));
 #pragma unroll
-                  for (int h = 0; h < H_I; ++h) sc += fmaxf(__uint_as_float(r[k][cc + h]), 0.f);
-                  sc += 0.0f;  // -0 -> +0
+                  for (int h = 1; h < H_I; ++h) sc += __int_as_float(max((int)r[k][cc + h], 0));
                   if (all_vis || j < qvis[ql]) {
                     srow[(int64_t)ql * p.E] = f32_to_bf16_bits(sc);
                     if constexpr (F32OUT)
