@@ -4,12 +4,17 @@ ABI) with the fp64 oracle.
 The conversion from bf16 values is integer work and is compared bit for bit. The pooled index
 key is rounded to bf16 from the kernel's fp32 sum and from the oracle's fp64 sum; the two can
 differ where the exact pooled value lies within the fp32 error of a bf16 rounding boundary. The
-kernel's fp32 error is bounded by its arithmetic, with u = 2^-24 and A the largest distance of
-a block's logit from its maximum: the weights exp(w_i - max) carry (A + 2) u from the rounded
-argument and expf, the sum of m of them (m - 1) u more, the reciprocal and the weight product
-2 u, and the m fused multiply-adds m u of sum_i p_i |x_i|; in all below
-(2m + 20 + A) u sum_i p_i |x_i|. An element whose exact value +- that bound rounds to another
-bf16 value is ambiguous. Every other element must match exactly: a block without an ambiguous
+kernel's fp32 error is bounded by its arithmetic (IEEE division, expf within 2 ulp), to first
+order in u = 2^-24, with A the largest distance of a block's logit from its maximum and
+L = ceil(log2 m):
+  - e_i = expf(fl(w_i - max)): the rounded argument gives A u, expf's 2 ulp 4 u (relative);
+  - the sum of the m weights over a shuffle tree: every weight passes at most L roundings
+    (partners beyond the m lanes add exact zeros), so the sum carries (4 + A + L) u;
+  - the reciprocal and the product e_i * (1 / sum): 2 u; each p_i is within (10 + 2A + L) u;
+  - the m fused multiply-adds of sum_i p_i x_i: m u of sum_i p_i |x_i|.
+In all |kernel - exact| <= (m + L + 10 + 2A) u sum_i p_i |x_i|; the test allows one u more for
+the second-order terms. An element whose exact value +- that bound rounds to another bf16 value
+is ambiguous. Every other element must match exactly: a block without an ambiguous
 element is compared bit for bit, and a block with one must equal the conversion of some
 admissible choice of its ambiguous elements, the rest fixed. The tests also require ambiguous
 elements to stay rare (a few percent), so the comparison is exact almost everywhere."""
@@ -105,7 +110,8 @@ def _check_seq_keys(codes_g, scales_g, xi_bits, logits, m, j0, j1, what):
     a = np.abs(w - w.max(axis=1, keepdims=True)).max(axis=1)
     p = O.pooling_weights(w)
     mag = np.einsum("ji,jid->jd", p, np.abs(O.bf16_to_f64(xi_bits)[: E * m].reshape(E, m, d)))
-    delta = ((2 * m + 20 + a) * U)[:, None] * mag
+    L = int(np.ceil(np.log2(m))) if m > 1 else 0
+    delta = ((m + L + 11 + 2 * a) * U)[:, None] * mag
     lo = O.f64_to_bf16_rne_any(pooled - delta)
     hi = O.f64_to_bf16_rne_any(pooled + delta)
     amb = (lo != pb_o) | (hi != pb_o)                      # [E, d]
