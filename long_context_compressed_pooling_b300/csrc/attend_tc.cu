@@ -160,7 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
   const int groups = (p.H + kM - 1) / kM;
   const int64_t n_items = (int64_t)p.tokens * groups;
   const int64_t item0 = kPersist ? (int64_t)blockIdx.y : (int64_t)blockIdx.y * groups + blockIdx.z;
-  const int64_t item_step = kPersist ? (int64_t)gridDim.y : n_items;  // else: one item
+  // a non-persistent CTA's loops run once, over item0, as the compiler can see
+  const int64_t item_step = kPersist ? (int64_t)gridDim.y : 1;
+  const int64_t item_end = kPersist ? n_items : item0 + 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
     bool waited = !early;
     bool run = true;
     int gc = 0;  // this CTA's chunks so far, over all its items
-    for (int64_t ii = item0; ii < n_items && run; ii += item_step) {
+    for (int64_t ii = item0; ii < item_end && run; ii += item_step) {
       const Item I = item_at(ii);
       for (int it = 0; it < I.nloc; ++it, ++gc) {
         const int s = gc % kStages;
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
     bool run = true;
     int gc = 0;
     int64_t q_item = item0;  // the item whose Q tile is in shared memory
-    for (int64_t ii = item0; ii < n_items && run; ii += item_step) {
+    for (int64_t ii = item0; ii < item_end && run; ii += item_step) {
       const Item I = item_at(ii);
       if constexpr (kPersist) {
         const int64_t nx = ii + item_step;
@@ -453,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
     const uint32_t id_pv = idesc_bf16(kM, kD, false, true);
     bool run = true;
     int gc = 0, nprev = 0;  // chunks so far; items with chunks so far
-    for (int64_t ii = item0; ii < n_items && run; ii += item_step) {
+    for (int64_t ii = item0; ii < item_end && run; ii += item_step) {
       const Item I = item_at(ii);
       // the first PV of an item overwrites O: the softmax warps have read the previous one's
       if (kPersist && I.nloc > 0 && nprev > 0 &&
@@ -494,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
     // Keys [64 hf, 64 hf + 64) of every chunk, with their own running maximum and sum; the two
     // key halves accumulate into separate O accumulators that are combined at the end.
     int gc = 0;
-    for (int64_t ii = item0; ii < n_items; ii += item_step) {
+    for (int64_t ii = item0; ii < item_end; ii += item_step) {
       const Item I = item_at(ii);
       sm_nloc = I.nloc;
       m0 = -INFINITY;
