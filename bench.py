@@ -727,6 +727,7 @@ def run_e2e(wl, states, call, flush, K, dev, world, barrier, index_keys=False):
     pinned host memory, runs the layer pair, and reads the outputs back."""
     import torch
     import torch.distributed as dist
+    import long_context_compressed_pooling_b300 as csa
     # The step's new inputs travel packed in one pinned host buffer (one upload per step) into a
     # device staging buffer, from which they are placed into the layer buffers on the device.
     views, off = [], 0
@@ -749,8 +750,9 @@ def run_e2e(wl, states, call, flush, K, dev, world, barrier, index_keys=False):
     ups = [(view, dbuf[o:o + nb].view(view.dtype).view(view.shape)) for view, o, nb in views]
     def step():
         dbuf.copy_(hbuf, non_blocking=True)
-        for dv, staged in ups:
-            dv.copy_(staged)
+        # the staged rows into the layer buffers: csa_scatter_rows, one launch per 16 views
+        for i in range(0, len(ups), csa.MAX_COPIES):
+            csa.scatter_rows(ups[i:i + csa.MAX_COPIES])
         call()
         for dv, h in downs:
             h.copy_(dv, non_blocking=True)
@@ -758,7 +760,8 @@ def run_e2e(wl, states, call, flush, K, dev, world, barrier, index_keys=False):
     # The step (uploads from pinned memory, the layer-pair call, the download) is captured once
     # into a CUDA graph and replayed: every replay moves the bytes over the bus again, without the
     # host's per-call launch cost. Eager launches if the capture is refused.
-    api = "csa_hca_layer_pair with one packed pinned-host upload and the download (CUDA graph replay)"
+    api = ("csa_hca_layer_pair with one packed pinned-host upload placed by csa_scatter_rows, "
+           "and the download (CUDA graph replay)")
     run = step
     try:
         side = torch.cuda.Stream(device=dev)
@@ -773,7 +776,8 @@ def run_e2e(wl, states, call, flush, K, dev, world, barrier, index_keys=False):
         torch.cuda.synchronize()
         run = g.replay
     except Exception as e:  # keep eager launches
-        api = "csa_hca_layer_pair with one packed pinned-host upload and the download (eager launches)"
+        api = ("csa_hca_layer_pair with one packed pinned-host upload placed by csa_scatter_rows, "
+               "and the download (eager launches)")
         print(f"# e2e graph capture unavailable, launching eagerly: {e}", file=sys.stderr)
     e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]

@@ -404,6 +404,30 @@ csa_status csa_lse_merge(const uint16_t* parts, const float* parts_lse, int S, i
 csa_status csa_test_set_faults(long long wait_budget_cycles, uint32_t skip_mask);
 
 /* ----------------------------------------------------------------------------------------
+ * Batched row copies on the device (data movement of a serving loop; no counterpart on the
+ * pages). A step's new inputs can travel host-to-device as one packed upload into a staging
+ * buffer; this call then places them into the layer buffers in one launch. Copy i moves
+ * rows rows of row_bytes bytes each from src (rows packed: row r at src + r * row_bytes) to dst
+ * (row r at dst + r * dst_stride). dst and src are device pointers; descs is a host array of
+ * n <= CSA_MAX_COPIES descriptors, read before the call returns. Copies must not overlap one
+ * another or their sources. Rows move 16 bytes at a time when a copy's pointers, row_bytes and
+ * dst_stride are multiples of 16. The launch signals no dependent kernel before it completes,
+ * so a library call enqueued after it on the same stream reads the placed rows.
+ * Errors: CSA_ERR_INVALID_ARG for descs == NULL with n > 0, n < 0 or n > CSA_MAX_COPIES,
+ * negative rows / row_bytes, dst_stride < row_bytes with rows > 1, or a null pointer in a
+ * copy that moves bytes; CSA_ERR_CUDA if the launch fails.
+ * ---------------------------------------------------------------------------------------- */
+#define CSA_MAX_COPIES 16
+typedef struct csa_copy_desc {
+  void* dst;
+  const void* src;
+  int64_t rows;
+  int64_t row_bytes;
+  int64_t dst_stride;
+} csa_copy_desc;
+csa_status csa_scatter_rows(const csa_copy_desc* descs, int n, void* stream);
+
+/* ----------------------------------------------------------------------------------------
  * Per-kernel timing (tracing aid; no counterpart on the pages). While enabled, every kernel
  * launch of the library is bracketed by two CUDA events recorded on its launch stream.
  * csa_profiler_collect synchronises those events and returns, per kernel name, the number of

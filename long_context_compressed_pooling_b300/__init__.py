@@ -12,6 +12,7 @@ from ._native import (  # noqa: F401
     CsaError,
     FAULT_SKIP_KEY_COPIES,
     LIB_PATH,
+    MAX_COPIES,
     PAGE_TOKENS,
     PreparedLayerPair,
     PreparedPagedPair,
@@ -28,6 +29,7 @@ from ._native import (  # noqa: F401
     layer_pair,
     lse_merge,
     load_library,
+    scatter_rows,
     paged_decode_step,
     profiler_collect,
     profiler_enable,

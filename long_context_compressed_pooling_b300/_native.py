@@ -69,6 +69,13 @@ class KernelTime(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 32), ("launches", _I), ("total_ms", ctypes.c_double)]
 
 
+class CopyDesc(ctypes.Structure):
+    _fields_ = [("dst", _P), ("src", _P), ("rows", _L), ("row_bytes", _L), ("dst_stride", _L)]
+
+
+MAX_COPIES = 16
+
+
 _SIGS = {
     "csa_profiler_enable": (_I, [_I]),
     "csa_profiler_collect": (_I, [ctypes.POINTER(KernelTime), _I, ctypes.POINTER(_I), _I]),
@@ -106,6 +113,7 @@ _SIGS = {
     "csa_topk_merge": (_I, [_P, _P, _P, ctypes.POINTER(ctypes.c_int64), _I, _I, _I, _P, _P, _P,
                             _P, _P]),
     "csa_lse_merge": (_I, [_P, _P, _I, _L, _I, _P, _P, _P]),
+    "csa_scatter_rows": (_I, [ctypes.POINTER(CopyDesc), _I, _P]),
 }
 
 _lib: Optional[ctypes.CDLL] = None
@@ -527,6 +535,47 @@ def lse_merge(parts, parts_lse, out=None, lse=None, want_lse: bool = False):
     _check("csa_lse_merge", lib.csa_lse_merge(_ptr(_u16(parts)), _ptr(parts_lse), S, rows, d,
                                               _ptr(out), _ptr(lse), _stream(dev)))
     return out, lse
+
+
+def _rows_view(t: torch.Tensor):
+    """(rows, row_bytes, row_stride_bytes) of a device view whose dimensions after the first
+    are contiguous (a whole tensor, or a slice of the second dimension of [B, N, ...])."""
+    if not t.is_cuda:
+        raise ValueError("tensors must live on the CUDA device")
+    es = t.element_size()
+    if t.is_contiguous():
+        return 1, t.numel() * es, t.numel() * es
+    inner = t.shape[1:]
+    want, acc = [], 1
+    for n in reversed(inner):
+        want.append(acc)
+        acc *= n
+    if t.dim() < 2 or list(t.stride()[1:]) != list(reversed(want)):
+        raise ValueError("the view's rows (dimensions after the first) must be contiguous")
+    return t.shape[0], acc * es, t.stride(0) * es
+
+
+def scatter_rows(pairs) -> None:
+    """Copy each (dst, src) pair on the device in one launch (csa_scatter_rows): dst a view
+    whose dimensions after the first are contiguous (rows strided by its first dimension), src a
+    contiguous tensor of the same shape and dtype (rows packed), e.g. slices of one staging
+    buffer that a single host-to-device copy filled. At most MAX_COPIES pairs per call."""
+    pairs = list(pairs)
+    if len(pairs) > MAX_COPIES:
+        raise ValueError(f"at most {MAX_COPIES} copies per call")
+    descs = (CopyDesc * max(1, len(pairs)))()
+    dev = None
+    for i, (dst, src) in enumerate(pairs):
+        if dst.shape != src.shape or dst.dtype != src.dtype:
+            raise ValueError("each source must match its destination's shape and dtype")
+        rows, row_bytes, stride = _rows_view(dst)
+        descs[i].dst = dst.data_ptr()
+        descs[i].src = _ptr(src).value
+        descs[i].rows, descs[i].row_bytes, descs[i].dst_stride = rows, row_bytes, stride
+        dev = dst.device
+    if dev is None:
+        return
+    _check("csa_scatter_rows", load_library().csa_scatter_rows(descs, len(pairs), _stream(dev)))
 
 
 FAULT_SKIP_KEY_COPIES = 0x1

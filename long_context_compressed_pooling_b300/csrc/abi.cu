@@ -553,6 +553,22 @@ csa_status csa_lse_merge(const uint16_t* parts, const float* parts_lse, int S, i
                                     static_cast<cudaStream_t>(stream)));
 }
 
+csa_status csa_scatter_rows(const csa_copy_desc* descs, int n, void* stream) {
+  if (n < 0 || n > CSA_MAX_COPIES || (n > 0 && !descs)) return CSA_ERR_INVALID_ARG;
+  static_assert(CSA_MAX_COPIES == kMaxScatterCopies, "copy limits agree");
+  ScatterCopy c[kMaxScatterCopies];
+  int m = 0;
+  for (int i = 0; i < n; ++i) {
+    const csa_copy_desc& d = descs[i];
+    if (d.rows < 0 || d.row_bytes < 0 || (d.rows > 1 && d.dst_stride < d.row_bytes))
+      return CSA_ERR_INVALID_ARG;
+    if (d.rows == 0 || d.row_bytes == 0) continue;
+    if (!d.dst || !d.src) return CSA_ERR_INVALID_ARG;
+    c[m++] = ScatterCopy{d.dst, d.src, d.rows, d.row_bytes, d.dst_stride};
+  }
+  return from_cuda(launch_scatter_rows(c, m, static_cast<cudaStream_t>(stream)));
+}
+
 int csa_abi_version(void) { return 3; }
 
 csa_status csa_test_set_faults(long long wait_budget_cycles, uint32_t skip_mask) {

@@ -171,6 +171,16 @@ cudaError_t launch_topk_merge(const uint16_t* cand_scores, const int32_t* cand_i
 cudaError_t launch_lse_merge(const uint16_t* parts, const float* lse, int S, int64_t rows, int d,
                              uint16_t* out, float* lse_out, cudaStream_t stream);
 
+// ---- batched row copies (stage.cu): a step's staged inputs into the layer buffers ----
+constexpr int kMaxScatterCopies = 16;
+struct ScatterCopy {
+  void* dst;           // row r at dst + r * dst_stride
+  const void* src;     // row r at src + r * row_bytes (rows packed)
+  int64_t rows, row_bytes, dst_stride;
+};
+// n <= kMaxScatterCopies copies (validated by the caller) in one launch.
+cudaError_t launch_scatter_rows(const ScatterCopy* copies, int n, cudaStream_t stream);
+
 // ---- fused CSA decode step (decode.cu): indexer + top-k (+ sparse attention) in one launch ----
 constexpr int kDecodeMaxCluster = 16;   // CTAs per sequence
 constexpr int kDecodeMaxChunk = 16384;  // entries one CTA scores (BF16 scores kept on chip)

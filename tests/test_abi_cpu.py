@@ -218,3 +218,19 @@ def test_sharded_calls_validate_before_launching(lib):
     assert lib.csa_lse_merge(a, a, 2, 10, 60, a, None, None) == 5              # d % 8
     assert lib.csa_lse_merge(a, a, 0, 10, 64, a, None, None) == 1
     assert lib.csa_shard_candidates_workspace_size(2, 1000, 64) == 4096
+
+
+def test_scatter_rows_validates_before_launching(lib):
+    # host-only: every refused call returns before touching CUDA; copies that move no byte are
+    # dropped, so a call made of them launches nothing
+    a = _p(ALN)
+    D = N.CopyDesc
+    assert lib.csa_scatter_rows(None, 1, None) == 1                    # no descriptors
+    assert lib.csa_scatter_rows((D * 1)(), -1, None) == 1              # negative count
+    assert lib.csa_scatter_rows((D * 17)(), 17, None) == 1             # above CSA_MAX_COPIES
+    assert lib.csa_scatter_rows((D * 1)(D(a, a, -1, 16, 16)), 1, None) == 1   # negative rows
+    assert lib.csa_scatter_rows((D * 1)(D(a, a, 2, 32, 16)), 1, None) == 1    # stride < row
+    assert lib.csa_scatter_rows((D * 1)(D(None, a, 2, 16, 16)), 1, None) == 1  # null dst
+    assert lib.csa_scatter_rows((D * 2)(D(None, None, 0, 16, 16), D(None, None, 3, 0, 0)), 2,
+                                None) == 0                             # nothing to move
+    assert lib.csa_scatter_rows(None, 0, None) == 0
