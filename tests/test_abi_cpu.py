@@ -198,6 +198,9 @@ def test_host_tensors_are_refused(lib):
         csa.topk_f32(s.float(), 7, 1, 2)
     with pytest.raises(ValueError, match="CUDA device"):
         csa.quantize_mxfp4(torch.zeros((4, 64), dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="CUDA device"):
+        z = torch.zeros((2, 8), dtype=torch.bfloat16)
+        csa.scatter_rows([(z, z.clone())])
 
 
 def test_fault_injection_switches_are_validated_and_restorable(lib):
