@@ -386,8 +386,14 @@ def step_inputs(s, d):
     return items
 
 
-def kernel_sha(name):
-    src = os.path.join(ROOT, "long_context_compressed_pooling_b300", "csrc", KERNEL_SOURCES[name])
+# The indexer of a decode step outside the one-launch kernel (one query per sequence, e.g. the
+# 1M-context pair) is that kernel's scores-only mode: its source is decode.cu.
+KERNEL_SOURCES_BY_WORKLOAD = {("pair_decode_1m", "indexer_mxf4"): "decode.cu"}
+
+
+def kernel_sha(name, workload=None):
+    fname = KERNEL_SOURCES_BY_WORKLOAD.get((workload, name), KERNEL_SOURCES[name])
+    src = os.path.join(ROOT, "long_context_compressed_pooling_b300", "csrc", fname)
     with open(src, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
@@ -400,7 +406,7 @@ def load_traffic(name, workload):
         with open(p) as f:
             tab = json.load(f)
         e = tab[workload][name]
-        if e.get("source_sha") == kernel_sha(name):
+        if e.get("source_sha") == kernel_sha(name, workload):
             return e["dram_bytes_per_launch"]
     except Exception:
         pass
