@@ -388,7 +388,10 @@ def step_inputs(s, d):
 
 # The indexer of a decode step outside the one-launch kernel (one query per sequence, e.g. the
 # 1M-context pair) is that kernel's scores-only mode: its source is decode.cu.
-KERNEL_SOURCES_BY_WORKLOAD = {("pair_decode_1m", "indexer_mxf4"): "decode.cu"}
+# Head dim 64 prefill (the small pair) attends in the packed kernel of attend_pk.cu.
+KERNEL_SOURCES_BY_WORKLOAD = {("pair_decode_1m", "indexer_mxf4"): "decode.cu",
+                              ("tiny_pair_prefill_2k", "csa_attend"): "attend_pk.cu",
+                              ("tiny_pair_prefill_2k", "hca_attend"): "attend_pk.cu"}
 
 
 def kernel_sha(name, workload=None):
